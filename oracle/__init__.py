@@ -1,0 +1,376 @@
+"""CPU oracle for the preshuffle GEMM  C[M,N] = A[M,K] . B[N,K]^T.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and
+``bench.py``'s ``cpu_baseline`` leg may import this package.  It shares no
+code with the CUDA path and imports nothing from it.  The two meet only in
+the seeded input generator (``dense_gemm_preshuffle_gb300.inputs``), which
+holds no GEMM arithmetic.
+
+Contents:
+
+* Codecs written from the format definitions:
+  - E4M3FN (OCP 8-bit floating point spec: bias 7, no infinities, S.1111.111
+    is NaN)
+  - E2M1 and UE8M0 (OCP Microscaling formats v1.0)
+  - BF16 (the upper half of an IEEE binary32)
+* GEMMs in fp64 / int64.  The triple loops live in ``gemm_oracle.c``, built
+  by ``oracle/build.py``:
+  - INT8: C = sum_k a*b, exact in int64.
+  - BF16: C = sum_k a*b, fp64.
+  - E4M3 with per-row/per-column fp32 scales: C = (sum_k qa*qb) * sa[m] * sb[n].
+    "GEMM Optimization Guide", section 7.1 (direct store): the epilogue forms
+    acc * scale_a * scale_b.  Every E4M3 product is a multiple of 2^-18 and
+    |sum| < K*448^2 < 2^31, so the fp64 sum is exact.
+  - MXFP4: C = sum_j 2^(ea[m,j]-127) 2^(eb[n,j]-127) sum_{k in block j} qa*qb.
+    Same guide, section 8.2: one UE8M0 byte per 32 K-elements of each
+    operand.
+* The packed-B layout model used to check the device packer byte by byte.
+  The layout is this library's own, not the one the guide prints.
+* Tile bookkeeping from the guide: section 1.2 (derived tile parameters),
+  section 1.5 (MFMA count per tile), sections 8.1-8.2 (flops, bytes moved) and
+  section 14 (worked example).
+* The float parity metric max |C - C_ref| / (|C_ref| + 1e-2).
+
+Parity pins (tests/test_oracle.py): brute force in exact rational arithmetic,
+identity and permutation operands, library decodes (torch float8/bfloat16),
+the guide's printed worked numbers (tests/golden/), and round trips of the
+pack model.  No function here is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import time
+from typing import Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "_lib", "liboracle.so")
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        from . import build as _b
+        _b.build()
+    lib = ctypes.CDLL(_LIB_PATH)
+    i64 = ctypes.c_int64
+    vp = ctypes.c_void_p
+    lib.oracle_gemm_i8_i64.argtypes = [vp, vp, i64, i64, i64, vp]
+    lib.oracle_gemm_f64.argtypes = [vp, vp, i64, i64, i64, vp]
+    lib.oracle_gemm_block_f64.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, vp]
+    lib.oracle_num_threads.restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def num_threads() -> int:
+    return int(_load().oracle_num_threads())
+
+
+def _p(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+# ----------------------------------------------------------------------------
+# Codecs (decode only; the oracle never needs to encode)
+# ----------------------------------------------------------------------------
+
+def decode_e4m3(codes: np.ndarray) -> np.ndarray:
+    """E4M3FN code -> value (fp64).  Layout s.eeee.mmm, exponent bias 7.
+
+    e == 0  : subnormal, (-1)^s * 2^-6 * m/8
+    e  > 0  : normal,    (-1)^s * 2^(e-7) * (1 + m/8)
+    e == 15 and m == 7 : NaN (E4M3FN has no infinities).
+    """
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    s = (c >> 7) & 1
+    e = (c >> 3) & 0xF
+    m = c & 0x7
+    mag = np.where(e == 0, np.ldexp(m / 8.0, -6), np.ldexp(1.0 + m / 8.0, e - 7))
+    val = np.where(s == 1, -mag, mag)
+    return np.where((e == 15) & (m == 7), np.nan, val)
+
+
+def decode_e2m1(codes: np.ndarray) -> np.ndarray:
+    """E2M1 code (low 4 bits) -> value (fp64).  Layout s.ee.m, exponent bias 1.
+
+    e == 0 : subnormal, (-1)^s * 0.5 * m
+    e  > 0 : normal,    (-1)^s * 2^(e-1) * (1 + m/2)
+    """
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64) & 0xF
+    s = (c >> 3) & 1
+    e = (c >> 1) & 0x3
+    m = c & 0x1
+    mag = np.where(e == 0, 0.5 * m, np.ldexp(1.0 + m / 2.0, e - 1))
+    return np.where(s == 1, -mag, mag)
+
+
+def decode_ue8m0(codes: np.ndarray) -> np.ndarray:
+    """UE8M0 scale byte -> 2^(code - 127) (fp64); 0xFF is NaN."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    return np.where(c == 255, np.nan, np.ldexp(1.0, c - 127))
+
+
+def decode_bf16(bits: np.ndarray) -> np.ndarray:
+    """BF16 bit pattern -> value (fp64): the upper 16 bits of a binary32."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32).astype(np.float64)
+
+
+def unpack_e2m1_rows(packed: np.ndarray, K: int) -> np.ndarray:
+    """[rows, K/2] bytes (low nibble = even k) -> [rows, K] codes."""
+    p = np.asarray(packed, dtype=np.uint8)
+    out = np.empty((p.shape[0], K), dtype=np.uint8)
+    out[:, 0::2] = p & 0xF
+    out[:, 1::2] = p >> 4
+    return out
+
+
+# ----------------------------------------------------------------------------
+# GEMMs.  All return the exact (unrounded) fp64 result, or int64 for INT8.
+# ----------------------------------------------------------------------------
+
+def gemm_int8(a: np.ndarray, b: np.ndarray) -> np.ndarray:
+    """C = A . B^T for int8 A [M,K], B [N,K]; int64 result."""
+    a = np.ascontiguousarray(a, dtype=np.int8)
+    b = np.ascontiguousarray(b, dtype=np.int8)
+    M, K = a.shape
+    N = b.shape[0]
+    c = np.empty((M, N), dtype=np.int64)
+    _load().oracle_gemm_i8_i64(_p(a), _p(b), M, N, K, _p(c))
+    return c
+
+
+def gemm_f64(a: np.ndarray, b: np.ndarray) -> np.ndarray:
+    """C = A . B^T for already-decoded fp64 A [M,K], B [N,K]."""
+    a = np.ascontiguousarray(a, dtype=np.float64)
+    b = np.ascontiguousarray(b, dtype=np.float64)
+    M, K = a.shape
+    N = b.shape[0]
+    c = np.empty((M, N), dtype=np.float64)
+    _load().oracle_gemm_f64(_p(a), _p(b), M, N, K, _p(c))
+    return c
+
+
+def gemm_bf16(a_bits: np.ndarray, b_bits: np.ndarray) -> np.ndarray:
+    return gemm_f64(decode_bf16(a_bits), decode_bf16(b_bits))
+
+
+def gemm_e4m3_rowcol(qa: np.ndarray, qb: np.ndarray, sa: np.ndarray, sb: np.ndarray) -> np.ndarray:
+    """C[m,n] = (sum_k qa[m,k] qb[n,k]) * sa[m] * sb[n]: the accumulator is
+    scaled by the row scale of A and the column scale (row of B)."""
+    acc = gemm_f64(decode_e4m3(qa), decode_e4m3(qb))
+    return acc * np.asarray(sa, np.float64)[:, None] * np.asarray(sb, np.float64)[None, :]
+
+
+def gemm_mxfp4(pa: np.ndarray, pb: np.ndarray, ea: np.ndarray, eb: np.ndarray, K: int) -> np.ndarray:
+    """MXFP4 product: packed E2M1 [rows, K/2] with UE8M0 [rows, K/32]."""
+    a = np.ascontiguousarray(decode_e2m1(unpack_e2m1_rows(pa, K)))
+    b = np.ascontiguousarray(decode_e2m1(unpack_e2m1_rows(pb, K)))
+    sa = np.ascontiguousarray(decode_ue8m0(ea))
+    sb = np.ascontiguousarray(decode_ue8m0(eb))
+    M, N = a.shape[0], b.shape[0]
+    c = np.empty((M, N), dtype=np.float64)
+    _load().oracle_gemm_block_f64(_p(a), _p(b), _p(sa), _p(sb), M, N, K, 32, _p(c))
+    return c
+
+
+def gemm_operands(ops, rows: Optional[np.ndarray] = None, cols: Optional[np.ndarray] = None) -> np.ndarray:
+    """Reference C for an ``Operands`` bundle, optionally restricted to the
+    given output rows (of A) and columns (rows of B)."""
+    a, b, sa, sb = ops.a, ops.b, ops.scale_a, ops.scale_b
+    if rows is not None:
+        a = a[rows]
+        sa = None if sa is None else sa[rows]
+    if cols is not None:
+        b = b[cols]
+        sb = None if sb is None else sb[cols]
+    if ops.dtype == "int8":
+        return gemm_int8(a, b)
+    if ops.dtype == "bf16":
+        return gemm_bf16(a, b)
+    if ops.dtype == "e4m3":
+        return gemm_e4m3_rowcol(a, b, sa, sb)
+    if ops.dtype == "e2m1":
+        return gemm_mxfp4(a, b, sa, sb, ops.K)
+    raise ValueError(ops.dtype)
+
+
+# ----------------------------------------------------------------------------
+# Output rounding model and the parity metric
+# ----------------------------------------------------------------------------
+
+def max_rel_err(c: np.ndarray, c_ref: np.ndarray) -> float:
+    """max over all elements of |C - C_ref| / (|C_ref| + 1e-2)."""
+    c = np.asarray(c, np.float64)
+    r = np.asarray(c_ref, np.float64)
+    if c.size == 0:
+        return 0.0
+    return float(np.max(np.abs(c - r) / (np.abs(r) + 1e-2)))
+
+
+FLOAT_TOL = 8e-3
+
+
+# ----------------------------------------------------------------------------
+# Packed-B layout model (this library's own layout)
+#
+# B is a byte matrix [N, Kb] (Kb = K * element bytes; E2M1 packs two per
+# byte).  It is cut into tiles of 128 rows x 128 bytes; tile (tn, tk) is
+# stored at tile index tn * (Kb/128) + tk, i.e. all K-tiles of one 128-row
+# band are contiguous.  Inside a tile, row r occupies 128 bytes at r*128 and
+# its eight 16-byte chunks are permuted: chunk c of the row is stored at
+# chunk position c XOR (r mod 8).
+# ----------------------------------------------------------------------------
+
+TILE_ROWS = 128
+TILE_BYTES = 128
+
+
+def elem_bits(dtype: str) -> int:
+    return {"bf16": 16, "e4m3": 8, "int8": 8, "e2m1": 4}[dtype]
+
+
+def packed_offset(n: np.ndarray, kb: np.ndarray, Kb: int) -> np.ndarray:
+    """Byte offset in the packed buffer of byte (n, kb) of B."""
+    n = np.asarray(n, np.int64)
+    kb = np.asarray(kb, np.int64)
+    tiles_k = Kb // TILE_BYTES
+    tn, r = n // TILE_ROWS, n % TILE_ROWS
+    tk, col = kb // TILE_BYTES, kb % TILE_BYTES
+    chunk, byte = col // 16, col % 16
+    tile_index = tn * tiles_k + tk
+    return tile_index * (TILE_ROWS * TILE_BYTES) + r * TILE_BYTES + ((chunk ^ (r % 8)) * 16) + byte
+
+
+def pack_b_bytes(b_bytes: np.ndarray) -> np.ndarray:
+    """Scatter every byte of B [N, Kb] to its packed offset."""
+    b = np.ascontiguousarray(b_bytes).view(np.uint8)
+    N, Kb = b.shape
+    nn, kk = np.meshgrid(np.arange(N), np.arange(Kb), indexing="ij")
+    out = np.zeros(N * Kb, dtype=np.uint8)
+    out[packed_offset(nn, kk, Kb).ravel()] = b.ravel()
+    return out
+
+
+def unpack_b_bytes(packed: np.ndarray, N: int, Kb: int) -> np.ndarray:
+    """Gather B [N, Kb] back from the packed buffer."""
+    nn, kk = np.meshgrid(np.arange(N), np.arange(Kb), indexing="ij")
+    return np.asarray(packed, np.uint8)[packed_offset(nn, kk, Kb)]
+
+
+# Block scales of an MXFP4 B ([N, K/32] UE8M0) are packed per (128-row band,
+# 128-byte K tile) = 128 rows x 8 scale bytes, in two 512-byte groups of four
+# K-blocks.  Inside a group, the byte of (row r, block j) is at
+# (r % 32) * 16 + (r // 32) * 4 + (j % 4).  The scale region follows the data
+# region in the same buffer.
+
+def packed_scale_offset(n: np.ndarray, j: np.ndarray, nblk: int) -> np.ndarray:
+    """Offset (within the scale region) of the scale of (row n, K block j)."""
+    n = np.asarray(n, np.int64)
+    j = np.asarray(j, np.int64)
+    tiles_k = nblk // 8            # 8 scale blocks per 128-byte K tile of E2M1
+    tn, r = n // TILE_ROWS, n % TILE_ROWS
+    tk, jj = j // 8, j % 8
+    group = tn * (tiles_k * 2) + tk * 2 + jj // 4
+    return group * 512 + (r % 32) * 16 + (r // 32) * 4 + (jj % 4)
+
+
+def pack_b_scales(scales: np.ndarray) -> np.ndarray:
+    s = np.ascontiguousarray(scales, dtype=np.uint8)
+    N, nblk = s.shape
+    nn, jj = np.meshgrid(np.arange(N), np.arange(nblk), indexing="ij")
+    out = np.zeros(N * nblk, dtype=np.uint8)
+    out[packed_scale_offset(nn, jj, nblk).ravel()] = s.ravel()
+    return out
+
+
+def unpack_b_scales(packed: np.ndarray, N: int, nblk: int) -> np.ndarray:
+    nn, jj = np.meshgrid(np.arange(N), np.arange(nblk), indexing="ij")
+    return np.asarray(packed, np.uint8)[packed_scale_offset(nn, jj, nblk)]
+
+
+def pack_b(b: np.ndarray, dtype: str, scales: Optional[np.ndarray] = None) -> np.ndarray:
+    """Whole packed buffer for B (data region, then the scale region for E2M1)."""
+    data = pack_b_bytes(np.ascontiguousarray(b).view(np.uint8).reshape(b.shape[0], -1))
+    if dtype == "e2m1":
+        return np.concatenate([data, pack_b_scales(scales)])
+    return data
+
+
+# ----------------------------------------------------------------------------
+# Tile bookkeeping and byte/flop counts ("GEMM Optimization Guide")
+# ----------------------------------------------------------------------------
+
+def tile_params(tile_m: int, tile_n: int, tile_k: int, elem_bytes: float, a_elem_vec_pack: int = 1) -> dict:
+    """Section 1.2: derived tile parameters of the 4-wave, 16x16-MFMA tiling."""
+    tile_k_bytes = int(tile_k * elem_bytes)
+    return {
+        "m_repeat": tile_m // 16,
+        "n_per_wave": tile_n // 4,
+        "num_acc_n": (tile_n // 4) // 16,
+        "k_unroll": tile_k_bytes // a_elem_vec_pack // 64,
+    }
+
+
+def mfma_per_tile(tile_m: int, tile_n: int, tile_k: int, elem_bytes: float) -> int:
+    """Section 1.5: k_unroll * m_repeat * num_acc_n * 2 (two K32 per K64 step)."""
+    p = tile_params(tile_m, tile_n, tile_k, elem_bytes)
+    return p["k_unroll"] * p["m_repeat"] * p["num_acc_n"] * 2
+
+
+def grid_blocks(M: int, N: int, tile_m: int, tile_n: int) -> int:
+    """Section 1.1: one block per (M tile, N tile)."""
+    return (M // tile_m) * (N // tile_n)
+
+
+def mfma_per_block(K: int, tile_m: int, tile_n: int, tile_k: int, elem_bytes: float) -> int:
+    """Section 14, step 2: MFMAs per tile times the number of K tiles."""
+    return mfma_per_tile(tile_m, tile_n, tile_k, elem_bytes) * (K // tile_k)
+
+
+def lds_bytes(tile_m: int, tile_k: int, elem_bytes: float, stages: int = 2) -> int:
+    """Section 2.4: stages * tile_m * tile_k * elem_bytes."""
+    return int(stages * tile_m * tile_k * elem_bytes)
+
+
+def flops(M: int, N: int, K: int) -> int:
+    """Section 8.1: 2*M*N*K."""
+    return 2 * M * N * K
+
+
+def bytes_moved(M: int, N: int, K: int, kind: str) -> int:
+    """Section 8.2 byte counts.
+
+    kind = "fp8" / "int8"  : M*K + N*K + 2*M*N + 4*(M+N)
+    kind = "int4"          : M*K + N*K/2 + 2*M*N + 4*(M+N)
+    kind = "mxfp4"         : M*K/2 + N*K/2 + 2*M*N + (M+N)*K/32
+    """
+    if kind in ("fp8", "int8"):
+        return M * K + N * K + M * N * 2 + (M + N) * 4
+    if kind == "int4":
+        return M * K + (N * K) // 2 + M * N * 2 + (M + N) * 4
+    if kind == "mxfp4":
+        return (M * K) // 2 + (N * K) // 2 + M * N * 2 + (M + N) * (K // 32)
+    raise ValueError(kind)
+
+
+def tflops(M: int, N: int, K: int, us: float) -> float:
+    """Section 8.1: flops / (us/1e6) / 1e12."""
+    return flops(M, N, K) / (us / 1e6) / 1e12
+
+
+# ----------------------------------------------------------------------------
+# CPU baseline timing helper (used by bench.py's cpu_baseline leg only)
+# ----------------------------------------------------------------------------
+
+def time_gemm(ops, rows: np.ndarray) -> float:
+    """Wall-clock seconds for the reference C of the given output rows."""
+    t0 = time.perf_counter()
+    gemm_operands(ops, rows=rows)
+    return time.perf_counter() - t0

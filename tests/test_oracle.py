@@ -1,0 +1,388 @@
+"""Pins of the CPU oracle against things other than itself.
+
+- Codecs: torch's float8_e4m3fn / bfloat16 decodes (library routines) and the
+  OCP E2M1 table (tests/golden/).
+- GEMMs: brute force in exact rational arithmetic (fractions.Fraction) on tiny
+  shapes, numpy's int64 matmul, identity and permutation operands, and the
+  block-scaled form reducing to the plain one when every scale is 1.
+- Bookkeeping: the numbers the "GEMM Optimization Guide" prints
+  (tests/golden/).
+- Pack model: round trips and layout invariants.
+
+The last group plants mistakes in the oracle, on the CPU, and checks that
+some pin fails for each one.
+"""
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from dense_gemm_preshuffle_gb300 import inputs
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ---------------------------------------------------------------- codecs
+
+def torch_e4m3_values():
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    return codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def test_e4m3_decode_matches_torch_all_codes():
+    ref = torch_e4m3_values()
+    got = oracle.decode_e4m3(np.arange(256, dtype=np.uint8))
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert nan.sum() == 2  # 0x7F and 0xFF
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert got[0x7E] == 448.0 and got[0x01] == 2.0 ** -9
+
+
+def load_e2m1_golden():
+    vals = {}
+    for line in open(os.path.join(GOLDEN, "ocp_e2m1_values.txt")):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        c, v = line.split()
+        vals[int(c)] = float(v)
+    return vals
+
+
+def test_e2m1_decode_matches_ocp_table():
+    table = load_e2m1_golden()
+    got = oracle.decode_e2m1(np.arange(16, dtype=np.uint8))
+    for c in range(16):
+        assert got[c] == table[c], c
+        assert np.signbit(got[c]) == np.signbit(table[c]) or table[c] == 0.0
+
+
+def test_ue8m0_decode():
+    got = oracle.decode_ue8m0(np.arange(256, dtype=np.uint8))
+    assert got[127] == 1.0 and got[128] == 2.0 and got[126] == 0.5
+    assert got[0] == float.fromhex("0x1p-127") and got[254] == float.fromhex("0x1p+127")
+    assert np.isnan(got[255])
+    assert np.all(got[1:255] == 2.0 * got[0:254])
+
+
+def test_bf16_decode_matches_torch():
+    rng = np.random.default_rng(1)
+    bits = rng.integers(0, 1 << 16, size=100000, dtype=np.uint16)
+    t = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    got = oracle.decode_bf16(bits)
+    nan = np.isnan(t)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], t[~nan])
+
+
+# ---------------------------------------------------------------- GEMMs
+
+def frac_gemm(a_vals, b_vals):
+    """Exact C[m][n] = sum_k a[m][k] * b[n][k] over Fractions (pure Python)."""
+    M, K = len(a_vals), len(a_vals[0])
+    N = len(b_vals)
+    return [[sum((a_vals[m][k] * b_vals[n][k] for k in range(K)), Fraction(0)) for n in range(N)]
+            for m in range(M)]
+
+
+def to_frac(x):
+    return [[Fraction(float(v)) for v in row] for row in np.asarray(x, np.float64)]
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 1), (3, 5, 7), (8, 8, 64), (2, 9, 33)])
+def test_int8_bruteforce_and_numpy(M, N, K):
+    rng = np.random.default_rng(M * 100 + N * 10 + K)
+    a = rng.integers(-128, 128, size=(M, K)).astype(np.int8)
+    b = rng.integers(-128, 128, size=(N, K)).astype(np.int8)
+    got = oracle.gemm_int8(a, b)
+    brute = [[sum(int(a[m, k]) * int(b[n, k]) for k in range(K)) for n in range(N)] for m in range(M)]
+    assert got.tolist() == brute
+    assert np.array_equal(got, a.astype(np.int64) @ b.astype(np.int64).T)
+
+
+def test_int8_extremes_fit_int32():
+    # max |C| for the small-batch workload's K=4096: 4096 * 128^2 < 2^31
+    K = 4096
+    a = np.full((2, K), -128, dtype=np.int8)
+    b = np.full((3, K), -128, dtype=np.int8)
+    b[1] = 127
+    got = oracle.gemm_int8(a, b)
+    assert got[0, 0] == K * 128 * 128 and got[0, 1] == -K * 128 * 127
+    assert abs(int(got.max())) < 2 ** 31
+
+
+@pytest.mark.parametrize("M,N,K", [(3, 4, 64), (8, 8, 64), (5, 3, 96)])
+def test_e4m3_rowcol_vs_fraction(M, N, K):
+    ops = inputs.make_operands("e4m3", M, N, K, seed=7 + M)
+    vals = torch_e4m3_values()  # library decode
+    qa = to_frac(vals[ops.a])
+    qb = to_frac(vals[ops.b])
+    acc = frac_gemm(qa, qb)
+    got = oracle.gemm_operands(ops)
+    for m in range(M):
+        for n in range(N):
+            exact = acc[m][n] * Fraction(float(ops.scale_a[m])) * Fraction(float(ops.scale_b[n]))
+            # the unscaled sum is exact in fp64; two scalings each round once
+            assert abs(Fraction(got[m, n]) - exact) <= abs(exact) * Fraction(1, 2 ** 51)
+
+
+@pytest.mark.parametrize("M,N,K", [(3, 4, 16), (4, 2, 40)])
+def test_bf16_vs_fraction(M, N, K):
+    ops = inputs.make_operands("bf16", M, N, K, seed=11)
+    av = torch.from_numpy(ops.a.view(np.int16)).view(torch.bfloat16).double().numpy()
+    bv = torch.from_numpy(ops.b.view(np.int16)).view(torch.bfloat16).double().numpy()
+    exact = frac_gemm(to_frac(av), to_frac(bv))
+    got = oracle.gemm_operands(ops)
+    for m in range(M):
+        for n in range(N):
+            bound = sum(abs(Fraction(float(av[m, k])) * Fraction(float(bv[n, k]))) for k in range(K))
+            assert abs(Fraction(got[m, n]) - exact[m][n]) <= bound * K * Fraction(1, 2 ** 52)
+
+
+@pytest.mark.parametrize("M,N,K", [(2, 3, 64), (4, 4, 96)])
+def test_mxfp4_vs_fraction(M, N, K):
+    ops = inputs.make_operands("e2m1", M, N, K, seed=13)
+    table = load_e2m1_golden()
+    ca = oracle.unpack_e2m1_rows(ops.a, K)
+    cb = oracle.unpack_e2m1_rows(ops.b, K)
+    got = oracle.gemm_operands(ops)
+    for m in range(M):
+        for n in range(N):
+            tot = Fraction(0)
+            for j in range(K // 32):
+                part = sum((Fraction(table[int(ca[m, k])]) * Fraction(table[int(cb[n, k])])
+                            for k in range(32 * j, 32 * j + 32)), Fraction(0))
+                tot += part * Fraction(2) ** (int(ops.scale_a[m, j]) - 127) * Fraction(2) ** (int(ops.scale_b[n, j]) - 127)
+            assert Fraction(got[m, n]) == tot  # exact: power-of-two scales, short sums
+
+
+def test_block_scaled_reduces_to_plain_when_scales_are_one():
+    rng = np.random.default_rng(3)
+    M, N, K = 5, 6, 128
+    pa = rng.integers(0, 256, size=(M, K // 2), dtype=np.uint8)
+    pb = rng.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+    one_a = np.full((M, K // 32), 127, np.uint8)
+    one_b = np.full((N, K // 32), 127, np.uint8)
+    got = oracle.gemm_mxfp4(pa, pb, one_a, one_b, K)
+    plain = oracle.gemm_f64(oracle.decode_e2m1(oracle.unpack_e2m1_rows(pa, K)),
+                            oracle.decode_e2m1(oracle.unpack_e2m1_rows(pb, K)))
+    assert np.array_equal(got, plain)
+    # numpy's BLAS on the same decoded values (a library routine)
+    ref = oracle.decode_e2m1(oracle.unpack_e2m1_rows(pa, K)) @ oracle.decode_e2m1(oracle.unpack_e2m1_rows(pb, K)).T
+    assert np.array_equal(got, ref)
+
+
+def test_identity_and_permutation_operands():
+    K = 64
+    rng = np.random.default_rng(5)
+    # bf16: A = I (0x3F80 is 1.0) -> C = B^T
+    b = inputs.bf16_rows(48, K, inputs._gen(1))
+    eye = np.where(np.eye(K, dtype=bool), np.uint16(0x3F80), np.uint16(0))
+    c = oracle.gemm_bf16(eye, b)
+    assert np.array_equal(c, oracle.decode_bf16(b).T)
+    # A = permutation P -> C = P . B^T (rows of B^T permuted)
+    perm = rng.permutation(K)
+    pm = np.zeros((K, K), np.uint16)
+    pm[np.arange(K), perm] = 0x3F80
+    c = oracle.gemm_bf16(pm, b)
+    assert np.array_equal(c, oracle.decode_bf16(b).T[perm])
+    # e4m3 with unit scales: 0x38 is 1.0
+    qb, _ = inputs.e4m3_rows(40, K, inputs._gen(2))
+    eye8 = np.where(np.eye(K, dtype=bool), np.uint8(0x38), np.uint8(0))
+    c = oracle.gemm_e4m3_rowcol(eye8, qb, np.ones(K, np.float32), np.ones(40, np.float32))
+    assert np.array_equal(c, oracle.decode_e4m3(qb).T)
+    # row and column scales act on rows and columns of C
+    sa = np.arange(1, K + 1, dtype=np.float32)
+    sb = np.full(40, 0.5, np.float32)
+    c = oracle.gemm_e4m3_rowcol(eye8, qb, sa, sb)
+    assert np.array_equal(c, oracle.decode_e4m3(qb).T * sa[:, None] * 0.5)
+    # int8: diagonal A scales the rows of B^T
+    d = np.diag(np.arange(-32, 32)).astype(np.int8)
+    bi = rng.integers(-128, 128, size=(20, K)).astype(np.int8)
+    c = oracle.gemm_int8(d, bi)
+    assert np.array_equal(c, np.arange(-32, 32)[:, None] * bi.T.astype(np.int64))
+
+
+def test_sampled_rows_cols_equal_full():
+    ops = inputs.make_operands("e4m3", 40, 72, 128, seed=3)
+    full = oracle.gemm_operands(ops)
+    rows = np.array([0, 7, 39])
+    cols = np.array([1, 64, 71, 5])
+    part = oracle.gemm_operands(ops, rows=rows, cols=cols)
+    assert np.array_equal(part, full[np.ix_(rows, cols)])
+
+
+def test_parity_metric():
+    r = np.array([[0.0, 1.0], [-100.0, 3.0]])
+    assert oracle.max_rel_err(r, r) == 0.0
+    c = r.copy()
+    c[1, 0] *= 1 + 0.009       # 0.9 % off a large value -> above the bound
+    assert oracle.max_rel_err(c, r) > oracle.FLOAT_TOL
+    c = r.copy()
+    c[0, 0] = 5e-5             # near zero: the +1e-2 floor governs
+    assert oracle.max_rel_err(c, r) == pytest.approx(5e-3)
+
+
+# ---------------------------------------------------------------- bookkeeping
+
+def load_worked_numbers():
+    rows = []
+    for line in open(os.path.join(GOLDEN, "gemm_optimization_worked_numbers.txt")):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        key, args, val, how = [x.strip() for x in line.split("|")]
+        rows.append((key, args.split(), float(val), how))
+    return rows
+
+
+def _eval(key, args):
+    if key == "mfma_per_tile":
+        m, n, k, eb = map(int, args)
+        return oracle.mfma_per_tile(m, n, k, eb)
+    if key in ("k_unroll", "m_repeat", "num_acc_n"):
+        m, n, k, eb = map(int, args)
+        return oracle.tile_params(m, n, k, eb)[key]
+    if key == "lds_kb":
+        m, k, eb = map(int, args)
+        return oracle.lds_bytes(m, k, eb) / 1024
+    if key == "grid_blocks":
+        M, N, tm, tn = map(int, args)
+        return oracle.grid_blocks(M, N, tm, tn)
+    if key == "mfma_per_block":
+        K, tm, tn, tk, eb = map(int, args)
+        return oracle.mfma_per_block(K, tm, tn, tk, eb)
+    if key == "gflop":
+        M, N, K = map(int, args)
+        return oracle.flops(M, N, K) / 1e9
+    if key == "mbytes":
+        M, N, K, kind = int(args[0]), int(args[1]), int(args[2]), args[3]
+        return oracle.bytes_moved(M, N, K, kind) / 1e6
+    if key == "gbps_at_ms":
+        M, N, K, kind, ms = int(args[0]), int(args[1]), int(args[2]), args[3], float(args[4])
+        return oracle.bytes_moved(M, N, K, kind) / (ms * 1e-3) / 1e9
+    raise KeyError(key)
+
+
+@pytest.mark.parametrize("row", load_worked_numbers(), ids=lambda r: r[0] + ":" + "x".join(r[1]))
+def test_worked_numbers(row):
+    key, args, printed, how = row
+    got = _eval(key, args)
+    if how == "exact":
+        assert got == printed
+    elif how.startswith("round:"):
+        d = int(how.split(":")[1])
+        assert round(got, d) == printed
+    elif how.startswith("trunc:"):
+        d = int(how.split(":")[1])
+        assert int(got * 10 ** d) / 10 ** d == pytest.approx(printed)
+
+
+def test_tflops_formula():
+    # section 8.1: 2*M*N*K flops in `us` microseconds
+    assert oracle.tflops(1000, 1000, 1000, 1.0) == pytest.approx(2000.0)
+
+
+# ---------------------------------------------------------------- pack model
+
+@pytest.mark.parametrize("N,Kb", [(128, 128), (256, 512), (384, 256)])
+def test_pack_roundtrip_and_permutation(N, Kb):
+    rng = np.random.default_rng(N + Kb)
+    b = rng.integers(0, 256, size=(N, Kb), dtype=np.uint8)
+    p = oracle.pack_b_bytes(b)
+    assert p.size == b.size
+    assert np.array_equal(oracle.unpack_b_bytes(p, N, Kb), b)
+    offs = oracle.packed_offset(*np.meshgrid(np.arange(N), np.arange(Kb), indexing="ij"), Kb)
+    assert np.array_equal(np.sort(offs.ravel()), np.arange(N * Kb))  # a bijection
+
+
+def test_pack_layout_invariants():
+    N, Kb = 256, 384
+    # index-encode: byte value identifies (row mod 128, 16-byte chunk) etc.
+    n, k = np.meshgrid(np.arange(N), np.arange(Kb), indexing="ij")
+    off = oracle.packed_offset(n, k, Kb)
+    tile = off // 16384
+    # each 16 KiB tile holds exactly one 128-row x 128-byte block of B
+    assert np.all(tile == (n // 128) * (Kb // 128) + k // 128)
+    # a 16-byte chunk of a row stays contiguous and in order
+    assert np.all(off[:, 1:][k[:, 1:] % 16 != 0] == off[:, :-1][k[:, 1:] % 16 != 0] + 1)
+    # rows sit at a 128-byte pitch inside their tile
+    assert np.all((off % 16384) // 128 == n % 128)
+    # any 8 consecutive rows (aligned) reading the same logical chunk hit 8
+    # distinct 16-byte positions: no shared-memory bank conflicts
+    pos = (off % 128) // 16
+    for c in range(8):
+        for g in range(0, N, 8):
+            assert len(set(pos[g:g + 8, c * 16].tolist())) == 8
+
+
+def test_pack_scale_roundtrip():
+    rng = np.random.default_rng(9)
+    N, nblk = 256, 64
+    s = rng.integers(0, 255, size=(N, nblk), dtype=np.uint8)
+    p = oracle.pack_b_scales(s)
+    assert np.array_equal(oracle.unpack_b_scales(p, N, nblk), s)
+    offs = oracle.packed_scale_offset(*np.meshgrid(np.arange(N), np.arange(nblk), indexing="ij"), nblk)
+    assert np.array_equal(np.sort(offs.ravel()), np.arange(N * nblk))
+
+
+# ---------------------------------------------------------------- planted mistakes
+
+def _pins_fail(monkeypatch, attr, mutant, check):
+    monkeypatch.setattr(oracle, attr, mutant)
+    with pytest.raises(AssertionError):
+        check()
+
+
+def test_planted_e4m3_subnormal_bug_is_caught(monkeypatch):
+    good = oracle.decode_e4m3
+
+    def bad(c):
+        v = good(c)
+        c = np.asarray(c, np.uint8)
+        return np.where(((c >> 3) & 0xF) == 0, v * 2, v)  # wrong subnormal exponent
+    _pins_fail(monkeypatch, "decode_e4m3", bad, test_e4m3_decode_matches_torch_all_codes)
+
+
+def test_planted_e2m1_bias_bug_is_caught(monkeypatch):
+    good = oracle.decode_e2m1
+    _pins_fail(monkeypatch, "decode_e2m1", lambda c: good(c) * 2.0, test_e2m1_decode_matches_ocp_table)
+
+
+def test_planted_transposed_operand_is_caught(monkeypatch):
+    good = oracle.gemm_f64
+    _pins_fail(monkeypatch, "gemm_f64", lambda a, b: good(a, np.ascontiguousarray(b[:, ::-1])),
+               lambda: test_e4m3_rowcol_vs_fraction(3, 4, 64))
+
+
+def test_planted_dropped_term_is_caught(monkeypatch):
+    good = oracle.gemm_f64
+    _pins_fail(monkeypatch, "gemm_f64", lambda a, b: good(a[:, :-1], b[:, :-1]),
+               lambda: test_bf16_vs_fraction(3, 4, 16))
+
+
+def test_planted_scale_sign_bug_is_caught(monkeypatch):
+    good = oracle.decode_ue8m0
+    _pins_fail(monkeypatch, "decode_ue8m0", lambda c: 1.0 / good(c),
+               lambda: test_mxfp4_vs_fraction(2, 3, 64))
+
+
+def test_planted_missing_column_scale_is_caught(monkeypatch):
+    good = oracle.gemm_e4m3_rowcol
+    _pins_fail(monkeypatch, "gemm_e4m3_rowcol", lambda qa, qb, sa, sb: good(qa, qb, sa, np.ones_like(sb)),
+               lambda: test_e4m3_rowcol_vs_fraction(3, 4, 64))
+
+
+def test_planted_pack_swizzle_bug_is_caught(monkeypatch):
+    good = oracle.packed_offset
+
+    def bad(n, kb, Kb):
+        o = good(n, kb, Kb)
+        return o - (o % 128) + (np.asarray(kb) % 128)  # forgets the chunk permutation
+    monkeypatch.setattr(oracle, "packed_offset", bad)
+    with pytest.raises(AssertionError):
+        test_pack_layout_invariants()
