@@ -1,0 +1,491 @@
+"""Benchmark of the preshuffle GEMM on GB300.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                [--workload NAME] [--no-others]
+
+One step is one gemm_run call (C = A . B^T with B already packed) on the
+named workload: the hot path with the weight resident in HBM.  The offline
+preshuffle of B is timed separately (key "pack_b") because the method runs
+it once per weight, not per product.
+
+- L2: each step uses its own packed-B / A copy, rotating through enough
+  copies that their total exceeds 2x the 129 MB L2.  Every step therefore
+  streams B from HBM.
+- Timing: W warm-up steps, then exactly K steps, replayed from a CUDA graph
+  of back-to-back gemm_run launches (no host gaps).  The K steps sit between
+  a barrier and torch.cuda.synchronize() on both sides and are timed with
+  CUDA events on the launch stream.
+- Reported value: the maximum over ranks.  Under torchrun every rank runs the
+  same independent problem on its own GPU (weak scaling, no collective).
+- JSON line keys:
+  - "e2e": the same metric through the public call, with pinned host
+    buffers.  A and its scales are copied host->device and C device->host
+    every step.
+  - "roofline": the GEMM kernel against the measured HBM or tensor peak.
+  - "cpu_baseline": the oracle, timed on this host's cores on a bounded
+    sample.
+  - "others": the other workloads, each with its own device-timed TFLOP/s
+    and roofline fraction.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GEMM TFLOPS & % of GB300 dtype peak; HBM GB/s % for small-M shapes"
+DEFAULT_WORKLOAD = "int8_16x7168x4096"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# nominal dense tensor-rate ratios to bf16 (2.25 PF): fp8 4.5, fp4 13.5
+DTYPE_RATIO = {"bf16": 1.0, "e4m3": 2.0, "e2m1": 6.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def algorithmic_bytes(dtype: str, M: int, N: int, K: int) -> int:
+    """A + B + C + scales, as the GEMM guide counts them (section 8.2); the
+    INT8 workload's C is int32 and it has no scales."""
+    if dtype == "int8":
+        return M * K + N * K + M * N * 4
+    if dtype == "e4m3":
+        return M * K + N * K + M * N * 2 + (M + N) * 4
+    if dtype == "bf16":
+        return 2 * M * K + 2 * N * K + 2 * M * N
+    if dtype == "e2m1":
+        return M * K // 2 + N * K // 2 + M * N * 2 + (M + N) * (K // 32)
+    raise ValueError(dtype)
+
+
+def bound_of(dtype: str, M: int) -> str:
+    # the guide's rule of thumb (section 8.3): M <= 512 memory-bound; the
+    # int8 small-batch workload is the weight-streaming case
+    return "hbm" if dtype == "int8" else "tensor"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 50 ms."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return self
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 8:
+                self.samples.append((time.perf_counter(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float):
+        inside = [p for (t, p) in self.samples if t0 <= t <= t1]
+        use = inside if inside else [p for (t, p) in self.samples]
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[0]) for p in use if num(p[0]) is not None]
+        mx = [num(p[1]) for p in use if num(p[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in use for i in range(4) if p[4 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(use), "samples_in_timed_region": len(inside),
+                "power_w_max": max((num(p[2]) or 0.0) for p in use)}
+
+
+# ------------------------------------------------------------------ distributed
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        dist.init_process_group(backend=backend)
+        pg = dist
+    return world, rank, local, pg
+
+
+def barrier(pg, device=None):
+    if pg is not None:
+        if device is not None:
+            pg.barrier(device_ids=[device])
+        else:
+            pg.barrier()
+
+
+def max_over_ranks(pg, x: float, device):
+    if pg is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ our arm
+
+class Problem:
+    """Device-resident copies of one workload, ready for gemm_run."""
+
+    def __init__(self, name: str, device, copies: int | None = None):
+        import torch
+        import dense_gemm_preshuffle_gb300 as gp
+        from dense_gemm_preshuffle_gb300 import inputs
+        self.gp = gp
+        self.name = name
+        self.ops = ops = inputs.workload_operands(name)
+        self.dtype, self.M, self.N, self.K = ops.dtype, ops.M, ops.N, ops.K
+
+        def t(x):
+            if x is None:
+                return None
+            if x.dtype == np.uint16:
+                x = x.view(np.int16)
+            return torch.from_numpy(np.ascontiguousarray(x))
+        self.host_a, self.host_sa = t(ops.a), t(ops.scale_a)
+        B = t(ops.b).to(device)
+        sb = t(ops.scale_b).to(device) if ops.scale_b is not None else None
+        # time the offline pack once (device events), then make the copies
+        torch.cuda.synchronize(device)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for _ in range(2):
+            e0.record()
+            bp = gp.preshuffle_b(B, self.dtype, B_scales=sb if self.dtype == "e2m1" else None)
+            e1.record()
+        torch.cuda.synchronize(device)
+        self.pack_us = e0.elapsed_time(e1) * 1e3
+        self.packed_bytes = bp.numel()
+        if copies is None:
+            copies = max(1, math.ceil(2 * L2_BYTES / max(1, bp.numel())) + 1)
+        self.copies = copies
+        self.Bp = [bp] + [bp.clone() for _ in range(copies - 1)]
+        A = self.host_a.to(device)
+        self.A = [A] + [A.clone() for _ in range(copies - 1)]
+        self.sa = self.host_sa.to(device) if self.host_sa is not None else None
+        self.sb = sb if self.dtype == "e4m3" else None
+        cdt = torch.int32 if self.dtype == "int8" else torch.bfloat16
+        self.C = [torch.empty((self.M, self.N), dtype=cdt, device=device) for _ in range(min(copies, 4))]
+        self.c_dtype = "int32" if self.dtype == "int8" else "bf16"
+        self.mode = {"int8": "none", "bf16": "none", "e4m3": "rowcol_f32", "e2m1": "block32_ue8m0"}[self.dtype]
+        self.flops = 2 * self.M * self.N * self.K
+        self.bytes = algorithmic_bytes(self.dtype, self.M, self.N, self.K)
+
+    def step(self, i: int, stream=None):
+        j = i % self.copies
+        self.gp.gemm_run(self.A[j], self.Bp[j], self.dtype, self.M, self.N, self.K, self.mode,
+                         self.sa, self.sb, self.C[j % len(self.C)], self.c_dtype, stream)
+
+
+def time_device(prob: Problem, steps: int, warmup: int, pg, device, graph_len: int = 100):
+    """Device time (s) of exactly `steps` steps after `warmup` warm-up steps."""
+    import torch
+    stream = torch.cuda.current_stream(device)
+    for i in range(max(3, warmup)):
+        prob.step(i)
+    torch.cuda.synchronize(device)
+    g_len = max(1, min(graph_len, steps))
+    graph = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream(device)
+    s.wait_stream(stream)
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            for i in range(g_len):
+                prob.step(i)
+    stream.wait_stream(s)
+    graph.replay()  # untimed warm replay
+    torch.cuda.synchronize(device)
+    full, rest = divmod(steps, g_len)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(pg, device.index if pg is not None else None)
+    torch.cuda.synchronize(device)
+    e0.record(stream)
+    for _ in range(full):
+        graph.replay()
+    for i in range(rest):
+        prob.step(i)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    barrier(pg, device.index if pg is not None else None)
+    return e0.elapsed_time(e1) / 1e3
+
+
+def time_e2e(prob: Problem, steps: int, warmup: int, device):
+    """Through the public call with pinned host buffers: H2D of A (+ its
+    scales), gemm_run, D2H of C, every step.  Returns (seconds, h2d, d2h)."""
+    import torch
+    ha = prob.host_a.pin_memory()
+    hsa = prob.host_sa.pin_memory() if prob.host_sa is not None else None
+    hc = torch.empty(prob.C[0].shape, dtype=prob.C[0].dtype).pin_memory()
+    stream = torch.cuda.current_stream(device)
+
+    def one(i):
+        j = i % prob.copies
+        prob.A[j].copy_(ha, non_blocking=True)
+        if hsa is not None:
+            prob.sa.copy_(hsa, non_blocking=True)
+        prob.gp.gemm_run(prob.A[j], prob.Bp[j], prob.dtype, prob.M, prob.N, prob.K, prob.mode, prob.sa, prob.sb,
+                         prob.C[0], prob.c_dtype)
+        hc.copy_(prob.C[0], non_blocking=True)
+    for i in range(max(3, warmup)):
+        one(i)
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(steps):
+        one(i)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    h2d = ha.numel() * ha.element_size() + (hsa.numel() * hsa.element_size() if hsa is not None else 0)
+    d2h = hc.numel() * hc.element_size()
+    return e0.elapsed_time(e1) / 1e3, h2d, d2h
+
+
+def roofline(prob: Problem, sec_per_step: float, peaks: dict, peak_kind: str, traffic=None):
+    if bound_of(prob.dtype, prob.M) == "hbm":
+        achieved = prob.bytes / sec_per_step / 1e9
+        peak = float(peaks["hbm_gbs"])
+        return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": traffic,
+                "peak_source": f"hbm_gbs ({peak_kind})",
+                "algorithmic_bytes_per_launch": prob.bytes}
+    ratio = DTYPE_RATIO[prob.dtype]
+    base = float(peaks["bf16_tflops"])
+    peak = base * ratio
+    achieved = prob.flops / sec_per_step / 1e12
+    return {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak, 1), "unit": "TFLOP/s",
+            "frac": round(achieved / peak, 4), "traffic": traffic,
+            "peak_source": f"bf16_tflops burst ({peak_kind}) x {ratio:g} nominal {prob.dtype}/bf16 ratio",
+            "algorithmic_flops_per_launch": prob.flops}
+
+
+def traffic_from_profiles(name: str):
+    """DRAM bytes per launch recorded from an ncu capture, if a summary for
+    this workload is committed under profiles/ (key `traffic_bytes_per_launch`)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        with open(p) as f:
+            return json.load(f).get(name)
+    except (OSError, ValueError):
+        return None
+
+
+def cpu_baseline(name: str, budget_s: float = 12.0):
+    """The oracle as it stands, on this host's cores, over a bounded sample
+    of rows of the workload; value in the metric's unit (TFLOP/s)."""
+    import oracle
+    from dense_gemm_preshuffle_gb300 import inputs
+    ops = inputs.workload_operands(name)
+    cores = oracle.num_threads()
+    rows = 1
+    t = oracle.time_gemm(ops, np.arange(rows))
+    while t < 1.0 and rows < ops.M:
+        rows = min(ops.M, rows * 2)
+        t = oracle.time_gemm(ops, np.arange(rows))
+    reps, total = 1, t
+    while total + t < budget_s and reps < 1000:
+        total += oracle.time_gemm(ops, np.arange(rows))
+        reps += 1
+    flops = 2.0 * rows * ops.N * ops.K * reps
+    return {"value": flops / total / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{reps} x C rows [0,{rows}) of {ops.M} ({rows * ops.N} outputs, K={ops.K}), "
+                      f"{total:.1f} s wall"}
+
+
+def run_ours(args):
+    import torch
+    world, rank, local, pg = dist_setup(args)
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    peaks, peak_kind = load_peaks()
+    import dense_gemm_preshuffle_gb300 as gp
+    gp.load_library()
+
+    clocks = ClockSampler(local).start()
+    prob = Problem(args.workload, device)
+    t_start = time.perf_counter()
+    sec = time_device(prob, args.steps, args.warmup, pg, device)
+    t_end = time.perf_counter()
+    sec = max_over_ranks(pg, sec, device)
+    clock_summary = clocks.summary(t_start, t_end)
+    e2e_sec, h2d, d2h = time_e2e(prob, max(10, min(args.steps, 2000)), args.warmup, device)
+    e2e_steps = max(10, min(args.steps, 2000))
+    e2e_sec = max_over_ranks(pg, e2e_sec, device)
+    clocks.stop()
+
+    per = sec / args.steps
+    value = world * prob.flops * args.steps / sec / 1e12
+    out = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(per * 1e3, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": prob.dtype,
+        "data": "synthetic, seeded (workload recipe)",
+        "config": {"workload": prob.name, "M": prob.M, "N": prob.N, "K": prob.K,
+                   "parallelism": f"replicas x{world}",
+                   "l2": f"inputs larger than L2: {prob.copies} rotating packed-B/A copies "
+                         f"({prob.copies * prob.packed_bytes / 1e6:.0f} MB)",
+                   "timing": "CUDA-graph replay of back-to-back gemm_run launches, CUDA events"},
+        "gpu_launches": args.steps,
+        "e2e": {"value": round(world * prob.flops * e2e_steps / e2e_sec / 1e12, 3), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_sec / e2e_steps * 1e3, 5), "steps": e2e_steps},
+        "roofline": roofline(prob, per, peaks, peak_kind, traffic_from_profiles(prob.name)),
+        "clocks": clock_summary,
+        "pack_b": {"us": round(prob.pack_us, 2), "bytes": prob.packed_bytes,
+                   "GB/s": round(2 * prob.packed_bytes / (prob.pack_us * 1e-6) / 1e9, 1)},
+    }
+    del prob
+    torch.cuda.empty_cache()
+    if not args.no_others:
+        others = {}
+        from dense_gemm_preshuffle_gb300 import inputs
+        for name in inputs.WORKLOADS:
+            if name == args.workload:
+                continue
+            try:
+                p2 = Problem(name, device)
+                steps2 = max(20, min(args.steps, 400))
+                s2 = time_device(p2, steps2, args.warmup, pg, device)
+                s2 = max_over_ranks(pg, s2, device)
+                r = roofline(p2, s2 / steps2, peaks, peak_kind, traffic_from_profiles(name))
+                others[name] = {"us_per_step": round(s2 / steps2 * 1e6, 3),
+                                "TFLOP/s": round(p2.flops * steps2 / s2 / 1e12, 2),
+                                "GB/s": round(p2.bytes * steps2 / s2 / 1e9, 1), "roofline": r,
+                                "steps": steps2, "pack_b_us": round(p2.pack_us, 2)}
+                del p2
+                torch.cuda.empty_cache()
+            except Exception as e:  # a workload whose kernel is not built yet
+                others[name] = {"unavailable": f"{type(e).__name__}: {e}"[:200]}
+        out["others"] = others
+    if rank == 0:
+        out["cpu_baseline"] = cpu_baseline(args.workload)
+        print(json.dumps(out), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+def run_reference(args):
+    """The oracle on this host's cores: each step is a bounded sample (a set
+    of C rows) of the same workload; rank 0 alone runs it."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    from dense_gemm_preshuffle_gb300 import inputs
+    ops = inputs.workload_operands(args.workload)
+    cores = oracle.num_threads()
+    # size each step so that warm-up + K steps take about a minute in total
+    target = min(0.5, 60.0 / (args.steps + args.warmup))
+    rows, cols = np.arange(1), None
+    t_row = oracle.time_gemm(ops, rows)
+    if t_row > target:
+        ncols = max(1, int(ops.N * target / t_row))
+        cols = np.arange(ncols)
+    else:
+        nrows = 1
+        while nrows < ops.M and oracle.time_gemm(ops, np.arange(min(ops.M, nrows * 2))) < target:
+            nrows = min(ops.M, nrows * 2)
+        rows = np.arange(nrows)
+    for _ in range(args.warmup):
+        oracle.time_gemm(ops, rows, cols)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.time_gemm(ops, rows, cols)
+    sec = time.perf_counter() - t0
+    n_out = len(rows) * (ops.N if cols is None else len(cols))
+    flops = 2.0 * n_out * ops.K * args.steps
+    value = flops / sec / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": ops.dtype,
+        "data": "synthetic, seeded (workload recipe)",
+        "config": {"workload": args.workload, "M": ops.M, "N": ops.N, "K": ops.K},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"each step: {n_out} of the {ops.M * ops.N} outputs of C "
+                                   f"(rows [0,{len(rows)}), {'all' if cols is None else len(cols)} columns; K={ops.K})"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-others", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,293 @@
+// C ABI of the preshuffle GEMM library (declared in include/gemm_preshuffle.h).
+//
+// This layer:
+//   - validates every argument on the host before launching anything;
+//   - builds the TMA tensor maps for A and C;
+//   - picks the kernel (tcgen05 tile kernel, block-scaled MXFP4 kernel, or
+//     the INT8 weight-streaming kernel) and launches it on the caller's
+//     stream.
+//
+// It owns no per-call memory.  Each device gets a 4-byte status word (a
+// __device__ variable) and a cached SM count.
+#include <atomic>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "kernels.h"
+
+namespace gp {
+
+__device__ uint32_t g_status_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  bool ready = false;
+  int num_sms = 0;
+  uint32_t* status = nullptr;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+int device_info(DeviceInfo** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GP_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return GP_ERR_CUDA;
+    void* addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_status_word) != cudaSuccess) return GP_ERR_CUDA;
+    d.status = static_cast<uint32_t*>(addr);
+    if (g_encode == nullptr) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+              cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return GP_ERR_CUDA;
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    d.ready = true;
+  }
+  *out = &d;
+  return GP_OK;
+}
+
+int elem_bits(int dtype) {
+  switch (dtype) {
+    case GP_BF16: return 16;
+    case GP_E4M3: return 8;
+    case GP_INT8: return 8;
+    case GP_E2M1: return 4;
+    default: return 0;
+  }
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shape rules shared by the packer and the GEMM (N, K part).
+int check_nk(int dtype, int64_t N, int64_t K, int64_t* kbytes) {
+  const int bits = elem_bits(dtype);
+  if (bits == 0) return GP_ERR_INVALID_ARG;
+  if (N < 0 || K < 0 || N >= (int64_t(1) << 31) || K >= (int64_t(1) << 31)) return GP_ERR_SHAPE;
+  if ((K * bits) % 8 != 0) return GP_ERR_SHAPE;
+  const int64_t kb = K * bits / 8;
+  if (N % 128 != 0 || kb % 128 != 0) return GP_ERR_SHAPE;
+  *kbytes = kb;
+  return GP_OK;
+}
+
+int encode_2d(CUtensorMap* map, CUtensorMapDataType type, const void* ptr, uint64_t inner, uint64_t outer,
+              uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz) {
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, type, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? GP_OK : GP_ERR_CUDA;
+}
+
+uint64_t wait_limit_ns() {
+  // Bounded-wait limit for the GEMM kernels; GP_WAIT_LIMIT_MS overrides the
+  // 2 s default (tests shorten it to exercise the timeout path quickly).
+  static std::atomic<uint64_t> cached{0};
+  uint64_t v = cached.load();
+  if (v == 0) {
+    v = 2000000000ull;
+    if (const char* e = std::getenv("GP_WAIT_LIMIT_MS")) {
+      const long long ms = std::atoll(e);
+      if (ms > 0) v = (uint64_t)ms * 1000000ull;
+    }
+    cached.store(v);
+  }
+  return v;
+}
+
+std::atomic<int> g_debug_skip_load{0};
+
+}  // namespace
+}  // namespace gp
+
+using namespace gp;
+
+extern "C" {
+
+const char* gemm_status_string(int status) {
+  switch (status) {
+    case GP_OK: return "GP_OK";
+    case GP_ERR_INVALID_ARG: return "GP_ERR_INVALID_ARG: null pointer or bad enum value";
+    case GP_ERR_UNSUPPORTED: return "GP_ERR_UNSUPPORTED: dtype / scale mode / output combination not offered";
+    case GP_ERR_SHAPE: return "GP_ERR_SHAPE: dimension rule violated";
+    case GP_ERR_ALIGNMENT: return "GP_ERR_ALIGNMENT: pointer not 16-byte aligned";
+    case GP_ERR_CUDA: return "GP_ERR_CUDA: a CUDA call failed";
+    case GP_ERR_DEVICE_TIMEOUT: return "GP_ERR_DEVICE_TIMEOUT: a bounded wait inside a kernel gave up";
+    default: return "unknown gp_status";
+  }
+}
+
+int gemm_packed_b_bytes(int dtype, int64_t N, int64_t K, size_t* bytes_out) {
+  if (bytes_out == nullptr) return GP_ERR_INVALID_ARG;
+  int64_t kb = 0;
+  const int rc = check_nk(dtype, N, K, &kb);
+  if (rc != GP_OK) return rc;
+  size_t total = (size_t)N * (size_t)kb;
+  if (dtype == GP_E2M1) total += (size_t)N * (size_t)(K / 32);
+  *bytes_out = total;
+  return GP_OK;
+}
+
+int gemm_preshuffle_b(const void* B, const void* B_scales, int dtype, int64_t N, int64_t K, void* B_packed,
+                      void* stream) {
+  int64_t kb = 0;
+  int rc = check_nk(dtype, N, K, &kb);
+  if (rc != GP_OK) return rc;
+  if (N == 0 || K == 0) return GP_OK;
+  if (B == nullptr || B_packed == nullptr) return GP_ERR_INVALID_ARG;
+  if ((dtype == GP_E2M1) != (B_scales != nullptr)) return GP_ERR_INVALID_ARG;
+  if (!aligned16(B) || !aligned16(B_packed)) return GP_ERR_ALIGNMENT;
+  DeviceInfo* d = nullptr;
+  if ((rc = device_info(&d)) != GP_OK) return rc;
+  return pack_b_launch(static_cast<const uint8_t*>(B), static_cast<const uint8_t*>(B_scales), N, kb, K / 32,
+                       static_cast<uint8_t*>(B_packed), static_cast<cudaStream_t>(stream));
+}
+
+int gemm_unpack_b(const void* B_packed, int dtype, int64_t N, int64_t K, void* B_out, void* B_scales_out,
+                  void* stream) {
+  int64_t kb = 0;
+  int rc = check_nk(dtype, N, K, &kb);
+  if (rc != GP_OK) return rc;
+  if (N == 0 || K == 0) return GP_OK;
+  if (B_packed == nullptr || B_out == nullptr) return GP_ERR_INVALID_ARG;
+  if (dtype == GP_E2M1 && B_scales_out == nullptr) return GP_ERR_INVALID_ARG;
+  if (!aligned16(B_out) || !aligned16(B_packed)) return GP_ERR_ALIGNMENT;
+  DeviceInfo* d = nullptr;
+  if ((rc = device_info(&d)) != GP_OK) return rc;
+  return unpack_b_launch(static_cast<const uint8_t*>(B_packed), N, kb, K / 32, static_cast<uint8_t*>(B_out),
+                         dtype == GP_E2M1 ? static_cast<uint8_t*>(B_scales_out) : nullptr,
+                         static_cast<cudaStream_t>(stream));
+}
+
+int gemm_run(const void* A, const void* B_packed, int dtype, int64_t M, int64_t N, int64_t K, int scale_mode,
+             const void* scale_a, const void* scale_b, void* C, int c_dtype, void* stream) {
+  // ---- combination
+  const bool combo_ok = (dtype == GP_BF16 && scale_mode == GP_SCALE_NONE && c_dtype == GP_BF16) ||
+                        (dtype == GP_E4M3 && scale_mode == GP_SCALE_ROWCOL_F32 && c_dtype == GP_BF16) ||
+                        (dtype == GP_E4M3 && scale_mode == GP_SCALE_NONE && c_dtype == GP_BF16) ||
+                        (dtype == GP_E2M1 && scale_mode == GP_SCALE_BLOCK32_UE8M0 && c_dtype == GP_BF16) ||
+                        (dtype == GP_INT8 && scale_mode == GP_SCALE_NONE && c_dtype == GP_INT32);
+  if (elem_bits(dtype) == 0 || scale_mode < GP_SCALE_NONE || scale_mode > GP_SCALE_BLOCK32_UE8M0 ||
+      (c_dtype != GP_BF16 && c_dtype != GP_INT32))
+    return GP_ERR_INVALID_ARG;
+  if (!combo_ok) return GP_ERR_UNSUPPORTED;
+  // ---- shapes
+  int64_t kb = 0;
+  int rc = check_nk(dtype, N, K, &kb);
+  if (rc != GP_OK) return rc;
+  if (M < 0 || M >= (int64_t(1) << 31)) return GP_ERR_SHAPE;
+  if (dtype == GP_INT8 && K > 131072) return GP_ERR_SHAPE;  // exact result must fit int32
+  const size_t c_elem = c_dtype == GP_INT32 ? 4 : 2;
+  if (M == 0 || N == 0) return GP_OK;  // empty output
+  // ---- pointers
+  if (C == nullptr) return GP_ERR_INVALID_ARG;
+  if (K > 0 && (A == nullptr || B_packed == nullptr)) return GP_ERR_INVALID_ARG;
+  if (scale_mode == GP_SCALE_ROWCOL_F32 && (scale_a == nullptr || scale_b == nullptr)) return GP_ERR_INVALID_ARG;
+  if (scale_mode == GP_SCALE_BLOCK32_UE8M0 && (scale_a == nullptr || scale_b != nullptr)) return GP_ERR_INVALID_ARG;
+  if (scale_mode == GP_SCALE_NONE && (scale_a != nullptr || scale_b != nullptr)) return GP_ERR_INVALID_ARG;
+  if (!aligned16(C) || (K > 0 && (!aligned16(A) || !aligned16(B_packed)))) return GP_ERR_ALIGNMENT;
+  if (scale_mode == GP_SCALE_ROWCOL_F32 && (!aligned16(scale_a) || !aligned16(scale_b))) return GP_ERR_ALIGNMENT;
+  if (scale_mode == GP_SCALE_BLOCK32_UE8M0 && !aligned16(scale_a)) return GP_ERR_ALIGNMENT;
+
+  DeviceInfo* d = nullptr;
+  if ((rc = device_info(&d)) != GP_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (K == 0) {  // empty sum: C = 0
+    return cudaMemsetAsync(C, 0, (size_t)M * (size_t)N * c_elem, st) == cudaSuccess ? GP_OK : GP_ERR_CUDA;
+  }
+
+  if (dtype == GP_INT8) {
+    CUtensorMap tmA;
+    if ((rc = encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, (uint64_t)kb, (uint64_t)M, (uint64_t)kb, 128, 16,
+                        CU_TENSOR_MAP_SWIZZLE_128B)) != GP_OK)
+      return rc;
+    I8Params p{};
+    p.Bp = static_cast<const uint8_t*>(B_packed);
+    p.C = static_cast<int32_t*>(C);
+    p.status = d->status;
+    p.wait_limit_ns = wait_limit_ns();
+    p.M = (int)M;
+    p.N = (int)N;
+    p.K = (int)K;
+    p.ktiles = (int)(kb / 128);
+    return i8_gemm_launch(tmA, p, d->num_sms, st);
+  }
+
+  CUtensorMap tmA, tmC;
+  if ((rc = encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, (uint64_t)kb, (uint64_t)M, (uint64_t)kb, 128, 128,
+                      CU_TENSOR_MAP_SWIZZLE_128B)) != GP_OK)
+    return rc;
+  if ((rc = encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, C, (uint64_t)N, (uint64_t)M, (uint64_t)N * 2, 64, 32,
+                      CU_TENSOR_MAP_SWIZZLE_128B)) != GP_OK)
+    return rc;
+  TcParams p{};
+  p.Bp = static_cast<const uint8_t*>(B_packed);
+  p.status = d->status;
+  p.wait_limit_ns = wait_limit_ns();
+  p.M = (int)M;
+  p.N = (int)N;
+  p.K = (int)K;
+  p.ktiles = (int)(kb / 128);
+  p.debug_skip_load = g_debug_skip_load.exchange(0);
+  if (scale_mode == GP_SCALE_ROWCOL_F32) {
+    p.sa = static_cast<const float*>(scale_a);
+    p.sb = static_cast<const float*>(scale_b);
+  }
+  if (dtype == GP_E2M1) {
+    p.Bsf = p.Bp + (size_t)N * (size_t)kb;
+    p.sfa = static_cast<const uint8_t*>(scale_a);
+    CUtensorMap tmSFA;
+    // A's UE8M0 scales [M, K/32]: 16-byte boxes (16 K blocks = two K steps) of 128 rows
+    if ((rc = encode_2d(&tmSFA, CU_TENSOR_MAP_DATA_TYPE_UINT8, scale_a, (uint64_t)(K / 32), (uint64_t)M,
+                        (uint64_t)(K / 32), 16, 128, CU_TENSOR_MAP_SWIZZLE_NONE)) != GP_OK)
+      return rc;
+    return mxf4_gemm_launch(tmA, tmC, tmSFA, p, d->num_sms, st);
+  }
+  const int64_t tiles_256 = ((M + 127) / 128) * (N / 256);
+  const int bn = (N % 256 == 0 && tiles_256 >= d->num_sms) ? 256 : 128;
+  return tc_gemm_launch(dtype == GP_BF16 ? 0 : 1, bn, tmA, tmC, p, d->num_sms, st);
+}
+
+int gemm_last_device_status(void* stream) {
+  DeviceInfo* d = nullptr;
+  int rc = device_info(&d);
+  if (rc != GP_OK) return rc;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return GP_ERR_CUDA;
+  uint32_t word = 0;
+  if (cudaMemcpy(&word, d->status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return GP_ERR_CUDA;
+  if (word != 0) {
+    const uint32_t zero = 0;
+    if (cudaMemcpy(d->status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return GP_ERR_CUDA;
+    return GP_ERR_DEVICE_TIMEOUT;
+  }
+  return GP_OK;
+}
+
+// Test hook: the next tcgen05 GEMM launch skips the producer's `index`-th
+// stage load (1-based), so its bounded waits time out.  0 disables it.
+int gemm_debug_skip_load(int index) {
+  if (index < 0) return GP_ERR_INVALID_ARG;
+  g_debug_skip_load.store(index);
+  return GP_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,47 @@
+// Internal interface between the C ABI layer (api.cu) and the kernels.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/gemm_preshuffle.h"
+
+namespace gp {
+
+struct TcParams {
+  const uint8_t* Bp;      // packed B (data region)
+  const uint8_t* Bsf;     // packed B scales (E2M1 only)
+  const uint8_t* sfa;     // A scales, UE8M0 [M, K/32] row-major (E2M1 only)
+  const float* sa;        // fp32 [M] row scales or null
+  const float* sb;        // fp32 [N] column scales or null
+  uint32_t* status;       // device status word
+  uint64_t wait_limit_ns; // bounded-wait limit
+  int M, N, K;            // K in elements
+  int ktiles;             // row bytes / 128
+  int tiles_m, tiles_n, num_tiles;
+  int debug_skip_load;    // 0 = off; i > 0: the producer skips its i-th stage load
+};
+
+struct I8Params {
+  const uint8_t* Bp;      // packed B
+  int32_t* C;             // [M, N] int32
+  uint32_t* status;
+  uint64_t wait_limit_ns;
+  int M, N, K;
+  int ktiles;             // K / 128
+  int strip;              // rows of B per CTA (multiple of 16)
+  int stages;
+};
+
+int tc_gemm_launch(int kind, int bn, const CUtensorMap& tmA, const CUtensorMap& tmC, TcParams p, int num_sms,
+                   cudaStream_t stream);
+int mxf4_gemm_launch(const CUtensorMap& tmA, const CUtensorMap& tmC, const CUtensorMap& tmSFA, TcParams p,
+                     int num_sms, cudaStream_t stream);
+int i8_gemm_launch(const CUtensorMap& tmA, I8Params p, int num_sms, cudaStream_t stream);
+
+int pack_b_launch(const uint8_t* B, const uint8_t* Bsf, int64_t N, int64_t kbytes, int64_t nblk, uint8_t* out,
+                  cudaStream_t stream);
+int unpack_b_launch(const uint8_t* packed, int64_t N, int64_t kbytes, int64_t nblk, uint8_t* B, uint8_t* Bsf,
+                    cudaStream_t stream);
+
+}  // namespace gp

@@ -1,0 +1,98 @@
+// The offline preshuffle of B ("GEMM Optimization Guide", section 12: B is
+// permuted once so that the GEMM's loads of B need no shuffle) and its
+// inverse.
+//
+// Layout (this library's own; the guide's CDNA layout targets MFMA
+// registers):
+//   - B's bytes [N, Kb] are cut into 128-row x 128-byte tiles.  Tile
+//     (tn, tk) is the 16 KiB block tn*(Kb/128) + tk.
+//   - Row r of a tile lives at r*128.  Its 16-byte chunk c is stored at slot
+//     c ^ (r % 8).  This is the 128-byte-swizzled K-major image that tcgen05
+//     descriptors and TMA use, so one bulk copy lands a tile in shared memory
+//     ready for the MMA, and 8 rows reading the same chunk hit 8 distinct
+//     bank groups.
+//   - E2M1 block scales ([N, K/32] bytes) follow the data region.  Per
+//     (tn, tk) they take two 512-byte groups of four K blocks.  Inside a
+//     group, (row r, block j) is at (r%32)*16 + (r/32)*4 + j%4: the 32-lane
+//     x 16-byte image that tcgen05.cp copies into tensor memory.
+#include "kernels.h"
+
+namespace gp {
+
+__device__ __forceinline__ int64_t packed_chunk_offset(int64_t n, int64_t cc, int64_t ktiles) {
+  const int64_t tn = n >> 7, r = n & 127;
+  const int64_t tk = cc >> 3, c = cc & 7;
+  return (((tn * ktiles + tk) << 7) + r) * 128 + ((c ^ (r & 7)) << 4);
+}
+
+__device__ __forceinline__ int64_t packed_scale_offset(int64_t n, int64_t j, int64_t nblk) {
+  const int64_t tiles_k = nblk >> 3;
+  const int64_t tn = n >> 7, r = n & 127;
+  const int64_t tk = j >> 3, jj = j & 7;
+  const int64_t group = tn * (tiles_k * 2) + tk * 2 + (jj >> 2);
+  return group * 512 + (r & 31) * 16 + (r >> 5) * 4 + (jj & 3);
+}
+
+// One thread per 16-byte chunk of B.
+__global__ void pack_data_kernel(const uint4* __restrict__ B, int64_t N, int64_t kbytes, uint8_t* __restrict__ out) {
+  const int64_t chunks_per_row = kbytes >> 4;
+  const int64_t total = N * chunks_per_row;
+  const int64_t ktiles = kbytes >> 7;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t n = i / chunks_per_row, cc = i - n * chunks_per_row;
+    *reinterpret_cast<uint4*>(out + packed_chunk_offset(n, cc, ktiles)) = B[i];
+  }
+}
+
+__global__ void unpack_data_kernel(const uint8_t* __restrict__ in, int64_t N, int64_t kbytes, uint4* __restrict__ B) {
+  const int64_t chunks_per_row = kbytes >> 4;
+  const int64_t total = N * chunks_per_row;
+  const int64_t ktiles = kbytes >> 7;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t n = i / chunks_per_row, cc = i - n * chunks_per_row;
+    B[i] = *reinterpret_cast<const uint4*>(in + packed_chunk_offset(n, cc, ktiles));
+  }
+}
+
+__global__ void pack_scale_kernel(const uint8_t* __restrict__ S, int64_t N, int64_t nblk, uint8_t* __restrict__ out) {
+  const int64_t total = N * nblk;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t n = i / nblk, j = i - n * nblk;
+    out[packed_scale_offset(n, j, nblk)] = S[i];
+  }
+}
+
+__global__ void unpack_scale_kernel(const uint8_t* __restrict__ in, int64_t N, int64_t nblk, uint8_t* __restrict__ S) {
+  const int64_t total = N * nblk;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t n = i / nblk, j = i - n * nblk;
+    S[i] = in[packed_scale_offset(n, j, nblk)];
+  }
+}
+
+static int grid_for(int64_t total, int threads) {
+  int64_t g = (total + threads - 1) / threads;
+  if (g > 65536) g = 65536;
+  if (g < 1) g = 1;
+  return (int)g;
+}
+
+int pack_b_launch(const uint8_t* B, const uint8_t* Bsf, int64_t N, int64_t kbytes, int64_t nblk, uint8_t* out,
+                  cudaStream_t stream) {
+  const int64_t chunks = N * (kbytes >> 4);
+  pack_data_kernel<<<grid_for(chunks, 256), 256, 0, stream>>>(reinterpret_cast<const uint4*>(B), N, kbytes, out);
+  if (Bsf != nullptr)
+    pack_scale_kernel<<<grid_for(N * nblk, 256), 256, 0, stream>>>(Bsf, N, nblk, out + N * kbytes);
+  return cudaGetLastError() == cudaSuccess ? GP_OK : GP_ERR_CUDA;
+}
+
+int unpack_b_launch(const uint8_t* packed, int64_t N, int64_t kbytes, int64_t nblk, uint8_t* B, uint8_t* Bsf,
+                    cudaStream_t stream) {
+  const int64_t chunks = N * (kbytes >> 4);
+  unpack_data_kernel<<<grid_for(chunks, 256), 256, 0, stream>>>(packed, N, kbytes, reinterpret_cast<uint4*>(B));
+  if (Bsf != nullptr)
+    unpack_scale_kernel<<<grid_for(N * nblk, 256), 256, 0, stream>>>(packed + N * kbytes, N, nblk, Bsf);
+  return cudaGetLastError() == cudaSuccess ? GP_OK : GP_ERR_CUDA;
+}
+
+}  // namespace gp

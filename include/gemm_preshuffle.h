@@ -1,0 +1,173 @@
+/*
+ * gemm_preshuffle.h -- C ABI of the GB300 (sm_103a) preshuffle GEMM library.
+ *
+ *   C[M,N] = A[M,K] . B[N,K]^T
+ *
+ * "GEMM Optimization Guide", section 1.1: the product and its tiling.
+ * Section 12 (B matrix preshuffle layout): B is permuted once, offline, into
+ * a layout that the kernel's loads copy without further shuffling.  This
+ * library uses its own layout for that step, shaped for TMA and tcgen05.
+ *
+ * Conventions for every entry point:
+ *   - Device pointers are CUDA global-memory pointers that the caller owns.
+ *     The library never frees them and never keeps them after a call returns.
+ *   - `stream` is a cudaStream_t passed as void*.  NULL means the legacy
+ *     default stream.
+ *   - Calls are asynchronous with respect to the host and ordered on `stream`.
+ *   - Argument errors are detected on the host before anything is launched.
+ *     The call then returns a nonzero gp_status and leaves all buffers
+ *     untouched.
+ *   - Device-side timeouts of the bounded waits inside the GEMM kernels set
+ *     a sticky status word.  gemm_last_device_status() reads and clears it.
+ *   - Matrices are row-major and densely packed (row pitch = K elements for
+ *     A and B, N elements for C).
+ *   - Every device pointer must be 16-byte aligned.
+ *   - Thread safety: calls from several host threads are safe.  Each call
+ *     keeps its state on the stack, apart from a per-device table of SM
+ *     counts and function attributes, which is written once under a lock.
+ */
+#ifndef GEMM_PRESHUFFLE_H
+#define GEMM_PRESHUFFLE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes returned by every entry point. */
+typedef enum gp_status {
+  GP_OK = 0,
+  GP_ERR_INVALID_ARG = 1,     /* null pointer where one is required, bad enum */
+  GP_ERR_UNSUPPORTED = 2,     /* dtype / scale-mode / output combination not offered */
+  GP_ERR_SHAPE = 3,           /* dimension rule violated (see gemm_run) */
+  GP_ERR_ALIGNMENT = 4,       /* a pointer is not 16-byte aligned */
+  GP_ERR_CUDA = 5,            /* a CUDA runtime/driver call failed */
+  GP_ERR_DEVICE_TIMEOUT = 6   /* a bounded in-kernel wait gave up (see gemm_last_device_status) */
+} gp_status;
+
+/* Element types.  E4M3 is OCP E4M3FN.  E2M1 packs two codes per byte, with
+ * the even-k element in the low nibble. */
+typedef enum gp_dtype {
+  GP_BF16 = 0,
+  GP_E4M3 = 1,
+  GP_INT8 = 2,
+  GP_E2M1 = 3,
+  GP_INT32 = 4
+} gp_dtype;
+
+/* How operand scales enter the product. */
+typedef enum gp_scale_mode {
+  GP_SCALE_NONE = 0,          /* C = sum_k A*B */
+  GP_SCALE_ROWCOL_F32 = 1,    /* C[m,n] = (sum_k A*B) * scale_a[m] * scale_b[n], fp32 scales.
+                                 "GEMM Optimization Guide" section 7.1: the epilogue forms
+                                 acc * scale_a * scale_b; section 8.2 counts (M+N) fp32 scales. */
+  GP_SCALE_BLOCK32_UE8M0 = 2  /* MX block scaling: one UE8M0 exponent per 32 consecutive K
+                                 elements of each row of A and of B (section 8.2, MXFP4 bytes):
+                                 C = sum_j 2^(ea[m,j]-127) 2^(eb[n,j]-127) sum_{k in block j} A*B */
+} gp_scale_mode;
+
+/*
+ * Size in bytes of the packed B buffer for a [N, K] operand of `dtype`.
+ * The packed layout holds the same bytes as B, followed by B's packed block
+ * scales for E2M1, with no padding.
+ *
+ * Shape rules: N % 128 == 0 and K*element_bits/8 % 128 == 0.  For the
+ * element types that means K % 128 (E4M3, INT8), K % 64 (BF16) and K % 256
+ * (E2M1).  Returns GP_ERR_SHAPE otherwise.  Host-only call.
+ */
+int gemm_packed_b_bytes(int dtype, int64_t N, int64_t K, size_t* bytes_out);
+
+/*
+ * The offline preshuffle of B ("GEMM Optimization Guide" section 12).
+ *
+ * B         : device, [N, K] row-major in `dtype` (E2M1: [N, K/2] bytes).
+ * B_scales  : device, UE8M0 [N, K/32] row-major, required for E2M1 (NULL otherwise).
+ * B_packed  : device, gemm_packed_b_bytes() bytes, written entirely.
+ *
+ * Layout of the packed buffer (a bijection of B's bytes):
+ *   - B's bytes are cut into tiles of 128 rows x 128 bytes.  The tile of
+ *     (row band tn, byte column tk) is the 16 KiB block with index
+ *     tn*(Kb/128)+tk, where Kb = row bytes.
+ *   - Inside a tile, row r sits at r*128.  Its 16-byte chunk c is stored at
+ *     chunk slot c ^ (r % 8).  That is the 128-byte-swizzled K-major image
+ *     that tcgen05 and TMA use, so one bulk copy moves a tile into shared
+ *     memory ready for the MMA.
+ *   - For E2M1, the block scales follow the data.  They are packed per
+ *     (row band, 128-byte K tile) in two 512-byte groups of four K blocks.
+ *     In a group, the byte for (row r, block j) is at
+ *     (r%32)*16 + (r/32)*4 + j%4.
+ * The call runs one device kernel on `stream`.
+ */
+int gemm_preshuffle_b(const void* B, const void* B_scales, int dtype, int64_t N, int64_t K,
+                      void* B_packed, void* stream);
+
+/*
+ * The inverse of gemm_preshuffle_b.  It rebuilds B (and, for E2M1, B_scales)
+ * from a packed buffer, for round-trip checks.  B_scales_out may be NULL
+ * except for E2M1.
+ */
+int gemm_unpack_b(const void* B_packed, int dtype, int64_t N, int64_t K, void* B_out,
+                  void* B_scales_out, void* stream);
+
+/*
+ * C = A . B^T with B pre-packed ("GEMM Optimization Guide" sections 1-7).
+ *
+ * A        : device, [M, K] row-major in `dtype` (E2M1: [M, K/2] bytes).
+ * B_packed : device, output of gemm_preshuffle_b for the same dtype, N, K.
+ * scale_a, scale_b : device, per `scale_mode`.  NULL for GP_SCALE_NONE.
+ *            ROWCOL_F32: fp32 [M] and fp32 [N].
+ *            BLOCK32_UE8M0: scale_a is UE8M0 [M, K/32] row-major (plain,
+ *            not packed), and scale_b must be NULL because B's scales live
+ *            in B_packed.
+ * C        : device, [M, N] row-major in `c_dtype`, written entirely.
+ *
+ * Supported (dtype, scale_mode, c_dtype) combinations:
+ *   (GP_BF16, GP_SCALE_NONE,          GP_BF16)   fp32 accumulation in TMEM
+ *   (GP_E4M3, GP_SCALE_ROWCOL_F32,    GP_BF16)   fp32 accumulation, scales in epilogue
+ *   (GP_E4M3, GP_SCALE_NONE,          GP_BF16)
+ *   (GP_E2M1, GP_SCALE_BLOCK32_UE8M0, GP_BF16)   block scales applied inside the MMA
+ *   (GP_INT8, GP_SCALE_NONE,          GP_INT32)  exact integer result
+ * Other combinations return GP_ERR_UNSUPPORTED.
+ *
+ * Shape rules: M >= 1 (any value), N and K as for gemm_packed_b_bytes, and
+ * M, N, K < 2^31.  For INT8 the exact result must fit int32, which holds for
+ * every input when K <= 131072.
+ * Float outputs are rounded to nearest-even from the fp32 value.
+ * The call launches one kernel and allocates no memory.  K == 0 writes
+ * zeros to C with an async memset.  M == 0 or N == 0 is a no-op.
+ */
+int gemm_run(const void* A, const void* B_packed, int dtype, int64_t M, int64_t N, int64_t K,
+             int scale_mode, const void* scale_a, const void* scale_b, void* C, int c_dtype,
+             void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the library's device status
+ * word on the current device.  The word is set when a bounded wait in a GEMM
+ * kernel times out.  Returns GP_OK, GP_ERR_DEVICE_TIMEOUT or GP_ERR_CUDA.
+ */
+int gemm_last_device_status(void* stream);
+
+/* Static, human-readable name of a gp_status value. */
+const char* gemm_status_string(int status);
+
+/*
+ * Fault-injection hook for tests of the bounded waits; it has no
+ * counterpart in the method.  The next tcgen05 GEMM launched by gemm_run
+ * skips its producer's `index`-th shared-memory stage load (1-based).  The
+ * MMA warp's wait for that stage then times out after the wait limit, which
+ * defaults to 2 s and is overridden by the environment variable
+ * GP_WAIT_LIMIT_MS, read once per process.
+ *
+ * When the wait times out, the kernel drains its in-flight copies, frees
+ * its tensor memory and exits.  The library's status word is set, and
+ * gemm_last_device_status() reports GP_ERR_DEVICE_TIMEOUT.  The hook
+ * disarms itself after one launch.  index = 0 disarms it.  Host-only.
+ */
+int gemm_debug_skip_load(int index);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GEMM_PRESHUFFLE_H */

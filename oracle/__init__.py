@@ -163,9 +163,14 @@ def gemm_bf16(a_bits: np.ndarray, b_bits: np.ndarray) -> np.ndarray:
 
 def gemm_e4m3_rowcol(qa: np.ndarray, qb: np.ndarray, sa: np.ndarray, sb: np.ndarray) -> np.ndarray:
     """C[m,n] = (sum_k qa[m,k] qb[n,k]) * sa[m] * sb[n]: the accumulator is
-    scaled by the row scale of A and the column scale (row of B)."""
+    scaled by the row scale of A and the column scale (row of B).  Missing
+    scales (None) mean an unscaled product."""
     acc = gemm_f64(decode_e4m3(qa), decode_e4m3(qb))
-    return acc * np.asarray(sa, np.float64)[:, None] * np.asarray(sb, np.float64)[None, :]
+    if sa is not None:
+        acc = acc * np.asarray(sa, np.float64)[:, None]
+    if sb is not None:
+        acc = acc * np.asarray(sb, np.float64)[None, :]
+    return acc
 
 
 def gemm_mxfp4(pa: np.ndarray, pb: np.ndarray, ea: np.ndarray, eb: np.ndarray, K: int) -> np.ndarray:
@@ -369,8 +374,8 @@ def tflops(M: int, N: int, K: int, us: float) -> float:
 # CPU baseline timing helper (used by bench.py's cpu_baseline leg only)
 # ----------------------------------------------------------------------------
 
-def time_gemm(ops, rows: np.ndarray) -> float:
-    """Wall-clock seconds for the reference C of the given output rows."""
+def time_gemm(ops, rows: np.ndarray, cols: Optional[np.ndarray] = None) -> float:
+    """Wall-clock seconds for the reference C of the given output rows (and columns)."""
     t0 = time.perf_counter()
-    gemm_operands(ops, rows=rows)
+    gemm_operands(ops, rows=rows, cols=cols)
     return time.perf_counter() - t0

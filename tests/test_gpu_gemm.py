@@ -1,0 +1,192 @@
+"""GPU parity: the CUDA path, called through the C ABI, against the CPU oracle.
+
+The tolerance metric is max |C - C_ref| / (|C_ref| + 1e-2) <= 8e-3 for bf16
+outputs, and INT8 must be bit-exact.  Inputs come from the seeded generator
+shared with the oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import dense_gemm_preshuffle_gb300 as gp
+from dense_gemm_preshuffle_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+TOL = 8e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from dense_gemm_preshuffle_gb300 import build
+    build.build()
+    gp.load_library()
+
+
+def dev(ops):
+    """Device tensors of an Operands bundle (raw bytes / codes)."""
+    def t(x):
+        if x is None:
+            return None
+        if x.dtype == np.uint16:
+            x = x.view(np.int16)
+        return torch.from_numpy(np.ascontiguousarray(x)).cuda()
+    return t(ops.a), t(ops.b), t(ops.scale_a), t(ops.scale_b)
+
+
+def gpu_gemm(ops, out=None):
+    A, B, sa, sb = dev(ops)
+    if ops.dtype == "e2m1":
+        Bp = gp.preshuffle_b(B, "e2m1", B_scales=sb)
+        C = gp.matmul(A, Bp, "e2m1", ops.N, ops.K, scale_a=sa, out=out)
+    else:
+        Bp = gp.preshuffle_b(B, ops.dtype)
+        C = gp.matmul(A, Bp, ops.dtype, ops.N, ops.K, scale_a=sa, scale_b=sb, out=out)
+    torch.cuda.synchronize()
+    assert gp.gemm_last_device_status() == 0
+    return C
+
+
+def as_host(C):
+    if C.dtype == torch.int32:
+        return C.cpu().numpy().astype(np.int64)
+    return C.float().cpu().numpy().astype(np.float64)
+
+
+def check(ops, C, rows=None):
+    c = as_host(C)
+    ref = oracle.gemm_operands(ops, rows=rows)
+    if rows is not None:
+        c = c[rows]
+    if ops.dtype == "int8":
+        assert np.array_equal(c, ref), f"{int((c != ref).sum())} mismatching int32 outputs"
+    else:
+        err = oracle.max_rel_err(c, ref)
+        assert err <= TOL, f"max rel err {err:.3e}"
+        return err
+
+
+# ---------------------------------------------------------------- packing
+
+@pytest.mark.parametrize("dtype,N,K", [("e4m3", 256, 512), ("int8", 384, 1024), ("bf16", 128, 192),
+                                       ("e2m1", 256, 1024), ("int8", 7168, 4096)])
+def test_pack_matches_oracle_layout_and_roundtrips(dtype, N, K):
+    ops = inputs.make_operands(dtype, 1, N, K, seed=123)
+    _, B, _, sb = dev(ops)
+    Bp = gp.preshuffle_b(B, dtype, B_scales=sb if dtype == "e2m1" else None)
+    expect = oracle.pack_b(ops.b, dtype, scales=ops.scale_b)
+    assert np.array_equal(Bp.cpu().numpy(), expect)
+    back = torch.empty_like(B)
+    back_s = torch.empty_like(sb) if dtype == "e2m1" else None
+    gp.gemm_unpack_b(Bp, dtype, N, K, back, back_s)
+    torch.cuda.synchronize()
+    assert torch.equal(back, B)
+    if dtype == "e2m1":
+        assert torch.equal(back_s, sb)
+
+
+# ---------------------------------------------------------------- small and ragged shapes
+
+SMALL = [
+    ("e4m3", 1, 128, 128), ("e4m3", 300, 512, 1024), ("e4m3", 129, 256, 256), ("e4m3", 17, 384, 640),
+    ("e4m3", 1000, 1024, 512),
+    ("bf16", 257, 384, 512), ("bf16", 128, 128, 64), ("bf16", 64, 256, 4096), ("bf16", 700, 640, 320),
+    ("int8", 1, 128, 128), ("int8", 37, 256, 384), ("int8", 16, 384, 256), ("int8", 100, 1152, 1280),
+    ("int8", 16, 7168, 4096),
+]
+
+
+@pytest.mark.parametrize("dtype,M,N,K", SMALL, ids=lambda v: str(v))
+def test_small_and_ragged(dtype, M, N, K):
+    ops = inputs.make_operands(dtype, M, N, K, seed=1000 + M + N + K)
+    check(ops, gpu_gemm(ops))
+
+
+def test_e4m3_without_scales():
+    ops = inputs.make_operands("e4m3", 200, 256, 384, seed=5)
+    ops.scale_a = ops.scale_b = None
+    check(ops, gpu_gemm(ops))
+
+
+# ---------------------------------------------------------------- the five workloads
+
+def sample_rows(M, n=32, seed=0):
+    rng = np.random.default_rng(seed)
+    r = set(rng.choice(M, size=min(n, M), replace=False).tolist())
+    r.update({0, M - 1})
+    return np.array(sorted(r))
+
+
+@pytest.mark.parametrize("name", ["fp8_128x256x512", "int8_16x7168x4096", "bf16_512x4096x4096"])
+def test_workload_full_compare(name):
+    ops = inputs.workload_operands(name)
+    check(ops, gpu_gemm(ops))
+
+
+@pytest.mark.parametrize("name", ["fp8_8192x8192x8192"])
+def test_workload_sampled_rows(name):
+    ops = inputs.workload_operands(name)
+    C = gpu_gemm(ops)
+    check(ops, C, rows=sample_rows(ops.M, 24, seed=1))
+    # whole-output properties at full size: finite everywhere
+    assert torch.isfinite(C.float()).all()
+
+
+# ---------------------------------------------------------------- edge cases
+
+def test_int8_extremes_bit_exact():
+    M, N, K = 16, 256, 4096
+    a = np.full((M, K), -128, np.int8)
+    b = np.full((N, K), -128, np.int8)
+    a[1] = 127
+    b[1] = 127
+    a[2, ::2] = 127          # alternating signs: large cancellation
+    b[2, 1::2] = -127
+    rng = np.random.default_rng(0)
+    a[3:] = rng.choice(np.array([-128, 127, 0, 1, -1], np.int8), size=(M - 3, K))
+    ops = inputs.Operands("int8", M, N, K, a, b)
+    check(ops, gpu_gemm(ops))
+
+
+def test_k_zero_gives_zeros():
+    C = torch.full((5, 128), 7.0, dtype=torch.bfloat16, device="cuda")
+    dummy = torch.empty(16, dtype=torch.uint8, device="cuda")
+    gp.gemm_run(dummy, dummy, "bf16", 5, 128, 0, "none", None, None, C, "bf16")
+    torch.cuda.synchronize()
+    assert (C == 0).all()
+
+
+def test_guard_bands_untouched():
+    ops = inputs.make_operands("e4m3", 77, 256, 512, seed=9)
+    M, N = ops.M, ops.N
+    guard = 4096
+    buf = torch.full((M * N + 2 * guard,), -3.0, dtype=torch.bfloat16, device="cuda")
+    C = buf[guard:guard + M * N].view(M, N)
+    gpu_gemm(ops, out=C)
+    assert (buf[:guard] == -3.0).all() and (buf[guard + M * N:] == -3.0).all()
+    check(ops, C)
+    ops8 = inputs.make_operands("int8", 19, 384, 256, seed=9)
+    buf8 = torch.full((19 * 384 + 2 * guard,), -7, dtype=torch.int32, device="cuda")
+    C8 = buf8[guard:guard + 19 * 384].view(19, 384)
+    gpu_gemm(ops8, out=C8)
+    assert (buf8[:guard] == -7).all() and (buf8[guard + 19 * 384:] == -7).all()
+    check(ops8, C8)
+
+
+def test_repeatable_bitwise():
+    ops = inputs.make_operands("e4m3", 512, 1024, 1024, seed=2)
+    A, B, sa, sb = dev(ops)
+    Bp = gp.preshuffle_b(B, "e4m3")
+    first = gp.matmul(A, Bp, "e4m3", ops.N, ops.K, sa, sb)
+    for _ in range(20):
+        again = gp.matmul(A, Bp, "e4m3", ops.N, ops.K, sa, sb)
+        assert torch.equal(again.view(torch.int16), first.view(torch.int16))
+    ops8 = inputs.make_operands("int8", 16, 7168, 4096, seed=3)
+    A8, B8, _, _ = dev(ops8)
+    Bp8 = gp.preshuffle_b(B8, "int8")
+    f8 = gp.matmul(A8, Bp8, "int8", ops8.N, ops8.K)
+    for _ in range(20):
+        assert torch.equal(gp.matmul(A8, Bp8, "int8", ops8.N, ops8.K), f8)
