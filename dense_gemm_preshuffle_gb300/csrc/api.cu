@@ -216,10 +216,6 @@ int gemm_run(const void* A, const void* B_packed, int dtype, int64_t M, int64_t 
   }
 
   if (dtype == GP_INT8) {
-    CUtensorMap tmA;
-    if ((rc = encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, (uint64_t)kb, (uint64_t)M, (uint64_t)kb, 128, 16,
-                        CU_TENSOR_MAP_SWIZZLE_128B)) != GP_OK)
-      return rc;
     I8Params p{};
     p.Bp = static_cast<const uint8_t*>(B_packed);
     p.C = static_cast<int32_t*>(C);
@@ -229,7 +225,7 @@ int gemm_run(const void* A, const void* B_packed, int dtype, int64_t M, int64_t 
     p.N = (int)N;
     p.K = (int)K;
     p.ktiles = (int)(kb / 128);
-    return i8_gemm_launch(tmA, p, d->num_sms, st);
+    return i8_gemm_launch(static_cast<const uint8_t*>(A), p, d->num_sms, st);
   }
 
   CUtensorMap tmA, tmC;
@@ -253,14 +249,10 @@ int gemm_run(const void* A, const void* B_packed, int dtype, int64_t M, int64_t 
     p.sb = static_cast<const float*>(scale_b);
   }
   if (dtype == GP_E2M1) {
+    if (N % 256 != 0) return GP_ERR_SHAPE;
     p.Bsf = p.Bp + (size_t)N * (size_t)kb;
     p.sfa = static_cast<const uint8_t*>(scale_a);
-    CUtensorMap tmSFA;
-    // A's UE8M0 scales [M, K/32]: 16-byte boxes (16 K blocks = two K steps) of 128 rows
-    if ((rc = encode_2d(&tmSFA, CU_TENSOR_MAP_DATA_TYPE_UINT8, scale_a, (uint64_t)(K / 32), (uint64_t)M,
-                        (uint64_t)(K / 32), 16, 128, CU_TENSOR_MAP_SWIZZLE_NONE)) != GP_OK)
-      return rc;
-    return mxf4_gemm_launch(tmA, tmC, tmSFA, p, d->num_sms, st);
+    return mxf4_gemm_launch(tmA, tmC, p, d->num_sms, st);
   }
   const int64_t tiles_256 = ((M + 127) / 128) * (N / 256);
   const int bn = (N % 256 == 0 && tiles_256 >= d->num_sms) ? 256 : 128;

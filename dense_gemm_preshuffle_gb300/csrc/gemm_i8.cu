@@ -36,14 +36,19 @@
 //     8 distinct bank groups.
 //   - The 8 warps' int32 partials are reduced through shared memory and
 //     stored as coalesced int32 rows of C.
+#include <cstdlib>
+
 #include "kernels.h"
 #include "ptx.cuh"
 
 namespace gp {
 
-constexpr int I8_CW = 8;                     // consumer warps
-constexpr int I8_THREADS = 32 * (I8_CW + 1);  // + one producer warp
-constexpr int I8_RING_BUDGET = 192 * 1024;
+constexpr int I8_CW = 8;  // warps per CTA, each with a private copy ring
+constexpr int I8_THREADS = 32 * I8_CW;
+// Two CTAs fit on one SM (registers <= 128/thread, shared memory <= 113 KiB),
+// so with programmatic dependent launch the next GEMM's CTAs sit beside this
+// one's and warm L2 with their weights while this one computes.
+constexpr int I8_CTAS_PER_SM = 2;
 
 __device__ __forceinline__ void i8x4_to_f16x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
   const uint32_t u = w ^ 0x80808080u;  // each byte b -> b + 128 in [0, 255]
@@ -56,84 +61,88 @@ __device__ __forceinline__ void i8x4_to_f16x2(uint32_t w, uint32_t& lo, uint32_t
   asm("sub.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(h), "r"(0x64806480u));
 }
 
+// Pure function of its register operands (no side effects), so ptxas may
+// interleave independent accumulator chains freely.
 __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                           uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-template <int NB8>
-__global__ void __launch_bounds__(I8_THREADS, 1) i8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, I8Params p) {
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Copy K tile `kt` (the 16 x 128-byte A tile and the strip's rows of the
+// packed B tile) into a warp-private ring slot.  A rows >= M read as zeros.
+// The A tile gets the 128-byte swizzle (chunk c of row r at slot c ^ (r%8));
+// the packed B rows already carry it.
+template <int SN>
+__device__ __forceinline__ void i8_copy_ktile(const I8Params& p, const uint8_t* A, int mg, int n0, int rows, int kt,
+                                              uint32_t slot, int lane) {
+  const size_t kb = (size_t)p.ktiles * 128;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int i = lane + 32 * j;
+    const int row = i >> 3, c = i & 7;
+    const int gm = mg * 16 + row;
+    const bool valid = gm < p.M;
+    cp_async_16(slot + row * 128 + ((c ^ (row & 7)) << 4), A + (size_t)(valid ? gm : 0) * kb + kt * 128 + c * 16,
+                valid ? 16u : 0u);
+  }
+  const uint32_t sb = slot + 2048;
+#pragma unroll 4
+  for (int i = lane; i < rows * 8; i += 32) {
+    const int row = i >> 3, c = i & 7;
+    const int r = n0 + row;
+    cp_async_16(sb + row * 128 + c * 16,
+                p.Bp + (((size_t)(r >> 7) * p.ktiles + kt) * 128 + (r & 127)) * 128 + c * 16, 16u);
+  }
+}
+
+template <int NB8, int R>
+__global__ void __launch_bounds__(I8_THREADS, I8_CTAS_PER_SM) i8_gemm_kernel(const uint8_t* __restrict__ A, I8Params p) {
   constexpr int SN = NB8 * 8;
   constexpr int STAGE = 2048 + SN * 128;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int stages = p.stages;
-  const int ring = stages * STAGE;
-  const int red_bytes = I8_CW * 16 * SN * 4;
-  uint64_t* full = reinterpret_cast<uint64_t*>(base + (ring > red_bytes ? ring : red_bytes));
-  uint64_t* empty = full + stages;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + stages);
-
+  extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int n0 = blockIdx.x * SN;
   const int rows = min(SN, p.N - n0);  // multiple of 16
   const int mg = blockIdx.y;
+  const uint32_t ring = smem_u32(smem) + (uint32_t)(warp * R * STAGE);
 
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < stages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
-    }
-    *abort_flag = 0;
-    fence_mbar_init();
-    prefetch_tensormap(&tmA);
-  }
-  __syncthreads();
-
-  if (warp == I8_CW) {
-    // ------------------------------------------------------------ producer
+  // Warm L2 with this warp's share of the weight strip while the previous
+  // kernel on the stream may still run: a prefetch is only a cache hint.
+  for (int kt = warp; kt < p.ktiles; kt += I8_CW) {
     if (lane == 0) {
-      const uint64_t pol_b = policy_evict_first();
-      uint32_t issued = 0;
-      bool ok = true;
-      for (int kt = 0; kt < p.ktiles; ++kt) {
-        const int s = kt % stages;
-        const uint32_t ph = (uint32_t)(kt / stages) & 1;
-        if (!wait_bounded(&empty[s], ph ^ 1, abort_flag, p.status, ST_TIMEOUT_PRODUCER, p.wait_limit_ns)) {
-          ok = false;
-          break;
-        }
-        uint8_t* st = base + s * STAGE;
-        mbar_arrive_expect_tx(&full[s], 2048u + (uint32_t)rows * 128u);
-        tma_load_2d(st, &tmA, kt * 128, mg * 16, &full[s]);
-        int r = n0;
-        while (r < n0 + rows) {
-          const int tn = r >> 7;
-          const int r_end = min(n0 + rows, (tn + 1) << 7);
-          bulk_load_hint(st + 2048 + (r - n0) * 128,
-                         p.Bp + ((size_t)tn * p.ktiles + kt) * 16384 + (size_t)(r & 127) * 128,
-                         (uint32_t)(r_end - r) * 128u, &full[s], pol_b);
-          r = r_end;
-        }
-        ++issued;
-      }
-      if (!ok) {
-        const uint32_t n = issued < (uint32_t)stages ? issued : (uint32_t)stages;
-        for (uint32_t i = 0; i < n; ++i) {
-          const uint32_t q = issued - 1 - i;
-          volatile int never = 0;
-          wait_bounded(&full[q % stages], (q / stages) & 1, &never, p.status, ST_TIMEOUT_DRAIN, p.wait_limit_ns);
-        }
+      int r = n0;
+      while (r < n0 + rows) {
+        const int tn = r >> 7;
+        const int r_end = min(n0 + rows, (tn + 1) << 7);
+        prefetch_l2_bulk(p.Bp + ((size_t)tn * p.ktiles + kt) * 16384 + (size_t)(r & 127) * 128,
+                         (uint32_t)(r_end - r) * 128u);
+        r = r_end;
       }
     }
-    return;  // the producer takes no part in the reduction below
+  }
+  pdl_launch_dependents();
+  pdl_wait();  // A may be produced, and C read, by the previous kernel
+
+  // Prologue: R K tiles of this warp in flight (one commit group each).
+#pragma unroll
+  for (int q = 0; q < R; ++q) {
+    const int kt = warp + q * I8_CW;
+    if (kt < p.ktiles) i8_copy_ktile<SN>(p, A, mg, n0, rows, kt, ring + q * STAGE, lane);
+    cp_async_commit();
   }
 
-  // ------------------------------------------------------------ consumers
   const int g = lane >> 2;  // mma group id: A rows g, g+8 and B row g of each 8-row block
   const int t = lane & 3;
   const int nb_valid = rows >> 3;
@@ -141,53 +150,65 @@ __global__ void __launch_bounds__(I8_THREADS, 1) i8_gemm_kernel(const __grid_con
 #pragma unroll
   for (int nb = 0; nb < NB8; ++nb) acc[nb][0] = acc[nb][1] = acc[nb][2] = acc[nb][3] = 0;
 
+  int q = 0;
   for (int kt = warp; kt < p.ktiles; kt += I8_CW) {
-    const int s = kt % stages;
-    const uint32_t ph = (uint32_t)(kt / stages) & 1;
-    if (!wait_bounded(&full[s], ph, abort_flag, p.status, ST_TIMEOUT_CONSUMER, p.wait_limit_ns)) break;
-    const uint32_t sa = smem_u32(base + s * STAGE);
-    const uint32_t sb = sa + 2048;
+    cp_async_wait<R - 1>();  // this lane's copies of the oldest tile are done
+    __syncwarp();            // ... and every other lane's
+    const uint8_t* sa = smem + (size_t)warp * R * STAGE + q * STAGE;
+    const uint8_t* sbp = sa + 2048;
+    const uint32_t slot_addr = ring + q * STAGE;
+    const int kn = kt + R * I8_CW;
+    q = (q + 1 == R) ? 0 : q + 1;
     float f[NB8][4];
 #pragma unroll
     for (int nb = 0; nb < NB8; ++nb) f[nb][0] = f[nb][1] = f[nb][2] = f[nb][3] = 0.f;
+    // Two 64-element halves of the K tile; only one half's raw bytes are live.
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      const uint32_t slot = (uint32_t)(((2 * t + h) ^ g) << 4);
-      uint32_t ag[4], ag8[4];
-      ld_shared_v4(sa + g * 128 + slot, ag[0], ag[1], ag[2], ag[3]);
-      ld_shared_v4(sa + (g + 8) * 128 + slot, ag8[0], ag8[1], ag8[2], ag8[3]);
+      const int slot = ((2 * t + h) ^ g) << 4;
+      const uint4 ag = *reinterpret_cast<const uint4*>(sa + g * 128 + slot);
+      const uint4 ag8 = *reinterpret_cast<const uint4*>(sa + (g + 8) * 128 + slot);
+      uint4 bw[NB8];
+#pragma unroll
+      for (int nb = 0; nb < NB8; ++nb)
+        if (nb < nb_valid) bw[nb] = *reinterpret_cast<const uint4*>(sbp + (nb * 8 + g) * 128 + slot);
+      if (h == 1) {
+        __syncwarp();  // the slot is free: refill it with this warp's tile R steps ahead
+        if (kn < p.ktiles) i8_copy_ktile<SN>(p, A, mg, n0, rows, kn, slot_addr, lane);
+        cp_async_commit();
+      }
+      const uint32_t aw[4] = {ag.x, ag.y, ag.z, ag.w};
+      const uint32_t a8w[4] = {ag8.x, ag8.y, ag8.z, ag8.w};
       uint32_t alo[4], ahi[4], a8lo[4], a8hi[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        i8x4_to_f16x2(ag[j], alo[j], ahi[j]);
-        i8x4_to_f16x2(ag8[j], a8lo[j], a8hi[j]);
+        i8x4_to_f16x2(aw[j], alo[j], ahi[j]);
+        i8x4_to_f16x2(a8w[j], a8lo[j], a8hi[j]);
       }
 #pragma unroll
       for (int nb = 0; nb < NB8; ++nb) {
         if (nb < nb_valid) {
-          uint32_t bw[4];
-          ld_shared_v4(sb + (nb * 8 + g) * 128 + slot, bw[0], bw[1], bw[2], bw[3]);
+          const uint32_t w[4] = {bw[nb].x, bw[nb].y, bw[nb].z, bw[nb].w};
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             uint32_t blo, bhi;
-            i8x4_to_f16x2(bw[j], blo, bhi);
+            i8x4_to_f16x2(w[j], blo, bhi);
             mma_16816(f[nb], alo[j], a8lo[j], ahi[j], a8hi[j], blo, bhi);
           }
         }
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
 #pragma unroll
     for (int nb = 0; nb < NB8; ++nb) {
 #pragma unroll
       for (int i = 0; i < 4; ++i) acc[nb][i] += __float2int_rn(f[nb][i]);
     }
   }
+  cp_async_wait<0>();
 
   // ------------------------------------------------------------ reduction
-  named_bar_sync(1, I8_CW * 32);  // every consumer is done with the ring
-  int32_t* red = reinterpret_cast<int32_t*>(base);  // [CW][16][SN]
+  __syncthreads();  // every warp is done with its ring
+  int32_t* red = reinterpret_cast<int32_t*>(smem);  // [CW][16][SN]
 #pragma unroll
   for (int nb = 0; nb < NB8; ++nb) {
     const int col = nb * 8 + 2 * t;
@@ -196,8 +217,8 @@ __global__ void __launch_bounds__(I8_THREADS, 1) i8_gemm_kernel(const __grid_con
     red[(warp * 16 + g + 8) * SN + col] = acc[nb][2];
     red[(warp * 16 + g + 8) * SN + col + 1] = acc[nb][3];
   }
-  named_bar_sync(1, I8_CW * 32);
-  for (int i = threadIdx.x; i < 16 * rows; i += I8_CW * 32) {
+  __syncthreads();
+  for (int i = threadIdx.x; i < 16 * rows; i += I8_THREADS) {
     const int m = i / rows, n = i - m * rows;
     int sum = 0;
 #pragma unroll
@@ -207,44 +228,63 @@ __global__ void __launch_bounds__(I8_THREADS, 1) i8_gemm_kernel(const __grid_con
   }
 }
 
-template <int NB8>
-static int launch_i8(const CUtensorMap& tmA, I8Params p, dim3 grid, cudaStream_t stream) {
+// Tuning overrides, read once per process: GP_I8_STRIP (rows of B per CTA:
+// 16, 32, 48 or 64).
+static int env_int(const char* name, int dflt) {
+  const char* e = std::getenv(name);
+  if (e == nullptr) return dflt;
+  const int v = std::atoi(e);
+  return v > 0 ? v : dflt;
+}
+
+template <int NB8, int R>
+static int launch_i8(const uint8_t* A, I8Params p, dim3 grid, cudaStream_t stream) {
   constexpr int STAGE = 2048 + NB8 * 8 * 128;
-  int stages = I8_RING_BUDGET / STAGE;
-  if (stages > p.ktiles) stages = p.ktiles;
-  if (stages < 1) stages = 1;
-  p.stages = stages;
-  const int ring = stages * STAGE;
-  const int red = I8_CW * 16 * NB8 * 8 * 4;
-  const int smem = (ring > red ? ring : red) + 2 * stages * 8 + 16 + 1024;
-  auto kern = i8_gemm_kernel<NB8>;
-  // the attribute is set once per device to the largest size this launcher uses
+  constexpr int RING = I8_CW * R * STAGE;
+  constexpr int RED = I8_CW * 16 * NB8 * 8 * 4;
+  constexpr int SMEM = RING > RED ? RING : RED;
+  static_assert(SMEM <= 227 * 1024, "shared memory budget");
+  auto kern = i8_gemm_kernel<NB8, R>;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 64 || !attr_set[dev]) {
-    const int max_smem = (I8_RING_BUDGET > I8_CW * 16 * 64 * 4 ? I8_RING_BUDGET : I8_CW * 16 * 64 * 4) + 2 * 256 * 8 +
-                         16 + 1024;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem) != cudaSuccess)
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM) != cudaSuccess)
       return GP_ERR_CUDA;
     if (dev < 64) attr_set[dev] = true;
   }
-  kern<<<grid, I8_THREADS, smem, stream>>>(tmA, p);
+  p.stages = R;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(I8_THREADS);
+  cfg.dynamicSmemBytes = (size_t)SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, A, p) != cudaSuccess) return GP_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? GP_OK : GP_ERR_CUDA;
 }
 
-int i8_gemm_launch(const CUtensorMap& tmA, I8Params p, int num_sms, cudaStream_t stream) {
-  // strip height: 16 * ceil(N / (16 * SMs)), at most 64 rows
-  int strip = 16 * ((p.N + 16 * num_sms - 1) / (16 * num_sms));
+int i8_gemm_launch(const uint8_t* A, I8Params p, int num_sms, cudaStream_t stream) {
+  // strip height: 16 * ceil(N / (16 * 2 * SMs)), at most 64 rows, so that
+  // the strips fill both CTA slots of every SM
+  static const int strip_override = env_int("GP_I8_STRIP", 0);
+  const int slots = I8_CTAS_PER_SM * num_sms;
+  int strip = 16 * ((p.N + 16 * slots - 1) / (16 * slots));
+  if (strip_override == 16 || strip_override == 32 || strip_override == 48 || strip_override == 64)
+    strip = strip_override;
   if (strip > 64) strip = 64;
   if (strip < 16) strip = 16;
   p.strip = strip;
   dim3 grid((unsigned)((p.N + strip - 1) / strip), (unsigned)((p.M + 15) / 16));
-  switch (strip) {
-    case 16: return launch_i8<2>(tmA, p, grid, stream);
-    case 32: return launch_i8<4>(tmA, p, grid, stream);
-    case 48: return launch_i8<6>(tmA, p, grid, stream);
-    default: return launch_i8<8>(tmA, p, grid, stream);
+  switch (strip) {  // ring depth R per warp: R * 8 warps * stage bytes within shared memory
+    case 16: return launch_i8<2, 2>(A, p, grid, stream);
+    case 32: return launch_i8<4, 2>(A, p, grid, stream);
+    case 48: return launch_i8<6, 1>(A, p, grid, stream);
+    default: return launch_i8<8, 1>(A, p, grid, stream);
   }
 }
 

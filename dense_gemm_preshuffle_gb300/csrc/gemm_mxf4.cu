@@ -1,8 +1,357 @@
-// Block-scaled MXFP4 GEMM (kind::mxf4): not yet built.
+// Block-scaled MXFP4 GEMM for sm_103a (tcgen05.mma kind::mxf4):
+//
+//   C[m,n] = sum_j 2^(ea[m,j]-127) 2^(eb[n,j]-127) sum_{k in block j} A[m,k] B[n,k]
+//
+// "GEMM Optimization Guide", section 8.2, counts MXFP4 operands as E2M1 with
+// one 1-byte scale per 32 K elements of each operand.  The block scales are
+// applied inside the tensor core: every MMA instruction consumes 64 K
+// elements, i.e. two UE8M0 scales per row of A and of B (scale_vec::2X).
+// The scales are read from tensor memory.
+//
+// The structure matches the dense tcgen05 kernel.  It is a persistent
+// 128 x 256 tile loop with a TMA/bulk producer warp, a single-thread MMA
+// warp and four epilogue warps.  It adds:
+//   - Scale layout in shared memory and TMEM.  A K step (256 elements,
+//     8 scale blocks) holds two 512-byte "atoms" of scales per 128 rows.  In
+//     an atom, the scale of (row r, block j) sits at byte
+//     (r%32)*16 + (r/32)*4 + j.  tcgen05.cp (32x128b, warpx4) copies an atom
+//     into four TMEM columns, replicated in the four 32-lane quarters.  So
+//     lane r%32 of quarter q holds rows r%32 + 32c in column c, and the MMA
+//     reads column r/32 for row r.
+//   - B's scales arrive already in that image.  gemm_preshuffle_b packs them
+//     next to B, and the producer bulk-copies them with the B tile.
+//   - A's scales are plain [M, K/32] bytes.  Warp 6 places them into the
+//     atom layout with 4-byte cp.async copies, two stages ahead of the MMA.
+//     After the copies land it fences them for the async proxy (tcgen05.cp
+//     reads shared memory through it) and arrives on the stage's barrier.
+//     A stage is therefore full after one producer arrival plus its
+//     transaction bytes and one arrival from warp 6.
+//   - TMEM: one 256-column fp32 accumulator, plus one scale slot per ring
+//     stage (A: 2 atoms x 4 columns; B: 2 atoms x 8 columns).  tcgen05.cp
+//     and tcgen05.mma issued by the same thread execute in order, so a
+//     stage's scale copy always lands before its MMAs read it.
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace gp {
-int mxf4_gemm_launch(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, TcParams, int, cudaStream_t) {
-  return GP_ERR_UNSUPPORTED;
+
+namespace {
+
+constexpr int F4_THREADS = 224;  // producer, MMA, 4 epilogue warps, A-scale warp
+constexpr int F4_BN = 256;
+constexpr int F4_STAGES = 4;
+constexpr int F4_SF_LOOKAHEAD = 2;  // stages the A-scale warp keeps in flight
+
+struct F4Cfg {
+  static constexpr int A_BYTES = 128 * 128;
+  static constexpr int B_BYTES = F4_BN * 128;
+  static constexpr int SFA_BYTES = 1024;          // 2 atoms
+  static constexpr int SFB_BYTES = F4_BN * 8;      // (BN/128) bands x 2 atoms
+  static constexpr int STAGE_TX = A_BYTES + B_BYTES + SFB_BYTES;
+  static constexpr int EPI_BYTES = 4 * 32 * 128;
+  static constexpr int ACC_COLS = F4_BN;
+  static constexpr int SFA_COLS = 8;
+  static constexpr int SFB_COLS = 2 * (F4_BN / 32);
+  static constexpr int SF_COL0 = ACC_COLS;
+  static constexpr int TMEM_COLS = 512;
+  static_assert(ACC_COLS + F4_STAGES * (SFA_COLS + SFB_COLS) <= TMEM_COLS, "tensor memory budget");
+  static constexpr int SMEM =
+      F4_STAGES * (A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES) + EPI_BYTES + 256 + 1024;
+  static_assert(SMEM <= 232448, "shared memory budget");
+};
+
+__device__ __forceinline__ void f4_tile_coords(int t, int tiles_m, int tiles_n, int& mb, int& nb) {
+  constexpr int G = 16;
+  const int group_size = G * tiles_n;
+  const int group = t / group_size;
+  const int first_m = group * G;
+  const int gm = min(tiles_m - first_m, G);
+  const int r = t - group * group_size;
+  mb = first_m + r % gm;
+  nb = r / gm;
 }
+
+// Shared-memory descriptor of a 32-row x 16-byte block stored contiguously
+// (no swizzle; 8-row core matrices 128 bytes apart), the source of tcgen05.cp.
+__device__ __forceinline__ uint64_t smem_desc_sf(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)(128u >> 4) << 16;   // leading byte offset
+  d |= (uint64_t)(128u >> 4) << 32;   // stride byte offset: next 8 rows
+  d |= (uint64_t)1 << 46;             // fixed 0b001
+  return d;                           // swizzle mode 0: none
+}
+
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(F4_THREADS, 1)
+    mxf4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmC, TcParams p) {
+  using Cfg = F4Cfg;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* s_a = base;
+  uint8_t* s_b = s_a + F4_STAGES * Cfg::A_BYTES;
+  uint8_t* s_sfa = s_b + F4_STAGES * Cfg::B_BYTES;
+  uint8_t* s_sfb = s_sfa + F4_STAGES * Cfg::SFA_BYTES;
+  uint8_t* s_epi = s_sfb + F4_STAGES * Cfg::SFB_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(s_epi + Cfg::EPI_BYTES);
+  uint64_t* empty = full + F4_STAGES;
+  uint64_t* accf = empty + F4_STAGES;
+  uint64_t* acce = accf + 1;
+  uint64_t* drain = acce + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint64_t limit = p.wait_limit_ns;
+  const int nblk = p.K / 32;  // scale bytes per row of A
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < F4_STAGES; ++s) {
+      mbar_init(&full[s], 2);  // producer (with tx bytes) + A-scale warp
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(accf, 1);
+    mbar_init(acce, 4);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tensormap(&tmA);
+    prefetch_tensormap(&tmC);
+  }
+  if (warp == 1) tmem_alloc<Cfg::TMEM_COLS>(tmem_slot);
+  pdl_launch_dependents();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  pdl_wait();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int s = 0;
+      uint32_t ph = 0;
+      uint32_t issued = 0;
+      bool ok = true;
+      const size_t sf_band_bytes = (size_t)p.ktiles * 1024;  // scales of one 128-row band
+      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+        int mb, nb;
+        f4_tile_coords(t, p.tiles_m, p.tiles_n, mb, nb);
+        for (int kt = 0; kt < p.ktiles; ++kt) {
+          if (!wait_bounded(&empty[s], ph ^ 1, abort_flag, p.status, ST_TIMEOUT_PRODUCER, limit)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[s], Cfg::STAGE_TX);
+          tma_load_2d(s_a + s * Cfg::A_BYTES, &tmA, kt * 128, mb * 128, &full[s]);
+#pragma unroll
+          for (int j = 0; j < F4_BN / 128; ++j) {
+            const int band = nb * (F4_BN / 128) + j;
+            bulk_load(s_b + s * Cfg::B_BYTES + j * 16384, p.Bp + ((size_t)band * p.ktiles + kt) * 16384, 16384,
+                      &full[s]);
+            bulk_load(s_sfb + s * Cfg::SFB_BYTES + j * 1024, p.Bsf + (size_t)band * sf_band_bytes + (size_t)kt * 1024,
+                      1024, &full[s]);
+          }
+          ++issued;
+          if (++s == F4_STAGES) {
+            s = 0;
+            ph ^= 1;
+          }
+        }
+      }
+      if (!ok) {
+        const uint32_t n = issued < (uint32_t)F4_STAGES ? issued : (uint32_t)F4_STAGES;
+        for (uint32_t i = 0; i < n; ++i) {
+          const uint32_t q = issued - 1 - i;
+          volatile int never = 0;
+          wait_bounded(&full[q % F4_STAGES], (q / F4_STAGES) & 1, &never, p.status, ST_TIMEOUT_DRAIN, limit);
+        }
+      }
+    }
+  } else if (warp == 6) {
+    // ------------------------------------------------------------ A-scale warp
+    // Lane l moves rows l + 32c (c = 0..3) of the tile: their 8 scale bytes
+    // of this K step split into atom 0 (blocks 0-3) and atom 1 (blocks 4-7),
+    // at byte l*16 + c*4 of each atom.
+    uint32_t q = 0;       // stage sequence number (same order as the producer)
+    uint32_t done = 0;    // stages already signalled
+    bool ok = true;
+    for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+      int mb, nb;
+      f4_tile_coords(t, p.tiles_m, p.tiles_n, mb, nb);
+      for (int kt = 0; kt < p.ktiles; ++kt, ++q) {
+        const int s = (int)(q % F4_STAGES);
+        const uint32_t ph = (q / F4_STAGES) & 1;
+        if (!wait_bounded(&empty[s], ph ^ 1, abort_flag, p.status, ST_TIMEOUT_PRODUCER, limit)) {
+          ok = false;
+          break;
+        }
+        const uint32_t dst = smem_u32(s_sfa + s * Cfg::SFA_BYTES) + lane * 16;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int m = mb * 128 + c * 32 + lane;
+          const bool valid = m < p.M;
+          const uint8_t* src = p.sfa + (size_t)(valid ? m : 0) * nblk + kt * 8;
+          cp_async_4(dst + c * 4, src, valid ? 4u : 0u);
+          cp_async_4(dst + 512 + c * 4, src + 4, valid ? 4u : 0u);
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+        if (q + 1 >= (uint32_t)F4_SF_LOOKAHEAD) {
+          // the stage issued LOOKAHEAD-1 steps ago has landed: publish it
+          asm volatile("cp.async.wait_group %0;" ::"n"(F4_SF_LOOKAHEAD - 1) : "memory");
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&full[done % F4_STAGES]);
+          ++done;
+        }
+      }
+    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    fence_proxy_async_smem();
+    __syncwarp();
+    for (; done < q; ++done)
+      if (lane == 0) mbar_arrive(&full[done % F4_STAGES]);
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int s = 0;
+      uint32_t ph = 0;
+      int local = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x, ++local) {
+        if (!wait_bounded(acce, (uint32_t)(local & 1) ^ 1, abort_flag, p.status, ST_TIMEOUT_MMA, limit)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem_base;
+        for (int kt = 0; kt < p.ktiles; ++kt) {
+          if (!wait_bounded(&full[s], ph, abort_flag, p.status, ST_TIMEOUT_MMA, limit)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sfa_t = tmem_base + Cfg::SF_COL0 + s * (Cfg::SFA_COLS + Cfg::SFB_COLS);
+          const uint32_t sfb_t = sfa_t + Cfg::SFA_COLS;
+          const uint32_t sfa_s = smem_u32(s_sfa + s * Cfg::SFA_BYTES);
+          const uint32_t sfb_s = smem_u32(s_sfb + s * Cfg::SFB_BYTES);
+#pragma unroll
+          for (int at = 0; at < 2; ++at) {
+            tmem_cp_32x128b_warpx4(sfa_t + at * 4, smem_desc_sf(sfa_s + at * 512));
+#pragma unroll
+            for (int j = 0; j < F4_BN / 128; ++j)
+              tmem_cp_32x128b_warpx4(sfb_t + at * (F4_BN / 32) + j * 4, smem_desc_sf(sfb_s + j * 1024 + at * 512));
+          }
+          const uint32_t a0 = smem_u32(s_a + s * Cfg::A_BYTES);
+          const uint32_t b0 = smem_u32(s_b + s * Cfg::B_BYTES);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint32_t at = (uint32_t)(k >> 1);
+            const uint32_t id = (uint32_t)(k & 1) * 2;
+            umma_mxf4(d, smem_desc_sw128(a0 + 32 * k), smem_desc_sw128(b0 + 32 * k), idesc_mxf4(128, F4_BN, id, id),
+                      sfa_t + at * 4, sfb_t + at * (F4_BN / 32), (kt | k) != 0 ? 1u : 0u);
+          }
+          umma_commit(&empty[s]);
+          if (++s == F4_STAGES) {
+            s = 0;
+            ph ^= 1;
+          }
+        }
+        if (!ok) break;
+        umma_commit(accf);
+      }
+      umma_commit(drain);
+      volatile int never = 0;
+      wait_bounded(drain, 0, &never, p.status, ST_TIMEOUT_DRAIN, limit);
+    }
+  } else if (warp >= 2 && warp <= 5) {
+    // ------------------------------------------------------------ epilogue
+    const int quad = warp & 3;
+    uint8_t* stg = s_epi + (warp - 2) * 4096;
+    const uint32_t stg_row = smem_u32(stg) + lane * 128;
+    int local = 0;
+    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++local) {
+      int mb, nb;
+      f4_tile_coords(t, p.tiles_m, p.tiles_n, mb, nb);
+      if (!wait_bounded(accf, (uint32_t)(local & 1), abort_flag, p.status, ST_TIMEOUT_EPILOGUE, limit)) break;
+      tc_fence_after();
+      const int row0 = mb * 128 + quad * 32;
+      const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16);
+#pragma unroll 1
+      for (int c = 0; c < F4_BN / 64; ++c) {
+        const int n0 = nb * F4_BN + c * 64;
+        if (lane == 0) bulk_wait_group_read<0>();
+        __syncwarp();
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(tbase + (uint32_t)(c * 64 + h * 32), r);
+          tmem_ld_wait();
+          uint32_t pk[16];
+#pragma unroll
+          for (int q = 0; q < 16; ++q) pk[q] = pack_bf16x2(__uint_as_float(r[2 * q]), __uint_as_float(r[2 * q + 1]));
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int chunk = h * 4 + q;
+            st_shared_v4(stg_row + (uint32_t)(((chunk ^ (lane & 7)) * 16)), pk[4 * q], pk[4 * q + 1], pk[4 * q + 2],
+                         pk[4 * q + 3]);
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && row0 < p.M) {
+          tma_store_2d(&tmC, n0, row0, stg);
+          bulk_commit_group();
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acce);
+    }
+    if (lane == 0) bulk_wait_group<0>();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc<Cfg::TMEM_COLS>(tmem_base);
+  }
+}
+
+int mxf4_gemm_launch(const CUtensorMap& tmA, const CUtensorMap& tmC, TcParams p, int num_sms, cudaStream_t stream) {
+  if (p.N % F4_BN != 0) return GP_ERR_SHAPE;
+  p.tiles_m = (p.M + 127) / 128;
+  p.tiles_n = p.N / F4_BN;
+  p.num_tiles = p.tiles_m * p.tiles_n;
+  const int grid = p.num_tiles < num_sms ? p.num_tiles : num_sms;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 64 || !attr_set[dev]) {
+    if (cudaFuncSetAttribute(mxf4_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, F4Cfg::SMEM) !=
+        cudaSuccess)
+      return GP_ERR_CUDA;
+    if (dev < 64) attr_set[dev] = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(F4_THREADS);
+  cfg.dynamicSmemBytes = F4Cfg::SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, mxf4_gemm_kernel, tmA, tmC, p) != cudaSuccess) return GP_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? GP_OK : GP_ERR_CUDA;
+}
+
 }  // namespace gp

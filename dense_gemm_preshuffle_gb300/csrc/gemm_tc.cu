@@ -125,9 +125,23 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     prefetch_tensormap(&tmC);
   }
   if (warp == 1) tmem_alloc<Cfg::TMEM_COLS>(sm.tmem_slot);
+  if (threadIdx.x == 32 * 2 && (int)blockIdx.x < p.num_tiles) {
+    // Warm L2 with the first K steps of this CTA's first tile while the
+    // previous kernel may still run (a prefetch never changes later loads).
+    int mb, nb;
+    tile_coords(blockIdx.x, p.tiles_m, p.tiles_n, mb, nb);
+    const int kpre = p.ktiles < STAGES ? p.ktiles : STAGES;
+    for (int kt = 0; kt < kpre; ++kt) {
+      prefetch_l2_tile_2d(&tmA, kt * 128, mb * 128);
+      for (int j = 0; j < BN / 128; ++j)
+        prefetch_l2_bulk(p.Bp + ((size_t)(nb * (BN / 128) + j) * p.ktiles + kt) * 16384, 16384);
+    }
+  }
+  pdl_launch_dependents();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  pdl_wait();  // inputs may come from, and C may be read by, the previous kernel
   const uint32_t tmem_base = *sm.tmem_slot;
 
   if (warp == 0) {
@@ -315,7 +329,17 @@ static int launch_tc(const CUtensorMap& tmA, const CUtensorMap& tmC, const TcPar
       return GP_ERR_CUDA;
     attr_set[dev] = true;
   }
-  kern<<<grid, TC_THREADS, Cfg::SMEM, stream>>>(tmA, tmC, p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(TC_THREADS);
+  cfg.dynamicSmemBytes = Cfg::SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, tmA, tmC, p) != cudaSuccess) return GP_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? GP_OK : GP_ERR_CUDA;
 }
 

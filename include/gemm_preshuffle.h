@@ -132,7 +132,7 @@ int gemm_unpack_b(const void* B_packed, int dtype, int64_t N, int64_t K, void* B
  * Other combinations return GP_ERR_UNSUPPORTED.
  *
  * Shape rules: M >= 1 (any value), N and K as for gemm_packed_b_bytes, and
- * M, N, K < 2^31.  For INT8 the exact result must fit int32, which holds for
+ * M, N, K < 2^31.  E2M1 also needs N % 256 == 0 (its tiles are 256 wide).  For INT8 the exact result must fit int32, which holds for
  * every input when K <= 131072.
  * Float outputs are rounded to nearest-even from the fp32 value.
  * The call launches one kernel and allocates no memory.  K == 0 writes

@@ -96,6 +96,7 @@ SMALL = [
     ("bf16", 257, 384, 512), ("bf16", 128, 128, 64), ("bf16", 64, 256, 4096), ("bf16", 700, 640, 320),
     ("int8", 1, 128, 128), ("int8", 37, 256, 384), ("int8", 16, 384, 256), ("int8", 100, 1152, 1280),
     ("int8", 16, 7168, 4096),
+    ("e2m1", 1, 256, 256), ("e2m1", 200, 512, 512), ("e2m1", 129, 256, 1024), ("e2m1", 300, 768, 2048),
 ]
 
 
@@ -103,6 +104,27 @@ SMALL = [
 def test_small_and_ragged(dtype, M, N, K):
     ops = inputs.make_operands(dtype, M, N, K, seed=1000 + M + N + K)
     check(ops, gpu_gemm(ops))
+
+
+def test_mxfp4_single_hot_scale_blocks():
+    """Every element 1.0 and every scale 2^-127 except one (row, block) per
+    probe: C shows exactly which output row and K block each A scale reaches."""
+    M, N, K = 128, 256, 512
+    a = np.full((M, K // 2), 0x22, np.uint8)   # E2M1 1.0 in both nibbles
+    b = np.full((N, K // 2), 0x22, np.uint8)
+    rng = np.random.default_rng(4)
+    ea = np.zeros((M, K // 32), np.uint8)
+    eb = np.full((N, K // 32), 127, np.uint8)
+    for m in range(M):
+        ea[m, rng.integers(0, K // 32)] = 127 + (m % 5)
+    ops = inputs.Operands("e2m1", M, N, K, a, b, ea, eb)
+    check(ops, gpu_gemm(ops))
+    ea2 = np.full((M, K // 32), 127, np.uint8)
+    eb2 = np.zeros((N, K // 32), np.uint8)
+    for n in range(N):
+        eb2[n, rng.integers(0, K // 32)] = 126 + (n % 7)
+    ops2 = inputs.Operands("e2m1", M, N, K, a, b, ea2, eb2)
+    check(ops2, gpu_gemm(ops2))
 
 
 def test_e4m3_without_scales():
@@ -126,7 +148,7 @@ def test_workload_full_compare(name):
     check(ops, gpu_gemm(ops))
 
 
-@pytest.mark.parametrize("name", ["fp8_8192x8192x8192"])
+@pytest.mark.parametrize("name", ["fp8_8192x8192x8192", "mxfp4_4096x8192x8192"])
 def test_workload_sampled_rows(name):
     ops = inputs.workload_operands(name)
     C = gpu_gemm(ops)
