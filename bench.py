@@ -364,9 +364,12 @@ def run_ours(args):
     t_end = time.perf_counter()
     sec = max_over_ranks(pg, sec, device)
     clock_summary = clocks.summary(t_start, t_end)
-    e2e_sec, h2d, d2h = time_e2e(prob, max(10, min(args.steps, 2000)), args.warmup, device)
     e2e_steps = max(10, min(args.steps, 2000))
-    e2e_sec = max_over_ranks(pg, e2e_sec, device)
+    if args.no_e2e:
+        e2e_sec, h2d, d2h = float("nan"), 0, 0
+    else:
+        e2e_sec, h2d, d2h = time_e2e(prob, e2e_steps, args.warmup, device)
+        e2e_sec = max_over_ranks(pg, e2e_sec, device)
     clocks.stop()
 
     per = sec / args.steps
@@ -390,7 +393,8 @@ def run_ours(args):
                          f"({prob.copies * prob.packed_bytes / 1e6:.0f} MB)",
                    "timing": "CUDA-graph replay of back-to-back gemm_run launches, CUDA events"},
         "gpu_launches": args.steps,
-        "e2e": {"value": round(world * prob.flops * e2e_steps / e2e_sec / 1e12, 3), "unit": "TFLOP/s",
+        "e2e": {"value": None if args.no_e2e else round(world * prob.flops * e2e_steps / e2e_sec / 1e12, 3),
+                "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_sec / e2e_steps * 1e3, 5), "steps": e2e_steps},
         "roofline": roofline(prob, per, peaks, peak_kind, traffic_from_profiles(prob.name)),
@@ -422,7 +426,8 @@ def run_ours(args):
                 others[name] = {"unavailable": f"{type(e).__name__}: {e}"[:200]}
         out["others"] = others
     if rank == 0:
-        out["cpu_baseline"] = cpu_baseline(args.workload)
+        if not args.no_cpu:
+            out["cpu_baseline"] = cpu_baseline(args.workload)
         print(json.dumps(out), flush=True)
     if pg is not None:
         pg.destroy_process_group()
@@ -481,7 +486,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
-    ap.add_argument("--no-others", action="store_true")
+    ap.add_argument("--no-others", action="store_true", help="skip the other workloads' lines")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffers) leg")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline leg")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

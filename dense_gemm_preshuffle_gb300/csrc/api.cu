@@ -225,7 +225,33 @@ int gemm_run(const void* A, const void* B_packed, int dtype, int64_t M, int64_t 
     p.N = (int)N;
     p.K = (int)K;
     p.ktiles = (int)(kb / 128);
-    return i8_gemm_launch(static_cast<const uint8_t*>(A), p, d->num_sms, st);
+    p.strip = i8_strip_rows((int)N, d->num_sms);
+    // A as [K tiles][M rows][128 B] (3-D view, 128-byte swizzle): one copy
+    // brings 8 K tiles of 16 rows.
+    CUtensorMap tmA, tmB;
+    {
+      cuuint64_t dims[3] = {128, (cuuint64_t)M, (cuuint64_t)p.ktiles};
+      cuuint64_t strides[2] = {(cuuint64_t)kb, 128};
+      cuuint32_t box[3] = {128, 16, 8};
+      cuuint32_t estr[3] = {1, 1, 1};
+      if (g_encode(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(A), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return GP_ERR_CUDA;
+    }
+    // packed B as [bands][K tiles][128 rows][128 B] (4-D view, already
+    // swizzled): one copy brings 8 K tiles of a strip of rows.
+    {
+      cuuint64_t dims[4] = {128, 128, (cuuint64_t)p.ktiles, (cuuint64_t)(N / 128)};
+      cuuint64_t strides[3] = {128, 16384, (cuuint64_t)p.ktiles * 16384};
+      cuuint32_t box[4] = {128, (cuuint32_t)p.strip, 8, 1};
+      cuuint32_t estr[4] = {1, 1, 1, 1};
+      if (g_encode(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(B_packed), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return GP_ERR_CUDA;
+    }
+    return i8_gemm_launch(tmA, tmB, p, d->num_sms, st);
   }
 
   CUtensorMap tmA, tmC;

@@ -43,8 +43,10 @@
 
 namespace gp {
 
-constexpr int I8_CW = 8;  // warps per CTA, each with a private copy ring
-constexpr int I8_THREADS = 32 * I8_CW;
+constexpr int I8_CW = 8;                       // consumer warps; warp I8_CW is the producer
+constexpr int I8_THREADS = 32 * (I8_CW + 1);
+constexpr int I8_KT_PER_STAGE = I8_CW;          // one K tile per consumer warp per stage
+constexpr int I8_STAGES = 2;
 // Two CTAs fit on one SM (registers <= 128/thread, shared memory <= 113 KiB),
 // so with programmatic dependent launch the next GEMM's CTAs sit beside this
 // one's and warm L2 with their weights while this one computes.
@@ -70,99 +72,110 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
+template <int NB8>
+__global__ void __launch_bounds__(I8_THREADS, (NB8 <= 4 ? I8_CTAS_PER_SM : 1))
+    i8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, I8Params p) {
+  constexpr int SN = NB8 * 8;                    // rows of B per CTA (divides 128)
+  constexpr int A_BYTES = I8_KT_PER_STAGE * 16 * 128;
+  constexpr int B_BYTES = I8_KT_PER_STAGE * SN * 128;
+  constexpr int STAGE = A_BYTES + B_BYTES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(base + I8_STAGES * STAGE);
+  uint64_t* empty = full + I8_STAGES;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + I8_STAGES);
 
-// Copy K tile `kt` (the 16 x 128-byte A tile and the strip's rows of the
-// packed B tile) into a warp-private ring slot.  A rows >= M read as zeros.
-// The A tile gets the 128-byte swizzle (chunk c of row r at slot c ^ (r%8));
-// the packed B rows already carry it.
-template <int SN>
-__device__ __forceinline__ void i8_copy_ktile(const I8Params& p, const uint8_t* A, int mg, int n0, int rows, int kt,
-                                              uint32_t slot, int lane) {
-  const size_t kb = (size_t)p.ktiles * 128;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int i = lane + 32 * j;
-    const int row = i >> 3, c = i & 7;
-    const int gm = mg * 16 + row;
-    const bool valid = gm < p.M;
-    cp_async_16(slot + row * 128 + ((c ^ (row & 7)) << 4), A + (size_t)(valid ? gm : 0) * kb + kt * 128 + c * 16,
-                valid ? 16u : 0u);
-  }
-  const uint32_t sb = slot + 2048;
-#pragma unroll 4
-  for (int i = lane; i < rows * 8; i += 32) {
-    const int row = i >> 3, c = i & 7;
-    const int r = n0 + row;
-    cp_async_16(sb + row * 128 + c * 16,
-                p.Bp + (((size_t)(r >> 7) * p.ktiles + kt) * 128 + (r & 127)) * 128 + c * 16, 16u);
-  }
-}
-
-template <int NB8, int R>
-__global__ void __launch_bounds__(I8_THREADS, I8_CTAS_PER_SM) i8_gemm_kernel(const uint8_t* __restrict__ A, I8Params p) {
-  constexpr int SN = NB8 * 8;
-  constexpr int STAGE = 2048 + SN * 128;
-  extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int n0 = blockIdx.x * SN;
-  const int rows = min(SN, p.N - n0);  // multiple of 16
+  const int band = n0 >> 7, r0 = n0 & 127;
   const int mg = blockIdx.y;
-  const uint32_t ring = smem_u32(smem) + (uint32_t)(warp * R * STAGE);
+  const int nstages = (p.ktiles + I8_KT_PER_STAGE - 1) / I8_KT_PER_STAGE;
+  const uint64_t limit = p.wait_limit_ns;
 
-  // Warm L2 with this warp's share of the weight strip while the previous
-  // kernel on the stream may still run: a prefetch is only a cache hint.
-  for (int kt = warp; kt < p.ktiles; kt += I8_CW) {
-    if (lane == 0) {
-      int r = n0;
-      while (r < n0 + rows) {
-        const int tn = r >> 7;
-        const int r_end = min(n0 + rows, (tn + 1) << 7);
-        prefetch_l2_bulk(p.Bp + ((size_t)tn * p.ktiles + kt) * 16384 + (size_t)(r & 127) * 128,
-                         (uint32_t)(r_end - r) * 128u);
-        r = r_end;
-      }
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < I8_STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], I8_CW);
     }
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tensormap(&tmA);
+    prefetch_tensormap(&tmB);
+  }
+  if (threadIdx.x == I8_CW * 32) {
+    // Warm L2 with this CTA's whole weight strip while the previous kernel
+    // on the stream may still run: a prefetch is only a cache hint.
+    for (int q = 0; q < nstages; ++q)
+      asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                       reinterpret_cast<uint64_t>(&tmB)),
+                   "r"(0), "r"(r0), "r"(q * I8_KT_PER_STAGE), "r"(band)
+                   : "memory");
   }
   pdl_launch_dependents();
+  __syncthreads();
   pdl_wait();  // A may be produced, and C read, by the previous kernel
 
-  // Prologue: R K tiles of this warp in flight (one commit group each).
-#pragma unroll
-  for (int q = 0; q < R; ++q) {
-    const int kt = warp + q * I8_CW;
-    if (kt < p.ktiles) i8_copy_ktile<SN>(p, A, mg, n0, rows, kt, ring + q * STAGE, lane);
-    cp_async_commit();
+  if (warp == I8_CW) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t issued = 0;
+      bool ok = true;
+      for (int q = 0; q < nstages; ++q) {
+        const int s = q % I8_STAGES;
+        const uint32_t ph = (uint32_t)(q / I8_STAGES) & 1;
+        if (!wait_bounded(&empty[s], ph ^ 1, abort_flag, p.status, ST_TIMEOUT_PRODUCER, limit)) {
+          ok = false;
+          break;
+        }
+        uint8_t* st = base + s * STAGE;
+        mbar_arrive_expect_tx(&full[s], STAGE);
+        // A: 8 K tiles x 16 rows x 128 B (rows >= M and K tiles >= ktiles read as zeros)
+        asm volatile(
+            "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::
+                "r"(smem_u32(st)),
+            "l"(reinterpret_cast<uint64_t>(&tmA)), "r"(0), "r"(mg * 16), "r"(q * I8_KT_PER_STAGE),
+            "r"(smem_u32(&full[s]))
+            : "memory");
+        // B: 8 K tiles x SN rows x 128 B of the packed band, one copy
+        asm volatile(
+            "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];" ::
+                "r"(smem_u32(st + A_BYTES)),
+            "l"(reinterpret_cast<uint64_t>(&tmB)), "r"(0), "r"(r0), "r"(q * I8_KT_PER_STAGE), "r"(band),
+            "r"(smem_u32(&full[s]))
+            : "memory");
+        ++issued;
+      }
+      if (!ok || *abort_flag) {
+        const uint32_t n = issued < (uint32_t)I8_STAGES ? issued : (uint32_t)I8_STAGES;
+        for (uint32_t i = 0; i < n; ++i) {
+          const uint32_t q = issued - 1 - i;
+          volatile int never = 0;
+          wait_bounded(&full[q % I8_STAGES], (q / I8_STAGES) & 1, &never, p.status, ST_TIMEOUT_DRAIN, limit);
+        }
+      }
+    }
+    return;  // the producer takes no part in the reduction below
   }
 
+  // ------------------------------------------------------------ consumers
+  // Warp w takes K tile w of every stage.
   const int g = lane >> 2;  // mma group id: A rows g, g+8 and B row g of each 8-row block
   const int t = lane & 3;
-  const int nb_valid = rows >> 3;
   int acc[NB8][4];
 #pragma unroll
   for (int nb = 0; nb < NB8; ++nb) acc[nb][0] = acc[nb][1] = acc[nb][2] = acc[nb][3] = 0;
 
-  int q = 0;
-  for (int kt = warp; kt < p.ktiles; kt += I8_CW) {
-    cp_async_wait<R - 1>();  // this lane's copies of the oldest tile are done
-    __syncwarp();            // ... and every other lane's
-    const uint8_t* sa = smem + (size_t)warp * R * STAGE + q * STAGE;
-    const uint8_t* sbp = sa + 2048;
-    const uint32_t slot_addr = ring + q * STAGE;
-    const int kn = kt + R * I8_CW;
-    q = (q + 1 == R) ? 0 : q + 1;
+  for (int q = 0; q < nstages; ++q) {
+    const int s = q % I8_STAGES;
+    const uint32_t ph = (uint32_t)(q / I8_STAGES) & 1;
+    if (!wait_bounded(&full[s], ph, abort_flag, p.status, ST_TIMEOUT_CONSUMER, limit)) break;
+    const bool live = q * I8_KT_PER_STAGE + warp < p.ktiles;
+    const uint8_t* sa = base + s * STAGE + warp * (16 * 128);
+    const uint8_t* sbp = base + s * STAGE + A_BYTES + warp * (SN * 128);
     float f[NB8][4];
 #pragma unroll
     for (int nb = 0; nb < NB8; ++nb) f[nb][0] = f[nb][1] = f[nb][2] = f[nb][3] = 0.f;
-    // Two 64-element halves of the K tile; only one half's raw bytes are live.
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int slot = ((2 * t + h) ^ g) << 4;
@@ -170,24 +183,22 @@ __global__ void __launch_bounds__(I8_THREADS, I8_CTAS_PER_SM) i8_gemm_kernel(con
       const uint4 ag8 = *reinterpret_cast<const uint4*>(sa + (g + 8) * 128 + slot);
       uint4 bw[NB8];
 #pragma unroll
-      for (int nb = 0; nb < NB8; ++nb)
-        if (nb < nb_valid) bw[nb] = *reinterpret_cast<const uint4*>(sbp + (nb * 8 + g) * 128 + slot);
+      for (int nb = 0; nb < NB8; ++nb) bw[nb] = *reinterpret_cast<const uint4*>(sbp + (nb * 8 + g) * 128 + slot);
       if (h == 1) {
-        __syncwarp();  // the slot is free: refill it with this warp's tile R steps ahead
-        if (kn < p.ktiles) i8_copy_ktile<SN>(p, A, mg, n0, rows, kn, slot_addr, lane);
-        cp_async_commit();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);  // this warp's reads of the stage are done
       }
-      const uint32_t aw[4] = {ag.x, ag.y, ag.z, ag.w};
-      const uint32_t a8w[4] = {ag8.x, ag8.y, ag8.z, ag8.w};
-      uint32_t alo[4], ahi[4], a8lo[4], a8hi[4];
+      if (live) {
+        const uint32_t aw[4] = {ag.x, ag.y, ag.z, ag.w};
+        const uint32_t a8w[4] = {ag8.x, ag8.y, ag8.z, ag8.w};
+        uint32_t alo[4], ahi[4], a8lo[4], a8hi[4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        i8x4_to_f16x2(aw[j], alo[j], ahi[j]);
-        i8x4_to_f16x2(a8w[j], a8lo[j], a8hi[j]);
-      }
+        for (int j = 0; j < 4; ++j) {
+          i8x4_to_f16x2(aw[j], alo[j], ahi[j]);
+          i8x4_to_f16x2(a8w[j], a8lo[j], a8hi[j]);
+        }
 #pragma unroll
-      for (int nb = 0; nb < NB8; ++nb) {
-        if (nb < nb_valid) {
+        for (int nb = 0; nb < NB8; ++nb) {
           const uint32_t w[4] = {bw[nb].x, bw[nb].y, bw[nb].z, bw[nb].w};
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
@@ -204,11 +215,10 @@ __global__ void __launch_bounds__(I8_THREADS, I8_CTAS_PER_SM) i8_gemm_kernel(con
       for (int i = 0; i < 4; ++i) acc[nb][i] += __float2int_rn(f[nb][i]);
     }
   }
-  cp_async_wait<0>();
 
   // ------------------------------------------------------------ reduction
-  __syncthreads();  // every warp is done with its ring
-  int32_t* red = reinterpret_cast<int32_t*>(smem);  // [CW][16][SN]
+  named_bar_sync(1, I8_CW * 32);  // every consumer is done with the ring
+  int32_t* red = reinterpret_cast<int32_t*>(base);  // [CW][16][SN]
 #pragma unroll
   for (int nb = 0; nb < NB8; ++nb) {
     const int col = nb * 8 + 2 * t;
@@ -217,9 +227,9 @@ __global__ void __launch_bounds__(I8_THREADS, I8_CTAS_PER_SM) i8_gemm_kernel(con
     red[(warp * 16 + g + 8) * SN + col] = acc[nb][2];
     red[(warp * 16 + g + 8) * SN + col + 1] = acc[nb][3];
   }
-  __syncthreads();
-  for (int i = threadIdx.x; i < 16 * rows; i += I8_THREADS) {
-    const int m = i / rows, n = i - m * rows;
+  named_bar_sync(1, I8_CW * 32);
+  for (int i = threadIdx.x; i < 16 * SN; i += I8_CW * 32) {
+    const int m = i / SN, n = i - m * SN;
     int sum = 0;
 #pragma unroll
     for (int w = 0; w < I8_CW; ++w) sum += red[(w * 16 + m) * SN + n];
@@ -228,8 +238,8 @@ __global__ void __launch_bounds__(I8_THREADS, I8_CTAS_PER_SM) i8_gemm_kernel(con
   }
 }
 
-// Tuning overrides, read once per process: GP_I8_STRIP (rows of B per CTA:
-// 16, 32, 48 or 64).
+// Tuning override, read once per process: GP_I8_STRIP (rows of B per CTA:
+// 16, 32 or 64).
 static int env_int(const char* name, int dflt) {
   const char* e = std::getenv(name);
   if (e == nullptr) return dflt;
@@ -237,14 +247,14 @@ static int env_int(const char* name, int dflt) {
   return v > 0 ? v : dflt;
 }
 
-template <int NB8, int R>
-static int launch_i8(const uint8_t* A, I8Params p, dim3 grid, cudaStream_t stream) {
-  constexpr int STAGE = 2048 + NB8 * 8 * 128;
-  constexpr int RING = I8_CW * R * STAGE;
+template <int NB8>
+static int launch_i8(const CUtensorMap& tmA, const CUtensorMap& tmB, I8Params p, dim3 grid, cudaStream_t stream) {
+  constexpr int STAGE = I8_KT_PER_STAGE * (16 + NB8 * 8) * 128;
   constexpr int RED = I8_CW * 16 * NB8 * 8 * 4;
-  constexpr int SMEM = RING > RED ? RING : RED;
-  static_assert(SMEM <= 227 * 1024, "shared memory budget");
-  auto kern = i8_gemm_kernel<NB8, R>;
+  constexpr int RING = I8_STAGES * STAGE;
+  constexpr int SMEM = (RING > RED ? RING : RED) + 2 * I8_STAGES * 8 + 16 + 1024;
+  static_assert(SMEM * (NB8 <= 4 ? I8_CTAS_PER_SM : 1) <= 228 * 1024, "shared memory budget");
+  auto kern = i8_gemm_kernel<NB8>;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -253,7 +263,7 @@ static int launch_i8(const uint8_t* A, I8Params p, dim3 grid, cudaStream_t strea
       return GP_ERR_CUDA;
     if (dev < 64) attr_set[dev] = true;
   }
-  p.stages = R;
+  p.stages = I8_STAGES;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(I8_THREADS);
@@ -264,27 +274,28 @@ static int launch_i8(const uint8_t* A, I8Params p, dim3 grid, cudaStream_t strea
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, kern, A, p) != cudaSuccess) return GP_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, p) != cudaSuccess) return GP_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? GP_OK : GP_ERR_CUDA;
 }
 
-int i8_gemm_launch(const uint8_t* A, I8Params p, int num_sms, cudaStream_t stream) {
-  // strip height: 16 * ceil(N / (16 * 2 * SMs)), at most 64 rows, so that
-  // the strips fill both CTA slots of every SM
+int i8_strip_rows(int N, int num_sms) {
+  // 16, 32 or 64 rows (a divisor of the 128-row band), chosen so the strips
+  // fill both CTA slots of every SM; GP_I8_STRIP overrides.
   static const int strip_override = env_int("GP_I8_STRIP", 0);
+  if (strip_override == 16 || strip_override == 32 || strip_override == 64) return strip_override;
   const int slots = I8_CTAS_PER_SM * num_sms;
-  int strip = 16 * ((p.N + 16 * slots - 1) / (16 * slots));
-  if (strip_override == 16 || strip_override == 32 || strip_override == 48 || strip_override == 64)
-    strip = strip_override;
-  if (strip > 64) strip = 64;
-  if (strip < 16) strip = 16;
-  p.strip = strip;
-  dim3 grid((unsigned)((p.N + strip - 1) / strip), (unsigned)((p.M + 15) / 16));
-  switch (strip) {  // ring depth R per warp: R * 8 warps * stage bytes within shared memory
-    case 16: return launch_i8<2, 2>(A, p, grid, stream);
-    case 32: return launch_i8<4, 2>(A, p, grid, stream);
-    case 48: return launch_i8<6, 1>(A, p, grid, stream);
-    default: return launch_i8<8, 1>(A, p, grid, stream);
+  if (N / 64 >= slots) return 64;
+  if (N / 32 >= slots / 2) return 32;
+  return 16;
+}
+
+int i8_gemm_launch(const CUtensorMap& tmA, const CUtensorMap& tmB, I8Params p, int num_sms, cudaStream_t stream) {
+  const int strip = p.strip;
+  dim3 grid((unsigned)(p.N / strip), (unsigned)((p.M + 15) / 16));
+  switch (strip) {
+    case 16: return launch_i8<2>(tmA, tmB, p, grid, stream);
+    case 32: return launch_i8<4>(tmA, tmB, p, grid, stream);
+    default: return launch_i8<8>(tmA, tmB, p, grid, stream);
   }
 }
 

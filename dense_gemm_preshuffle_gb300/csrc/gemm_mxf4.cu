@@ -165,7 +165,9 @@ __global__ void __launch_bounds__(F4_THREADS, 1)
           }
         }
       }
-      if (!ok) {
+      if (!ok || *abort_flag) {
+        // Another role (or this one) gave up: wait (bounded) for the loads
+        // still in flight, so nothing lands in shared memory after exit.
         const uint32_t n = issued < (uint32_t)F4_STAGES ? issued : (uint32_t)F4_STAGES;
         for (uint32_t i = 0; i < n; ++i) {
           const uint32_t q = issued - 1 - i;

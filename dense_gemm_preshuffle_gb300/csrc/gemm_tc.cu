@@ -178,9 +178,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           }
         }
       }
-      if (!ok) {
-        // Drain: wait (bounded) for the loads still in flight, so nothing
-        // lands in shared memory after this CTA exits.
+      if (!ok || *sm.abort_flag) {
+        // Another role (or this one) gave up: wait (bounded) for the loads
+        // still in flight, so nothing lands in shared memory after exit.
         const uint32_t n = issued < (uint32_t)STAGES ? issued : (uint32_t)STAGES;
         for (uint32_t i = 0; i < n; ++i) {
           const uint32_t q = issued - 1 - i;

@@ -36,7 +36,8 @@ struct I8Params {
 int tc_gemm_launch(int kind, int bn, const CUtensorMap& tmA, const CUtensorMap& tmC, TcParams p, int num_sms,
                    cudaStream_t stream);
 int mxf4_gemm_launch(const CUtensorMap& tmA, const CUtensorMap& tmC, TcParams p, int num_sms, cudaStream_t stream);
-int i8_gemm_launch(const uint8_t* A, I8Params p, int num_sms, cudaStream_t stream);
+int i8_strip_rows(int N, int num_sms);
+int i8_gemm_launch(const CUtensorMap& tmA, const CUtensorMap& tmB, I8Params p, int num_sms, cudaStream_t stream);
 
 int pack_b_launch(const uint8_t* B, const uint8_t* Bsf, int64_t N, int64_t kbytes, int64_t nblk, uint8_t* out,
                   cudaStream_t stream);
