@@ -75,7 +75,7 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
 template <int NB8>
 __global__ void __launch_bounds__(I8_THREADS, (NB8 <= 4 ? I8_CTAS_PER_SM : 1))
     i8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, I8Params p) {
-  constexpr int SN = NB8 * 8;                    // rows of B per CTA (divides 128)
+  constexpr int SN = NB8 * 8;                    // rows of B per CTA (a multiple of 16)
   constexpr int A_BYTES = I8_KT_PER_STAGE * 16 * 128;
   constexpr int B_BYTES = I8_KT_PER_STAGE * SN * 128;
   constexpr int STAGE = A_BYTES + B_BYTES;
@@ -88,7 +88,7 @@ __global__ void __launch_bounds__(I8_THREADS, (NB8 <= 4 ? I8_CTAS_PER_SM : 1))
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int n0 = blockIdx.x * SN;
-  const int band = n0 >> 7, r0 = n0 & 127;
+  const int rows = min(SN, p.N - n0);  // valid rows of this strip (a multiple of 16)
   const int mg = blockIdx.y;
   const int nstages = (p.ktiles + I8_KT_PER_STAGE - 1) / I8_KT_PER_STAGE;
   const uint64_t limit = p.wait_limit_ns;
@@ -107,10 +107,13 @@ __global__ void __launch_bounds__(I8_THREADS, (NB8 <= 4 ? I8_CTAS_PER_SM : 1))
     // Warm L2 with this CTA's whole weight strip while the previous kernel
     // on the stream may still run: a prefetch is only a cache hint.
     for (int q = 0; q < nstages; ++q)
-      asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
-                       reinterpret_cast<uint64_t>(&tmB)),
-                   "r"(0), "r"(r0), "r"(q * I8_KT_PER_STAGE), "r"(band)
-                   : "memory");
+#pragma unroll
+      for (int j = 0; j < SN / 16; ++j)
+        if (16 * j < rows)
+        asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                         reinterpret_cast<uint64_t>(&tmB)),
+                     "r"(0), "r"((n0 + 16 * j) & 127), "r"(q * I8_KT_PER_STAGE), "r"((n0 + 16 * j) >> 7)
+                     : "memory");
   }
   pdl_launch_dependents();
   __syncthreads();
@@ -137,13 +140,16 @@ __global__ void __launch_bounds__(I8_THREADS, (NB8 <= 4 ? I8_CTAS_PER_SM : 1))
             "l"(reinterpret_cast<uint64_t>(&tmA)), "r"(0), "r"(mg * 16), "r"(q * I8_KT_PER_STAGE),
             "r"(smem_u32(&full[s]))
             : "memory");
-        // B: 8 K tiles x SN rows x 128 B of the packed band, one copy
-        asm volatile(
-            "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];" ::
-                "r"(smem_u32(st + A_BYTES)),
-            "l"(reinterpret_cast<uint64_t>(&tmB)), "r"(0), "r"(r0), "r"(q * I8_KT_PER_STAGE), "r"(band),
-            "r"(smem_u32(&full[s]))
-            : "memory");
+        // B: 16-row pieces of the strip, 8 K tiles each (a 16-row piece never
+        // crosses a 128-row band of the packed layout)
+#pragma unroll
+        for (int j = 0; j < SN / 16; ++j)
+          asm volatile(
+              "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];" ::
+                  "r"(smem_u32(st + A_BYTES + j * (I8_KT_PER_STAGE * 16 * 128))),
+              "l"(reinterpret_cast<uint64_t>(&tmB)), "r"(0), "r"((n0 + 16 * j) & 127), "r"(q * I8_KT_PER_STAGE),
+              "r"((n0 + 16 * j) >> 7), "r"(smem_u32(&full[s]))
+              : "memory");
         ++issued;
       }
       if (!ok || *abort_flag) {
@@ -172,7 +178,7 @@ __global__ void __launch_bounds__(I8_THREADS, (NB8 <= 4 ? I8_CTAS_PER_SM : 1))
     if (!wait_bounded(&full[s], ph, abort_flag, p.status, ST_TIMEOUT_CONSUMER, limit)) break;
     const bool live = q * I8_KT_PER_STAGE + warp < p.ktiles;
     const uint8_t* sa = base + s * STAGE + warp * (16 * 128);
-    const uint8_t* sbp = base + s * STAGE + A_BYTES + warp * (SN * 128);
+    const uint8_t* sbp = base + s * STAGE + A_BYTES + warp * (16 * 128);  // + piece * (8 * 16 * 128)
     float f[NB8][4];
 #pragma unroll
     for (int nb = 0; nb < NB8; ++nb) f[nb][0] = f[nb][1] = f[nb][2] = f[nb][3] = 0.f;
@@ -183,7 +189,9 @@ __global__ void __launch_bounds__(I8_THREADS, (NB8 <= 4 ? I8_CTAS_PER_SM : 1))
       const uint4 ag8 = *reinterpret_cast<const uint4*>(sa + (g + 8) * 128 + slot);
       uint4 bw[NB8];
 #pragma unroll
-      for (int nb = 0; nb < NB8; ++nb) bw[nb] = *reinterpret_cast<const uint4*>(sbp + (nb * 8 + g) * 128 + slot);
+      for (int nb = 0; nb < NB8; ++nb)
+        bw[nb] = *reinterpret_cast<const uint4*>(sbp + (nb >> 1) * (I8_KT_PER_STAGE * 16 * 128) +
+                                                 ((nb & 1) * 8 + g) * 128 + slot);
       if (h == 1) {
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);  // this warp's reads of the stage are done
@@ -228,8 +236,8 @@ __global__ void __launch_bounds__(I8_THREADS, (NB8 <= 4 ? I8_CTAS_PER_SM : 1))
     red[(warp * 16 + g + 8) * SN + col + 1] = acc[nb][3];
   }
   named_bar_sync(1, I8_CW * 32);
-  for (int i = threadIdx.x; i < 16 * SN; i += I8_CW * 32) {
-    const int m = i / SN, n = i - m * SN;
+  for (int i = threadIdx.x; i < 16 * rows; i += I8_CW * 32) {
+    const int m = i / rows, n = i - m * rows;
     int sum = 0;
 #pragma unroll
     for (int w = 0; w < I8_CW; ++w) sum += red[(w * 16 + m) * SN + n];
@@ -279,22 +287,29 @@ static int launch_i8(const CUtensorMap& tmA, const CUtensorMap& tmB, I8Params p,
 }
 
 int i8_strip_rows(int N, int num_sms) {
-  // 16, 32 or 64 rows (a divisor of the 128-row band), chosen so the strips
-  // fill both CTA slots of every SM; GP_I8_STRIP overrides.
+  // Rows of B per CTA, a multiple of 16 (every strip is a whole number of
+  // 16-row pieces).  Prefer strips of at most 32 rows, which let two CTAs
+  // share an SM: with programmatic dependent launch the next product's CTAs
+  // then sit beside this one's and stream while it computes (measured 8.5 us
+  // against 9.5 us for one 48-row strip per SM at 16 x 7168 x 4096).  Wider
+  // problems take one strip per SM, at most 64 rows.  GP_I8_STRIP (16, 32,
+  // 48 or 64) overrides.
   static const int strip_override = env_int("GP_I8_STRIP", 0);
-  if (strip_override == 16 || strip_override == 32 || strip_override == 64) return strip_override;
-  const int slots = I8_CTAS_PER_SM * num_sms;
-  if (N / 64 >= slots) return 64;
-  if (N / 32 >= slots / 2) return 32;
-  return 16;
+  if (strip_override == 16 || strip_override == 32 || strip_override == 48 || strip_override == 64)
+    return strip_override;
+  const int two_per_sm = 16 * ((N + 16 * I8_CTAS_PER_SM * num_sms - 1) / (16 * I8_CTAS_PER_SM * num_sms));
+  if (two_per_sm <= 32) return two_per_sm;
+  const int one_per_sm = 16 * ((N + 16 * num_sms - 1) / (16 * num_sms));
+  return one_per_sm > 64 ? 64 : one_per_sm;
 }
 
 int i8_gemm_launch(const CUtensorMap& tmA, const CUtensorMap& tmB, I8Params p, int num_sms, cudaStream_t stream) {
   const int strip = p.strip;
-  dim3 grid((unsigned)(p.N / strip), (unsigned)((p.M + 15) / 16));
+  dim3 grid((unsigned)((p.N + strip - 1) / strip), (unsigned)((p.M + 15) / 16));
   switch (strip) {
     case 16: return launch_i8<2>(tmA, tmB, p, grid, stream);
     case 32: return launch_i8<4>(tmA, tmB, p, grid, stream);
+    case 48: return launch_i8<6>(tmA, tmB, p, grid, stream);
     default: return launch_i8<8>(tmA, tmB, p, grid, stream);
   }
 }

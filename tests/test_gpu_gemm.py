@@ -198,6 +198,18 @@ def test_guard_bands_untouched():
     check(ops8, C8)
 
 
+def test_int8_partial_last_strip_guard_bands():
+    # 7168 rows of B split into 48-row strips leave a 16-row last strip
+    ops = inputs.make_operands("int8", 16, 7168, 1024, seed=21)
+    M, N = ops.M, ops.N
+    guard = 8192
+    buf = torch.full((M * N + 2 * guard,), -5, dtype=torch.int32, device="cuda")
+    C = buf[guard:guard + M * N].view(M, N)
+    gpu_gemm(ops, out=C)
+    assert (buf[:guard] == -5).all() and (buf[guard + M * N:] == -5).all()
+    check(ops, C)
+
+
 def test_repeatable_bitwise():
     ops = inputs.make_operands("e4m3", 512, 1024, 1024, seed=2)
     A, B, sa, sb = dev(ops)
