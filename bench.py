@@ -164,13 +164,20 @@ def barrier(pg, device=None):
             pg.barrier()
 
 
-def max_over_ranks(pg, x: float, device):
+def max_over_ranks(pg, x: float, device=None):
+    """The maximum of x over all ranks (x itself without a process group)."""
     if pg is None:
         return x
     import torch
     t = torch.tensor([x], dtype=torch.float64, device=device)
     pg.all_reduce(t, op=pg.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_value(world: int, flops_per_step: float, steps: int, max_seconds: float) -> float:
+    """Weak scaling: every rank runs its own problem; the job's throughput is
+    all ranks' work over the slowest rank's time (TFLOP/s)."""
+    return world * flops_per_step * steps / max_seconds / 1e12
 
 
 # ------------------------------------------------------------------ our arm
@@ -373,7 +380,7 @@ def run_ours(args):
     clocks.stop()
 
     per = sec / args.steps
-    value = world * prob.flops * args.steps / sec / 1e12
+    value = whole_job_value(world, prob.flops, args.steps, sec)
     out = {
         "metric": METRIC,
         "value": round(value, 2),
