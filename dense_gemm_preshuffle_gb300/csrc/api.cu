@@ -254,9 +254,12 @@ int gemm_run(const void* A, const void* B_packed, int dtype, int64_t M, int64_t 
     return i8_gemm_launch(tmA, tmB, p, d->num_sms, st);
   }
 
+  // Tile height: 256 rows (two 128-row MMAs sharing each B tile) when that
+  // still gives every SM several tiles; the E2M1 kernel uses 128.
+  const int bm = dtype == GP_E2M1 ? 128 : tc_tile_m(M, N, d->num_sms);
   CUtensorMap tmA, tmC;
-  if ((rc = encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, (uint64_t)kb, (uint64_t)M, (uint64_t)kb, 128, 128,
-                      CU_TENSOR_MAP_SWIZZLE_128B)) != GP_OK)
+  if ((rc = encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, (uint64_t)kb, (uint64_t)M, (uint64_t)kb, 128,
+                      (uint32_t)bm, CU_TENSOR_MAP_SWIZZLE_128B)) != GP_OK)
     return rc;
   if ((rc = encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, C, (uint64_t)N, (uint64_t)M, (uint64_t)N * 2, 64, 32,
                       CU_TENSOR_MAP_SWIZZLE_128B)) != GP_OK)
@@ -281,8 +284,8 @@ int gemm_run(const void* A, const void* B_packed, int dtype, int64_t M, int64_t 
     return mxf4_gemm_launch(tmA, tmC, p, d->num_sms, st);
   }
   const int64_t tiles_256 = ((M + 127) / 128) * (N / 256);
-  const int bn = (N % 256 == 0 && tiles_256 >= d->num_sms) ? 256 : 128;
-  return tc_gemm_launch(dtype == GP_BF16 ? 0 : 1, bn, tmA, tmC, p, d->num_sms, st);
+  const int bn = bm == 256 ? 256 : ((N % 256 == 0 && tiles_256 >= d->num_sms) ? 256 : 128);
+  return tc_gemm_launch(dtype == GP_BF16 ? 0 : 1, bm, bn, tmA, tmC, p, d->num_sms, st);
 }
 
 int gemm_last_device_status(void* stream) {

@@ -1,34 +1,42 @@
 // tcgen05 GEMM for sm_103a: C[M,N] = A[M,K] . B[N,K]^T with B pre-packed.
 //
-// "GEMM Optimization Guide" sections 1-7 describe the method on AMD CDNA:
-//   - tiles of C
-//   - a double-buffered K loop (section 2)
-//   - a bank-conflict-free swizzle on both the write and read paths (section 3)
-//   - B loaded straight from its preshuffled layout (sections 4.2, 12)
-//   - an epilogue that scales, casts and stores coalesced (section 7)
+// "GEMM Optimization Guide", sections 1-7, describes the method on AMD CDNA:
+//   - tiles of C;
+//   - a double-buffered K loop (section 2);
+//   - a bank-conflict-free swizzle on both the write and read paths (section 3);
+//   - B loaded straight from its preshuffled layout (sections 4.2 and 12);
+//   - an epilogue that scales, casts and stores coalesced (section 7).
 //
-// This kernel is the Blackwell form of the same steps:
-//   - One persistent CTA per SM walks 128 x BN output tiles in a grouped
+// This kernel is the Blackwell form of those steps.
+//   - One persistent CTA per SM walks BM x BN output tiles in a grouped
 //     order, so that concurrent CTAs share A rows and B columns in L2.
 //   - Warp 0, one lane, is the producer.  Each K step it issues one 2-D TMA
-//     load for the 128 x 128-byte A tile (128-byte swizzle, rows >= M
-//     zero-filled) and BN/128 plain bulk copies of 16 KiB packed-B tiles.
-//     The packed tiles are already in the swizzled image.  Everything lands
-//     in an S-stage shared-memory ring with full/empty mbarriers.
-//   - Warp 1, one lane, issues tcgen05.mma.  The fp32 accumulator lives in
-//     tensor memory, double-buffered (2 x BN columns), so the epilogue of
-//     tile i overlaps the main loop of tile i+1.  tcgen05.commit releases
-//     each ring stage and signals a finished accumulator.
-//   - Warps 2-5 are the epilogue.  Each warp reads its 32 TMEM lanes with
-//     tcgen05.ld and forms acc * scale_a[m] * scale_b[n] in fp32.  It rounds
-//     to bf16 (RNE) and writes 32 x 64 staging tiles with the 128-byte
-//     swizzle, so the shared-memory stores are free of bank conflicts.
-//     A TMA store then writes them out; it clips rows >= M.
+//     load for the BM x 128-byte A tile (128-byte swizzle, rows >= M
+//     zero-filled) and BN/128 plain bulk copies of 16 KiB packed-B tiles,
+//     which already hold the swizzled image.  Data lands in an S-stage
+//     shared-memory ring with full/empty mbarriers.
+//   - Warp 1, one lane, issues tcgen05.mma.  Each 128-row half of the tile
+//     has its own fp32 accumulator in tensor memory, and both halves
+//     multiply the same B tile.
+//   - The accumulators are double-buffered when they fit (2 x BM/128 x BN
+//     <= 512 columns), so the epilogue of one tile overlaps the main loop of
+//     the next.  tcgen05.commit releases each ring stage and signals a
+//     finished accumulator.
+//   - Warps 2-5 are the epilogue.  Each warp reads its 32 TMEM lanes (in each
+//     half) with tcgen05.ld and forms acc * scale_a[m] * scale_b[n] in fp32.
+//     It rounds to bf16 (RNE) and writes 32 x 64 staging tiles with the
+//     128-byte swizzle, so the shared-memory stores are free of bank
+//     conflicts.  A TMA store writes the tiles out and clips rows >= M.
 //
-// KIND: 0 = bf16 x bf16 (kind::f16), 1 = e4m3 x e4m3 (kind::f8f6f4),
-//       2 = e2m1 x e2m1 with UE8M0 block-32 scales (kind::mxf4).
-// In every case one K step moves 128 bytes of each row: 64 bf16, 128 e4m3
-// or 256 e2m1 elements.  One MMA instruction consumes 32 bytes of K.
+// Why BM = 256: on GB300 each SM takes in operands at about 110 GB/s from
+// L2.  For the 128 x 256 tile that bound caps FP8 near 2.9 PFLOP/s.
+// A 256 x 256 tile does twice the math per B byte: 64 KiB per K step
+// instead of 2 x 48 KiB.  The cost is a single-buffered 512-column
+// accumulator.
+//
+// KIND: 0 = bf16 x bf16 (kind::f16), 1 = e4m3 x e4m3 (kind::f8f6f4).  One K
+// step moves 128 bytes of each row (64 bf16 or 128 e4m3 elements), and one
+// MMA instruction consumes 32 bytes of K.
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -36,46 +44,25 @@ namespace gp {
 
 constexpr int TC_THREADS = 192;
 
-template <int KIND, int BN, int STAGES>
+template <int BM, int BN, int STAGES>
 struct TcCfg {
-  static constexpr int BM = 128;
+  static constexpr int MH = BM / 128;  // 128-row halves (one MMA each)
   static constexpr int A_BYTES = BM * 128;
   static constexpr int B_BYTES = BN * 128;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  // E2M1 only: per stage, A scales (128 rows x 8 blocks) and B scales
-  // (BN rows x 8 blocks) in the 512-byte groups tcgen05.cp reads.
-  static constexpr int SFA_BYTES = (KIND == 2) ? 1024 : 0;
-  static constexpr int SFB_BYTES = (KIND == 2) ? BN * 8 : 0;
   static constexpr int EPI_BYTES = 4 * 32 * 128;
-  static constexpr int ACC_COLS = 2 * BN;
-  // Scale-factor TMEM columns per stage: A 2 groups x 4 cols, B 2 groups x BN/32 cols.
-  static constexpr int SF_COLS_PER_STAGE = (KIND == 2) ? (8 + 2 * (BN / 32)) : 0;
-  static constexpr int TMEM_NEED = ACC_COLS + STAGES * SF_COLS_PER_STAGE;
-  static constexpr int TMEM_COLS = TMEM_NEED <= 32 ? 32 : TMEM_NEED <= 64 ? 64 : TMEM_NEED <= 128 ? 128
-                                   : TMEM_NEED <= 256 ? 256 : 512;
+  static constexpr int ACC_COLS = MH * BN;  // one accumulator buffer
+  static constexpr int NBUF = (2 * ACC_COLS <= 512) ? 2 : 1;
+  static constexpr int TMEM_NEED = NBUF * ACC_COLS;
+  static constexpr int TMEM_COLS = TMEM_NEED <= 128 ? 128 : TMEM_NEED <= 256 ? 256 : 512;
   static_assert(TMEM_NEED <= 512, "tensor memory budget");
   static constexpr int BAR_BYTES = 256;
-  static constexpr int SMEM = STAGES * (STAGE_BYTES + SFA_BYTES + SFB_BYTES) + EPI_BYTES + BAR_BYTES + 1024;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES + 1024;
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
-struct TcSmem {
-  uint8_t* a;
-  uint8_t* b;
-  uint8_t* sfa;
-  uint8_t* sfb;
-  uint8_t* epi;
-  uint64_t* full;
-  uint64_t* empty;
-  uint64_t* accf;
-  uint64_t* acce;
-  uint64_t* drain;
-  uint32_t* tmem_slot;
-  volatile int* abort_flag;
-};
-
 __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int& mb, int& nb) {
-  constexpr int G = 16;  // M tiles per group: 152 concurrent tiles cover ~16 x 10 tiles
+  constexpr int G = 16;  // M tiles per group: concurrent CTAs cover a compact block of C
   const int group_size = G * tiles_n;
   const int group = t / group_size;
   const int first_m = group * G;
@@ -85,25 +72,23 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int
   nb = r / gm;
 }
 
-template <int KIND, int BN, int STAGES>
+template <int KIND, int BM, int BN, int STAGES>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmC, TcParams p) {
-  using Cfg = TcCfg<KIND, BN, STAGES>;
+  using Cfg = TcCfg<BM, BN, STAGES>;
+  constexpr int NBUF = Cfg::NBUF;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  TcSmem sm;
-  sm.a = base;
-  sm.b = sm.a + STAGES * Cfg::A_BYTES;
-  sm.sfa = sm.b + STAGES * Cfg::B_BYTES;
-  sm.sfb = sm.sfa + STAGES * Cfg::SFA_BYTES;
-  sm.epi = sm.sfb + STAGES * Cfg::SFB_BYTES;
-  sm.full = reinterpret_cast<uint64_t*>(sm.epi + Cfg::EPI_BYTES);
-  sm.empty = sm.full + STAGES;
-  sm.accf = sm.empty + STAGES;
-  sm.acce = sm.accf + 2;
-  sm.drain = sm.acce + 2;
-  sm.tmem_slot = reinterpret_cast<uint32_t*>(sm.drain + 1);
-  sm.abort_flag = reinterpret_cast<volatile int*>(sm.tmem_slot + 1);
+  uint8_t* s_a = base;
+  uint8_t* s_b = s_a + STAGES * Cfg::A_BYTES;
+  uint8_t* s_epi = s_b + STAGES * Cfg::B_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(s_epi + Cfg::EPI_BYTES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* accf = empty + STAGES;
+  uint64_t* acce = accf + 2;
+  uint64_t* drain = acce + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -111,20 +96,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&sm.full[s], 1);
-      mbar_init(&sm.empty[s], 1);
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&sm.accf[b], 1);
-      mbar_init(&sm.acce[b], 4);
+      mbar_init(&accf[b], 1);
+      mbar_init(&acce[b], 4);
     }
-    mbar_init(sm.drain, 1);
-    *sm.abort_flag = 0;
+    mbar_init(drain, 1);
+    *abort_flag = 0;
     fence_mbar_init();
     prefetch_tensormap(&tmA);
     prefetch_tensormap(&tmC);
   }
-  if (warp == 1) tmem_alloc<Cfg::TMEM_COLS>(sm.tmem_slot);
+  if (warp == 1) tmem_alloc<Cfg::TMEM_COLS>(tmem_slot);
   if (threadIdx.x == 32 * 2 && (int)blockIdx.x < p.num_tiles) {
     // Warm L2 with the first K steps of this CTA's first tile while the
     // previous kernel may still run (a prefetch never changes later loads).
@@ -132,7 +117,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     tile_coords(blockIdx.x, p.tiles_m, p.tiles_n, mb, nb);
     const int kpre = p.ktiles < STAGES ? p.ktiles : STAGES;
     for (int kt = 0; kt < kpre; ++kt) {
-      prefetch_l2_tile_2d(&tmA, kt * 128, mb * 128);
+      prefetch_l2_tile_2d(&tmA, kt * 128, mb * BM);
       for (int j = 0; j < BN / 128; ++j)
         prefetch_l2_bulk(p.Bp + ((size_t)(nb * (BN / 128) + j) * p.ktiles + kt) * 16384, 16384);
     }
@@ -142,7 +127,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   pdl_wait();  // inputs may come from, and C may be read by, the previous kernel
-  const uint32_t tmem_base = *sm.tmem_slot;
+  const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -157,7 +142,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         tile_coords(t, p.tiles_m, p.tiles_n, mb, nb);
         const uint8_t* bsrc = p.Bp + (size_t)nb * (BN / 128) * p.ktiles * 16384;
         for (int kt = 0; kt < p.ktiles; ++kt) {
-          if (!wait_bounded(&sm.empty[s], ph ^ 1, sm.abort_flag, p.status, ST_TIMEOUT_PRODUCER, limit)) {
+          if (!wait_bounded(&empty[s], ph ^ 1, abort_flag, p.status, ST_TIMEOUT_PRODUCER, limit)) {
             ok = false;
             break;
           }
@@ -165,11 +150,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             // Fault injection (host-selected): leave this stage's barrier
             // without its arrival, so the consumer's bounded wait times out.
           } else {
-            mbar_arrive_expect_tx(&sm.full[s], Cfg::STAGE_BYTES + Cfg::SFA_BYTES + Cfg::SFB_BYTES);
-            tma_load_2d(sm.a + s * Cfg::A_BYTES, &tmA, kt * 128, mb * 128, &sm.full[s]);
+            mbar_arrive_expect_tx(&full[s], Cfg::STAGE_BYTES);
+            tma_load_2d(s_a + s * Cfg::A_BYTES, &tmA, kt * 128, mb * BM, &full[s]);
             for (int j = 0; j < BN / 128; ++j)
-              bulk_load_hint(sm.b + s * Cfg::B_BYTES + j * 16384,
-                             bsrc + ((size_t)j * p.ktiles + kt) * 16384, 16384, &sm.full[s], pol_b);
+              bulk_load_hint(s_b + s * Cfg::B_BYTES + j * 16384, bsrc + ((size_t)j * p.ktiles + kt) * 16384, 16384,
+                             &full[s], pol_b);
           }
           ++issued;
           if (++s == STAGES) {
@@ -178,7 +163,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           }
         }
       }
-      if (!ok || *sm.abort_flag) {
+      if (!ok || *abort_flag) {
         // Another role (or this one) gave up: wait (bounded) for the loads
         // still in flight, so nothing lands in shared memory after exit.
         const uint32_t n = issued < (uint32_t)STAGES ? issued : (uint32_t)STAGES;
@@ -188,7 +173,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           const uint32_t par = (q / STAGES) & 1;
           volatile int never = 0;
           if (p.debug_skip_load == 1 + (int)q) continue;
-          wait_bounded(&sm.full[st], par, &never, p.status, ST_TIMEOUT_DRAIN, limit);
+          wait_bounded(&full[st], par, &never, p.status, ST_TIMEOUT_DRAIN, limit);
         }
       }
     }
@@ -202,106 +187,110 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       int local = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x, ++local) {
-        const int buf = local & 1;
-        const uint32_t use = (uint32_t)(local >> 1);
-        if (!wait_bounded(&sm.acce[buf], (use & 1) ^ 1, sm.abort_flag, p.status, ST_TIMEOUT_MMA, limit)) {
+        const int buf = local % NBUF;
+        const uint32_t use = (uint32_t)(local / NBUF);
+        if (!wait_bounded(&acce[buf], (use & 1) ^ 1, abort_flag, p.status, ST_TIMEOUT_MMA, limit)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t d = tmem_base + (uint32_t)(buf * BN);
+        const uint32_t d = tmem_base + (uint32_t)(buf * Cfg::ACC_COLS);
         for (int kt = 0; kt < p.ktiles; ++kt) {
-          if (!wait_bounded(&sm.full[s], ph, sm.abort_flag, p.status, ST_TIMEOUT_MMA, limit)) {
+          if (!wait_bounded(&full[s], ph, abort_flag, p.status, ST_TIMEOUT_MMA, limit)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = smem_u32(sm.a + s * Cfg::A_BYTES);
-          const uint32_t b0 = smem_u32(sm.b + s * Cfg::B_BYTES);
+          const uint32_t a0 = smem_u32(s_a + s * Cfg::A_BYTES);
+          const uint32_t b0 = smem_u32(s_b + s * Cfg::B_BYTES);
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            if constexpr (KIND == 2) {
-              // not instantiated here; see the block-scaled kernel
-            } else {
-              umma<KIND>(d, smem_desc_sw128(a0 + 32 * k), smem_desc_sw128(b0 + 32 * k), idesc,
+            const uint64_t bdesc = smem_desc_sw128(b0 + 32 * k);
+#pragma unroll
+            for (int mh = 0; mh < Cfg::MH; ++mh)
+              umma<KIND>(d + (uint32_t)(mh * BN), smem_desc_sw128(a0 + mh * 16384 + 32 * k), bdesc, idesc,
                          (kt | k) != 0 ? 1u : 0u);
-            }
           }
-          umma_commit(&sm.empty[s]);
+          umma_commit(&empty[s]);
           if (++s == STAGES) {
             s = 0;
             ph ^= 1;
           }
         }
         if (!ok) break;
-        umma_commit(&sm.accf[buf]);
+        umma_commit(&accf[buf]);
       }
       // Make sure every issued MMA has completed before TMEM is released.
-      umma_commit(sm.drain);
+      umma_commit(drain);
       volatile int never = 0;
-      wait_bounded(sm.drain, 0, &never, p.status, ST_TIMEOUT_DRAIN, limit);
+      wait_bounded(drain, 0, &never, p.status, ST_TIMEOUT_DRAIN, limit);
     }
   } else {
     // ------------------------------------------------------------ epilogue
     const int quad = warp & 3;  // TMEM lanes this warp may access: quad*32 .. +31
-    uint8_t* stg = sm.epi + (warp - 2) * 4096;
+    uint8_t* stg = s_epi + (warp - 2) * 4096;
     const uint32_t stg_row = smem_u32(stg) + lane * 128;
     int local = 0;
     for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++local) {
       int mb, nb;
       tile_coords(t, p.tiles_m, p.tiles_n, mb, nb);
-      const int buf = local & 1;
-      const uint32_t use = (uint32_t)(local >> 1);
-      if (!wait_bounded(&sm.accf[buf], use & 1, sm.abort_flag, p.status, ST_TIMEOUT_EPILOGUE, limit)) break;
+      const int buf = local % NBUF;
+      const uint32_t use = (uint32_t)(local / NBUF);
+      if (!wait_bounded(&accf[buf], use & 1, abort_flag, p.status, ST_TIMEOUT_EPILOGUE, limit)) break;
       tc_fence_after();
-      const int row0 = mb * 128 + quad * 32;
-      const int m = row0 + lane;
-      const float sa = (p.sa != nullptr && m < p.M) ? __ldg(p.sa + m) : 1.0f;
-      const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(buf * BN);
 #pragma unroll 1
-      for (int c = 0; c < BN / 64; ++c) {
-        const int n0 = nb * BN + c * 64;
-        // the previous TMA store from this staging tile must have read it
-        if (lane == 0) bulk_wait_group_read<0>();
-        __syncwarp();
+      for (int mh = 0; mh < Cfg::MH; ++mh) {
+        const int row0 = mb * BM + mh * 128 + quad * 32;
+        const int m = row0 + lane;
+        const float sa = (p.sa != nullptr && m < p.M) ? __ldg(p.sa + m) : 1.0f;
+        const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(buf * Cfg::ACC_COLS + mh * BN);
+#pragma unroll 1
+        for (int c = 0; c < BN / 64; ++c) {
+          const int n0 = nb * BN + c * 64;
+          // the previous TMA store from this staging tile must have read it
+          if (lane == 0) bulk_wait_group_read<0>();
+          __syncwarp();
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(tbase + (uint32_t)(c * 64 + h * 32), r);
-          tmem_ld_wait();
-          uint32_t pk[16];
-          if (p.sb != nullptr) {
-            const float4* sb4 = reinterpret_cast<const float4*>(p.sb + n0 + h * 32);
+          for (int h = 0; h < 2; ++h) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(tbase + (uint32_t)(c * 64 + h * 32), r);
+            tmem_ld_wait();
+            uint32_t pk[16];
+            if (p.sb != nullptr) {
+              const float4* sb4 = reinterpret_cast<const float4*>(p.sb + n0 + h * 32);
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              const float4 s4 = __ldg(sb4 + q);
-              pk[2 * q] = pack_bf16x2(__uint_as_float(r[4 * q]) * sa * s4.x, __uint_as_float(r[4 * q + 1]) * sa * s4.y);
-              pk[2 * q + 1] =
-                  pack_bf16x2(__uint_as_float(r[4 * q + 2]) * sa * s4.z, __uint_as_float(r[4 * q + 3]) * sa * s4.w);
+              for (int q = 0; q < 8; ++q) {
+                const float4 s4 = __ldg(sb4 + q);
+                pk[2 * q] =
+                    pack_bf16x2(__uint_as_float(r[4 * q]) * sa * s4.x, __uint_as_float(r[4 * q + 1]) * sa * s4.y);
+                pk[2 * q + 1] = pack_bf16x2(__uint_as_float(r[4 * q + 2]) * sa * s4.z,
+                                            __uint_as_float(r[4 * q + 3]) * sa * s4.w);
+              }
+            } else {
+#pragma unroll
+              for (int q = 0; q < 16; ++q)
+                pk[q] = pack_bf16x2(__uint_as_float(r[2 * q]), __uint_as_float(r[2 * q + 1]));
             }
-          } else {
+            // 128-byte swizzle: 16-byte chunk j of row `lane` goes to slot j ^ (lane % 8)
 #pragma unroll
-            for (int q = 0; q < 16; ++q) pk[q] = pack_bf16x2(__uint_as_float(r[2 * q]), __uint_as_float(r[2 * q + 1]));
+            for (int q = 0; q < 4; ++q) {
+              const int chunk = h * 4 + q;
+              st_shared_v4(stg_row + (uint32_t)(((chunk ^ (lane & 7)) * 16)), pk[4 * q], pk[4 * q + 1],
+                           pk[4 * q + 2], pk[4 * q + 3]);
+            }
           }
-          // 128-byte swizzle: 16-byte chunk j of row `lane` goes to slot j ^ (lane % 8)
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int chunk = h * 4 + q;
-            st_shared_v4(stg_row + (uint32_t)(((chunk ^ (lane & 7)) * 16)), pk[4 * q], pk[4 * q + 1], pk[4 * q + 2],
-                         pk[4 * q + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && row0 < p.M) {
+            tma_store_2d(&tmC, n0, row0, stg);
+            bulk_commit_group();
           }
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0 && row0 < p.M) {
-          tma_store_2d(&tmC, n0, row0, stg);
-          bulk_commit_group();
         }
       }
       // accumulator buffer is free once every lane's TMEM loads are done
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.acce[buf]);
+      if (lane == 0) mbar_arrive(&acce[buf]);
     }
     if (lane == 0) bulk_wait_group<0>();
   }
@@ -316,18 +305,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
 // ---------------------------------------------------------------- host side
 
-template <int KIND, int BN, int STAGES>
+template <int KIND, int BM, int BN, int STAGES>
 static int launch_tc(const CUtensorMap& tmA, const CUtensorMap& tmC, const TcParams& p, int grid,
                      cudaStream_t stream) {
-  using Cfg = TcCfg<KIND, BN, STAGES>;
-  auto kern = tc_gemm_kernel<KIND, BN, STAGES>;
+  using Cfg = TcCfg<BM, BN, STAGES>;
+  auto kern = tc_gemm_kernel<KIND, BM, BN, STAGES>;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 64 && !attr_set[dev]) {
+  if (dev >= 64 || !attr_set[dev]) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) != cudaSuccess)
       return GP_ERR_CUDA;
-    attr_set[dev] = true;
+    if (dev < 64) attr_set[dev] = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -343,18 +332,29 @@ static int launch_tc(const CUtensorMap& tmA, const CUtensorMap& tmC, const TcPar
   return cudaGetLastError() == cudaSuccess ? GP_OK : GP_ERR_CUDA;
 }
 
-int tc_gemm_launch(int kind, int bn, const CUtensorMap& tmA, const CUtensorMap& tmC, TcParams p, int num_sms,
+int tc_tile_m(int64_t M, int64_t N, int num_sms) {
+  // 256-row tiles when there are enough of them to fill every SM
+  // (at least 4 tiles per SM), else 128.
+  const int64_t tiles = ((M + 255) / 256) * (N / 256);
+  return (N % 256 == 0 && tiles >= 4 * (int64_t)num_sms) ? 256 : 128;
+}
+
+int tc_gemm_launch(int kind, int bm, int bn, const CUtensorMap& tmA, const CUtensorMap& tmC, TcParams p, int num_sms,
                    cudaStream_t stream) {
-  p.tiles_m = (p.M + 127) / 128;
+  p.tiles_m = (p.M + bm - 1) / bm;
   p.tiles_n = p.N / bn;
   p.num_tiles = p.tiles_m * p.tiles_n;
   const int grid = p.num_tiles < num_sms ? p.num_tiles : num_sms;
-  if (kind == 0) {
-    return bn == 256 ? launch_tc<0, 256, 4>(tmA, tmC, p, grid, stream) : launch_tc<0, 128, 6>(tmA, tmC, p, grid, stream);
-  } else if (kind == 1) {
-    return bn == 256 ? launch_tc<1, 256, 4>(tmA, tmC, p, grid, stream) : launch_tc<1, 128, 6>(tmA, tmC, p, grid, stream);
+  if (bm == 256) {
+    if (bn != 256) return GP_ERR_UNSUPPORTED;
+    return kind == 0 ? launch_tc<0, 256, 256, 3>(tmA, tmC, p, grid, stream)
+                     : launch_tc<1, 256, 256, 3>(tmA, tmC, p, grid, stream);
   }
-  return GP_ERR_UNSUPPORTED;
+  if (kind == 0)
+    return bn == 256 ? launch_tc<0, 128, 256, 4>(tmA, tmC, p, grid, stream)
+                     : launch_tc<0, 128, 128, 6>(tmA, tmC, p, grid, stream);
+  return bn == 256 ? launch_tc<1, 128, 256, 4>(tmA, tmC, p, grid, stream)
+                   : launch_tc<1, 128, 128, 6>(tmA, tmC, p, grid, stream);
 }
 
 }  // namespace gp

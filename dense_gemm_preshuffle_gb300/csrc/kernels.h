@@ -33,7 +33,8 @@ struct I8Params {
   int stages;
 };
 
-int tc_gemm_launch(int kind, int bn, const CUtensorMap& tmA, const CUtensorMap& tmC, TcParams p, int num_sms,
+int tc_tile_m(int64_t M, int64_t N, int num_sms);
+int tc_gemm_launch(int kind, int bm, int bn, const CUtensorMap& tmA, const CUtensorMap& tmC, TcParams p, int num_sms,
                    cudaStream_t stream);
 int mxf4_gemm_launch(const CUtensorMap& tmA, const CUtensorMap& tmC, TcParams p, int num_sms, cudaStream_t stream);
 int i8_strip_rows(int N, int num_sms);

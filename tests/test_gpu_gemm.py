@@ -157,6 +157,16 @@ def test_workload_sampled_rows(name):
     assert torch.isfinite(C.float()).all()
 
 
+@pytest.mark.parametrize("dtype", ["e4m3", "bf16"])
+def test_tile256_path_ragged(dtype):
+    # enough 256 x 256 tiles (17 x 38 >= 4 per SM) to take the 256-row tile
+    # path, with a ragged last row band
+    ops = inputs.make_operands(dtype, 4173, 9728, 256, seed=31)
+    C = gpu_gemm(ops)
+    rows = np.concatenate([sample_rows(ops.M, 24, seed=2), np.arange(4096, 4173)])
+    check(ops, C, rows=np.unique(rows))
+
+
 # ---------------------------------------------------------------- edge cases
 
 def test_int8_extremes_bit_exact():
