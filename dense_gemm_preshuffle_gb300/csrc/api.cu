@@ -255,8 +255,10 @@ int gemm_run(const void* A, const void* B_packed, int dtype, int64_t M, int64_t 
   }
 
   // Tile height: 256 rows (two 128-row MMAs sharing each B tile) when that
-  // still gives every SM several tiles; the E2M1 kernel uses 128.
-  const int bm = dtype == GP_E2M1 ? 128 : tc_tile_m(M, N, d->num_sms);
+  // still gives every SM several tiles, or when K is split over a cluster
+  // (few tiles); the E2M1 kernel uses 128.
+  const int split = dtype == GP_E2M1 ? 1 : splitk_choice(M, N, kb / 128, d->num_sms);
+  const int bm = dtype == GP_E2M1 ? 128 : (split > 1 ? 256 : tc_tile_m(M, N, d->num_sms));
   CUtensorMap tmA, tmC;
   if ((rc = encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, (uint64_t)kb, (uint64_t)M, (uint64_t)kb, 128,
                       (uint32_t)bm, CU_TENSOR_MAP_SWIZZLE_128B)) != GP_OK)
@@ -283,6 +285,7 @@ int gemm_run(const void* A, const void* B_packed, int dtype, int64_t M, int64_t 
     p.sfa = static_cast<const uint8_t*>(scale_a);
     return mxf4_gemm_launch(tmA, tmC, p, d->num_sms, st);
   }
+  if (split > 1) return splitk_gemm_launch(dtype == GP_BF16 ? 0 : 1, split, tmA, tmC, p, st);
   const int64_t tiles_256 = ((M + 127) / 128) * (N / 256);
   const int bn = bm == 256 ? 256 : ((N % 256 == 0 && tiles_256 >= d->num_sms) ? 256 : 128);
   return tc_gemm_launch(dtype == GP_BF16 ? 0 : 1, bm, bn, tmA, tmC, p, d->num_sms, st);

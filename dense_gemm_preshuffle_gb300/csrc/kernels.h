@@ -36,6 +36,9 @@ struct I8Params {
 int tc_tile_m(int64_t M, int64_t N, int num_sms);
 int tc_gemm_launch(int kind, int bm, int bn, const CUtensorMap& tmA, const CUtensorMap& tmC, TcParams p, int num_sms,
                    cudaStream_t stream);
+int splitk_choice(int64_t M, int64_t N, int64_t ktiles, int num_sms);
+int splitk_gemm_launch(int kind, int split, const CUtensorMap& tmA, const CUtensorMap& tmC, TcParams p,
+                       cudaStream_t stream);
 int mxf4_gemm_launch(const CUtensorMap& tmA, const CUtensorMap& tmC, TcParams p, int num_sms, cudaStream_t stream);
 int i8_strip_rows(int N, int num_sms);
 int i8_gemm_launch(const CUtensorMap& tmA, const CUtensorMap& tmB, I8Params p, int num_sms, cudaStream_t stream);

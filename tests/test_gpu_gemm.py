@@ -167,6 +167,16 @@ def test_tile256_path_ragged(dtype):
     check(ops, C, rows=np.unique(rows))
 
 
+@pytest.mark.parametrize("dtype,M,N,K", [("bf16", 400, 4096, 8192), ("e4m3", 300, 8192, 8192)])
+def test_split_k_cluster_path_ragged(dtype, M, N, K):
+    # few 256 x 256 tiles and a long K: K is split across a 4- (bf16) or
+    # 2-CTA (e4m3) cluster and reduced over distributed shared memory
+    ops = inputs.make_operands(dtype, M, N, K, seed=37)
+    C = gpu_gemm(ops)
+    rows = np.unique(np.concatenate([sample_rows(ops.M, 24, seed=3), np.arange(256, ops.M)]))
+    check(ops, C, rows=rows)
+
+
 # ---------------------------------------------------------------- edge cases
 
 def test_int8_extremes_bit_exact():
