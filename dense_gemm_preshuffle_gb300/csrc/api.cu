@@ -244,7 +244,7 @@ int gemm_run(const void* A, const void* B_packed, int dtype, int64_t M, int64_t 
     {
       cuuint64_t dims[4] = {128, 128, (cuuint64_t)p.ktiles, (cuuint64_t)(N / 128)};
       cuuint64_t strides[3] = {128, 16384, (cuuint64_t)p.ktiles * 16384};
-      cuuint32_t box[4] = {128, 16, 8, 1};
+      cuuint32_t box[4] = {128, (cuuint32_t)i8_box_rows_for(p.strip), 8, 1};
       cuuint32_t estr[4] = {1, 1, 1, 1};
       if (g_encode(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(B_packed), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

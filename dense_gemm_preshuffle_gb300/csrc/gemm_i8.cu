@@ -72,10 +72,16 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// Rows per B copy: the whole strip when it divides the 128-row band of the
+// packed layout (one copy per stage; each TMA copy costs a CTA ~170 ns
+// however large it is), else 16-row pieces, which never cross a band.
+__host__ __device__ constexpr int i8_box_rows(int sn) { return (128 % sn == 0) ? sn : 16; }
+
 template <int NB8>
 __global__ void __launch_bounds__(I8_THREADS, (NB8 <= 4 ? I8_CTAS_PER_SM : 1))
     i8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, I8Params p) {
   constexpr int SN = NB8 * 8;                    // rows of B per CTA (a multiple of 16)
+  constexpr int BOXR = i8_box_rows(SN);          // rows per B copy
   constexpr int A_BYTES = I8_KT_PER_STAGE * 16 * 128;
   constexpr int B_BYTES = I8_KT_PER_STAGE * SN * 128;
   constexpr int STAGE = A_BYTES + B_BYTES;
@@ -108,11 +114,11 @@ __global__ void __launch_bounds__(I8_THREADS, (NB8 <= 4 ? I8_CTAS_PER_SM : 1))
     // on the stream may still run: a prefetch is only a cache hint.
     for (int q = 0; q < nstages; ++q)
 #pragma unroll
-      for (int j = 0; j < SN / 16; ++j)
-        if (16 * j < rows)
+      for (int j = 0; j < SN / BOXR; ++j)
+        if (BOXR * j < rows)
         asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
                          reinterpret_cast<uint64_t>(&tmB)),
-                     "r"(0), "r"((n0 + 16 * j) & 127), "r"(q * I8_KT_PER_STAGE), "r"((n0 + 16 * j) >> 7)
+                     "r"(0), "r"((n0 + BOXR * j) & 127), "r"(q * I8_KT_PER_STAGE), "r"((n0 + BOXR * j) >> 7)
                      : "memory");
   }
   pdl_launch_dependents();
@@ -140,15 +146,15 @@ __global__ void __launch_bounds__(I8_THREADS, (NB8 <= 4 ? I8_CTAS_PER_SM : 1))
             "l"(reinterpret_cast<uint64_t>(&tmA)), "r"(0), "r"(mg * 16), "r"(q * I8_KT_PER_STAGE),
             "r"(smem_u32(&full[s]))
             : "memory");
-        // B: 16-row pieces of the strip, 8 K tiles each (a 16-row piece never
+        // B: BOXR-row pieces of the strip, 8 K tiles each (a piece never
         // crosses a 128-row band of the packed layout)
 #pragma unroll
-        for (int j = 0; j < SN / 16; ++j)
+        for (int j = 0; j < SN / BOXR; ++j)
           asm volatile(
               "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];" ::
-                  "r"(smem_u32(st + A_BYTES + j * (I8_KT_PER_STAGE * 16 * 128))),
-              "l"(reinterpret_cast<uint64_t>(&tmB)), "r"(0), "r"((n0 + 16 * j) & 127), "r"(q * I8_KT_PER_STAGE),
-              "r"((n0 + 16 * j) >> 7), "r"(smem_u32(&full[s]))
+                  "r"(smem_u32(st + A_BYTES + j * (I8_KT_PER_STAGE * BOXR * 128))),
+              "l"(reinterpret_cast<uint64_t>(&tmB)), "r"(0), "r"((n0 + BOXR * j) & 127), "r"(q * I8_KT_PER_STAGE),
+              "r"((n0 + BOXR * j) >> 7), "r"(smem_u32(&full[s]))
               : "memory");
         ++issued;
       }
@@ -178,7 +184,7 @@ __global__ void __launch_bounds__(I8_THREADS, (NB8 <= 4 ? I8_CTAS_PER_SM : 1))
     if (!wait_bounded(&full[s], ph, abort_flag, p.status, ST_TIMEOUT_CONSUMER, limit)) break;
     const bool live = q * I8_KT_PER_STAGE + warp < p.ktiles;
     const uint8_t* sa = base + s * STAGE + warp * (16 * 128);
-    const uint8_t* sbp = base + s * STAGE + A_BYTES + warp * (16 * 128);  // + piece * (8 * 16 * 128)
+    const uint8_t* sbp = base + s * STAGE + A_BYTES + warp * (BOXR * 128);  // + piece * (8 * BOXR * 128)
     float f[NB8][4];
 #pragma unroll
     for (int nb = 0; nb < NB8; ++nb) f[nb][0] = f[nb][1] = f[nb][2] = f[nb][3] = 0.f;
@@ -189,9 +195,11 @@ __global__ void __launch_bounds__(I8_THREADS, (NB8 <= 4 ? I8_CTAS_PER_SM : 1))
       const uint4 ag8 = *reinterpret_cast<const uint4*>(sa + (g + 8) * 128 + slot);
       uint4 bw[NB8];
 #pragma unroll
-      for (int nb = 0; nb < NB8; ++nb)
-        bw[nb] = *reinterpret_cast<const uint4*>(sbp + (nb >> 1) * (I8_KT_PER_STAGE * 16 * 128) +
-                                                 ((nb & 1) * 8 + g) * 128 + slot);
+      for (int nb = 0; nb < NB8; ++nb) {
+        const int row = nb * 8 + g;  // strip row; piece row / BOXR, row % BOXR within it
+        bw[nb] = *reinterpret_cast<const uint4*>(sbp + (row / BOXR) * (I8_KT_PER_STAGE * BOXR * 128) +
+                                                 (row % BOXR) * 128 + slot);
+      }
       if (h == 1) {
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);  // this warp's reads of the stage are done
@@ -302,6 +310,8 @@ int i8_strip_rows(int N, int num_sms) {
   const int one_per_sm = 16 * ((N + 16 * num_sms - 1) / (16 * num_sms));
   return one_per_sm > 64 ? 64 : one_per_sm;
 }
+
+int i8_box_rows_for(int strip) { return i8_box_rows(strip); }
 
 int i8_gemm_launch(const CUtensorMap& tmA, const CUtensorMap& tmB, I8Params p, int num_sms, cudaStream_t stream) {
   const int strip = p.strip;

@@ -41,6 +41,7 @@ int splitk_gemm_launch(int kind, int split, const CUtensorMap& tmA, const CUtens
                        cudaStream_t stream);
 int mxf4_gemm_launch(const CUtensorMap& tmA, const CUtensorMap& tmC, TcParams p, int num_sms, cudaStream_t stream);
 int i8_strip_rows(int N, int num_sms);
+int i8_box_rows_for(int strip);
 int i8_gemm_launch(const CUtensorMap& tmA, const CUtensorMap& tmB, I8Params p, int num_sms, cudaStream_t stream);
 
 int pack_b_launch(const uint8_t* B, const uint8_t* Bsf, int64_t N, int64_t kbytes, int64_t nblk, uint8_t* out,
