@@ -77,8 +77,12 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
 // however large it is), else 16-row pieces, which never cross a band.
 __host__ __device__ constexpr int i8_box_rows(int sn) { return (128 % sn == 0) ? sn : 16; }
 
+// CTAs that fit on one SM for a strip of NB8 * 8 rows (shared memory and
+// registers): 3 for 16-row strips, 2 up to 32 rows, else 1.
+__host__ __device__ constexpr int i8_ctas_per_sm(int nb8) { return nb8 <= 2 ? 3 : (nb8 <= 4 ? 2 : 1); }
+
 template <int NB8>
-__global__ void __launch_bounds__(I8_THREADS, (NB8 <= 4 ? I8_CTAS_PER_SM : 1))
+__global__ void __launch_bounds__(I8_THREADS, i8_ctas_per_sm(NB8))
     i8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, I8Params p) {
   constexpr int SN = NB8 * 8;                    // rows of B per CTA (a multiple of 16)
   constexpr int BOXR = i8_box_rows(SN);          // rows per B copy
@@ -269,7 +273,7 @@ static int launch_i8(const CUtensorMap& tmA, const CUtensorMap& tmB, I8Params p,
   constexpr int RED = I8_CW * 16 * NB8 * 8 * 4;
   constexpr int RING = I8_STAGES * STAGE;
   constexpr int SMEM = (RING > RED ? RING : RED) + 2 * I8_STAGES * 8 + 16 + 1024;
-  static_assert(SMEM * (NB8 <= 4 ? I8_CTAS_PER_SM : 1) <= 228 * 1024, "shared memory budget");
+  static_assert(SMEM * i8_ctas_per_sm(NB8) <= 228 * 1024, "shared memory budget");
   auto kern = i8_gemm_kernel<NB8>;
   static bool attr_set[64] = {};
   int dev = 0;
