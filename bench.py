@@ -50,6 +50,7 @@ L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # nominal dense tensor-rate ratios to bf16 (2.25 PF): fp8 4.5, fp4 13.5
 DTYPE_RATIO = {"bf16": 1.0, "e4m3": 2.0, "e2m1": 6.0}
+B_DEFAULT_FLAGS = False  # --b-default: time gemm_run without GP_RUN_B_CONSTANT
 
 
 def load_peaks():
@@ -231,11 +232,14 @@ class Problem:
         self.mode = {"int8": "none", "bf16": "none", "e4m3": "rowcol_f32", "e2m1": "block32_ue8m0"}[self.dtype]
         self.flops = 2 * self.M * self.N * self.K
         self.bytes = algorithmic_bytes(self.dtype, self.M, self.N, self.K)
+        # the packed weights are complete (synchronised above) and never
+        # rewritten: every step may pass GP_RUN_B_CONSTANT
+        self.flags = gp.GP_RUN_DEFAULT if B_DEFAULT_FLAGS else gp.GP_RUN_B_CONSTANT
 
     def step(self, i: int, stream=None):
         j = i % self.copies
-        self.gp.gemm_run(self.A[j], self.Bp[j], self.dtype, self.M, self.N, self.K, self.mode,
-                         self.sa, self.sb, self.C[j % len(self.C)], self.c_dtype, stream)
+        self.gp.gemm_run_ex(self.A[j], self.Bp[j], self.dtype, self.M, self.N, self.K, self.mode,
+                            self.sa, self.sb, self.C[j % len(self.C)], self.c_dtype, self.flags, stream)
 
 
 def time_device(prob: Problem, steps: int, warmup: int, pg, device, graph_len: int = 100):
@@ -285,8 +289,8 @@ def time_e2e(prob: Problem, steps: int, warmup: int, device):
         prob.A[j].copy_(ha, non_blocking=True)
         if hsa is not None:
             prob.sa.copy_(hsa, non_blocking=True)
-        prob.gp.gemm_run(prob.A[j], prob.Bp[j], prob.dtype, prob.M, prob.N, prob.K, prob.mode, prob.sa, prob.sb,
-                         prob.C[0], prob.c_dtype)
+        prob.gp.gemm_run_ex(prob.A[j], prob.Bp[j], prob.dtype, prob.M, prob.N, prob.K, prob.mode, prob.sa,
+                            prob.sb, prob.C[0], prob.c_dtype, prob.flags)
         hc.copy_(prob.C[0], non_blocking=True)
     for i in range(max(3, warmup)):
         one(i)
@@ -398,7 +402,8 @@ def run_ours(args):
                    "parallelism": f"replicas x{world}",
                    "l2": f"inputs larger than L2: {prob.copies} rotating packed-B/A copies "
                          f"({prob.copies * prob.packed_bytes / 1e6:.0f} MB)",
-                   "timing": "CUDA-graph replay of back-to-back gemm_run launches, CUDA events"},
+                   "timing": "CUDA-graph replay of back-to-back gemm_run_ex launches, CUDA events",
+                   "flags": "GP_RUN_DEFAULT" if B_DEFAULT_FLAGS else "GP_RUN_B_CONSTANT (weights packed once)"},
         "gpu_launches": args.steps,
         "e2e": {"value": None if args.no_e2e else round(world * prob.flops * e2e_steps / e2e_sec / 1e12, 3),
                 "unit": "TFLOP/s",
@@ -496,7 +501,11 @@ def main():
     ap.add_argument("--no-others", action="store_true", help="skip the other workloads' lines")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffers) leg")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline leg")
+    ap.add_argument("--b-default", action="store_true",
+                    help="call without GP_RUN_B_CONSTANT (B requested only after the previous kernel)")
     args = ap.parse_args()
+    global B_DEFAULT_FLAGS
+    B_DEFAULT_FLAGS = args.b_default
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

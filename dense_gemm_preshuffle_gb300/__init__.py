@@ -30,6 +30,8 @@ _HEADER = os.path.join(os.path.dirname(_HERE), "include", "gemm_preshuffle.h")
 GP_OK = 0
 DTYPES = {"bf16": 0, "e4m3": 1, "int8": 2, "e2m1": 3, "int32": 4}
 SCALE_MODES = {"none": 0, "rowcol_f32": 1, "block32_ue8m0": 2}
+GP_RUN_DEFAULT = 0
+GP_RUN_B_CONSTANT = 1
 
 _lib = None
 
@@ -59,11 +61,12 @@ def load_library():
     lib.gemm_preshuffle_b.argtypes = [vp, vp, i32, i64, i64, vp, vp]
     lib.gemm_unpack_b.argtypes = [vp, i32, i64, i64, vp, vp, vp]
     lib.gemm_run.argtypes = [vp, vp, i32, i64, i64, i64, i32, vp, vp, vp, i32, vp]
+    lib.gemm_run_ex.argtypes = [vp, vp, i32, i64, i64, i64, i32, vp, vp, vp, i32, ctypes.c_uint, vp]
     lib.gemm_last_device_status.argtypes = [vp]
     lib.gemm_status_string.argtypes = [i32]
     lib.gemm_status_string.restype = ctypes.c_char_p
     lib.gemm_debug_skip_load.argtypes = [i32]
-    for name in ("gemm_packed_b_bytes", "gemm_preshuffle_b", "gemm_unpack_b", "gemm_run",
+    for name in ("gemm_packed_b_bytes", "gemm_preshuffle_b", "gemm_unpack_b", "gemm_run", "gemm_run_ex",
                  "gemm_last_device_status", "gemm_debug_skip_load"):
         getattr(lib, name).restype = i32
     _lib = lib
@@ -136,6 +139,13 @@ def gemm_run(A, B_packed, dtype, M: int, N: int, K: int, scale_mode, scale_a, sc
                                    _ptr(scale_b), _ptr(C), _dt(c_dtype), _stream(stream)), "gemm_run")
 
 
+def gemm_run_ex(A, B_packed, dtype, M: int, N: int, K: int, scale_mode, scale_a, scale_b, C, c_dtype,
+                flags: int = GP_RUN_DEFAULT, stream=None) -> None:
+    _check(load_library().gemm_run_ex(_ptr(A), _ptr(B_packed), _dt(dtype), M, N, K, _sm(scale_mode),
+                                      _ptr(scale_a), _ptr(scale_b), _ptr(C), _dt(c_dtype), int(flags),
+                                      _stream(stream)), "gemm_run_ex")
+
+
 def gemm_last_device_status(stream=None) -> int:
     return int(load_library().gemm_last_device_status(_stream(stream)))
 
@@ -156,8 +166,12 @@ def preshuffle_b(B, dtype, B_scales=None, stream=None):
     return out
 
 
-def matmul(A, B_packed, dtype, N: int, K: int, scale_a=None, scale_b=None, out=None, stream=None):
-    """C = A . B^T with B packed; returns bf16 [M, N] (int32 for int8)."""
+def matmul(A, B_packed, dtype, N: int, K: int, scale_a=None, scale_b=None, out=None, stream=None,
+           b_constant: bool = False):
+    """C = A . B^T with B packed; returns bf16 [M, N] (int32 for int8).
+
+    b_constant=True passes GP_RUN_B_CONSTANT: B_packed must not be written
+    by any GPU work still in flight (pack once, then synchronise)."""
     import torch
     d = _dt(dtype)
     M = A.shape[0]
@@ -171,5 +185,6 @@ def matmul(A, B_packed, dtype, N: int, K: int, scale_a=None, scale_b=None, out=N
         c_dtype, mode, tdt = "bf16", "none", torch.bfloat16
     if out is None:
         out = torch.empty((M, N), dtype=tdt, device=A.device)
-    gemm_run(A, B_packed, d, M, N, K, mode, scale_a, scale_b, out, c_dtype, stream)
+    gemm_run_ex(A, B_packed, d, M, N, K, mode, scale_a, scale_b, out, c_dtype,
+                GP_RUN_B_CONSTANT if b_constant else GP_RUN_DEFAULT, stream)
     return out

@@ -180,6 +180,13 @@ int gemm_unpack_b(const void* B_packed, int dtype, int64_t N, int64_t K, void* B
 
 int gemm_run(const void* A, const void* B_packed, int dtype, int64_t M, int64_t N, int64_t K, int scale_mode,
              const void* scale_a, const void* scale_b, void* C, int c_dtype, void* stream) {
+  return gemm_run_ex(A, B_packed, dtype, M, N, K, scale_mode, scale_a, scale_b, C, c_dtype, GP_RUN_DEFAULT, stream);
+}
+
+int gemm_run_ex(const void* A, const void* B_packed, int dtype, int64_t M, int64_t N, int64_t K, int scale_mode,
+                const void* scale_a, const void* scale_b, void* C, int c_dtype, unsigned flags, void* stream) {
+  if ((flags & ~(unsigned)GP_RUN_B_CONSTANT) != 0) return GP_ERR_INVALID_ARG;
+  const int b_constant = (flags & GP_RUN_B_CONSTANT) ? 1 : 0;
   // ---- combination
   const bool combo_ok = (dtype == GP_BF16 && scale_mode == GP_SCALE_NONE && c_dtype == GP_BF16) ||
                         (dtype == GP_E4M3 && scale_mode == GP_SCALE_ROWCOL_F32 && c_dtype == GP_BF16) ||
@@ -226,6 +233,7 @@ int gemm_run(const void* A, const void* B_packed, int dtype, int64_t M, int64_t 
     p.K = (int)K;
     p.ktiles = (int)(kb / 128);
     p.strip = i8_strip_rows((int)N, d->num_sms);
+    p.b_constant = b_constant;
     // A as [K tiles][M rows][128 B] (3-D view, 128-byte swizzle): one copy
     // brings 8 K tiles of 16 rows.
     CUtensorMap tmA, tmB;
@@ -275,6 +283,7 @@ int gemm_run(const void* A, const void* B_packed, int dtype, int64_t M, int64_t 
   p.K = (int)K;
   p.ktiles = (int)(kb / 128);
   p.debug_skip_load = g_debug_skip_load.exchange(0);
+  p.b_constant = b_constant;
   if (scale_mode == GP_SCALE_ROWCOL_F32) {
     p.sa = static_cast<const float*>(scale_a);
     p.sb = static_cast<const float*>(scale_b);

@@ -9,7 +9,8 @@
 //     rows of B (a multiple of 16, chosen so the strips roughly fill the
 //     SMs) and all of K, for one group of 16 rows of A.  No split-K, so no
 //     cross-CTA reduction.
-//   - A producer warp (one lane) streams, per 128-byte K tile:
+//   - Two producer warps (one lane each: one for B, one for A) stream, per
+//     128-byte K tile:
 //       * the 16 x 128-byte A tile (2-D TMA, 128-byte swizzle, rows >= M
 //         zero-filled);
 //       * the strip's packed-B rows, as one or two contiguous bulk copies
@@ -43,8 +44,10 @@
 
 namespace gp {
 
-constexpr int I8_CW = 8;                       // consumer warps; warp I8_CW is the producer
-constexpr int I8_THREADS = 32 * (I8_CW + 1);
+constexpr int I8_CW = 8;                       // consumer warps 0..7
+constexpr int I8_B_WARP = I8_CW;               // issues the B copies
+constexpr int I8_A_WARP = I8_CW + 1;           // issues the A copies
+constexpr int I8_THREADS = 32 * (I8_CW + 2);
 constexpr int I8_KT_PER_STAGE = I8_CW;          // one K tile per consumer warp per stage
 constexpr int I8_STAGES = 2;
 // Two CTAs fit on one SM (registers <= 128/thread, shared memory <= 113 KiB),
@@ -105,7 +108,7 @@ __global__ void __launch_bounds__(I8_THREADS, i8_ctas_per_sm(NB8))
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < I8_STAGES; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], 2);  // the B and the A issuer
       mbar_init(&empty[s], I8_CW);
     }
     *abort_flag = 0;
@@ -113,7 +116,7 @@ __global__ void __launch_bounds__(I8_THREADS, i8_ctas_per_sm(NB8))
     prefetch_tensormap(&tmA);
     prefetch_tensormap(&tmB);
   }
-  if (threadIdx.x == I8_CW * 32) {
+  if (threadIdx.x == I8_B_WARP * 32) {
     // Warm L2 with this CTA's whole weight strip while the previous kernel
     // on the stream may still run: a prefetch is only a cache hint.
     for (int q = 0; q < nstages; ++q)
@@ -127,47 +130,71 @@ __global__ void __launch_bounds__(I8_THREADS, i8_ctas_per_sm(NB8))
   }
   pdl_launch_dependents();
   __syncthreads();
+
+  // A: 8 K tiles x 16 rows x 128 B (rows >= M and K tiles >= ktiles read as zeros)
+  auto load_a = [&](int q) {
+    const int s = q % I8_STAGES;
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::
+            "r"(smem_u32(base + s * STAGE)),
+        "l"(reinterpret_cast<uint64_t>(&tmA)), "r"(0), "r"(mg * 16), "r"(q * I8_KT_PER_STAGE), "r"(smem_u32(&full[s]))
+        : "memory");
+  };
+  // B: BOXR-row pieces of the strip, 8 K tiles each (a piece never crosses
+  // a 128-row band of the packed layout)
+  auto load_b = [&](int q) {
+    const int s = q % I8_STAGES;
+#pragma unroll
+    for (int j = 0; j < SN / BOXR; ++j)
+      asm volatile(
+          "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];" ::
+              "r"(smem_u32(base + s * STAGE + A_BYTES + j * (I8_KT_PER_STAGE * BOXR * 128))),
+          "l"(reinterpret_cast<uint64_t>(&tmB)), "r"(0), "r"((n0 + BOXR * j) & 127), "r"(q * I8_KT_PER_STAGE),
+          "r"((n0 + BOXR * j) >> 7), "r"(smem_u32(&full[s]))
+          : "memory");
+  };
+  // With constant weights the ring's first stages of B are requested before
+  // the wait on the previous kernel; their A halves follow after it.
+  const int early = p.b_constant ? min(nstages, I8_STAGES) : 0;
+  if (warp == I8_B_WARP && lane == 0) {
+    for (int q = 0; q < early; ++q) {
+      mbar_arrive_expect_tx(&full[q], B_BYTES);
+      load_b(q);
+    }
+  }
   pdl_wait();  // A may be produced, and C read, by the previous kernel
 
-  if (warp == I8_CW) {
-    // ------------------------------------------------------------ producer
+  if (warp >= I8_CW) {
+    // ------------------------------------------------------------ producers
+    // Two issuing warps, one for B and one for A: each thread's bulk copies
+    // complete one after another (about 0.4 us each from L2, whatever their
+    // size), so the two operands of a stage travel in parallel.
     if (lane == 0) {
-      uint32_t issued = 0;
+      const bool is_b = warp == I8_B_WARP;
+      int q = is_b ? early : 0;
       bool ok = true;
-      for (int q = 0; q < nstages; ++q) {
+      for (; q < nstages; ++q) {
         const int s = q % I8_STAGES;
         const uint32_t ph = (uint32_t)(q / I8_STAGES) & 1;
         if (!wait_bounded(&empty[s], ph ^ 1, abort_flag, p.status, ST_TIMEOUT_PRODUCER, limit)) {
           ok = false;
           break;
         }
-        uint8_t* st = base + s * STAGE;
-        mbar_arrive_expect_tx(&full[s], STAGE);
-        // A: 8 K tiles x 16 rows x 128 B (rows >= M and K tiles >= ktiles read as zeros)
-        asm volatile(
-            "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::
-                "r"(smem_u32(st)),
-            "l"(reinterpret_cast<uint64_t>(&tmA)), "r"(0), "r"(mg * 16), "r"(q * I8_KT_PER_STAGE),
-            "r"(smem_u32(&full[s]))
-            : "memory");
-        // B: BOXR-row pieces of the strip, 8 K tiles each (a piece never
-        // crosses a 128-row band of the packed layout)
-#pragma unroll
-        for (int j = 0; j < SN / BOXR; ++j)
-          asm volatile(
-              "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];" ::
-                  "r"(smem_u32(st + A_BYTES + j * (I8_KT_PER_STAGE * BOXR * 128))),
-              "l"(reinterpret_cast<uint64_t>(&tmB)), "r"(0), "r"((n0 + BOXR * j) & 127), "r"(q * I8_KT_PER_STAGE),
-              "r"((n0 + BOXR * j) >> 7), "r"(smem_u32(&full[s]))
-              : "memory");
-        ++issued;
+        if (is_b) {
+          mbar_arrive_expect_tx(&full[s], B_BYTES);
+          load_b(q);
+        } else {
+          mbar_arrive_expect_tx(&full[s], A_BYTES);
+          load_a(q);
+        }
       }
+      const uint32_t issued = (uint32_t)q;
       if (!ok || *abort_flag) {
         const uint32_t n = issued < (uint32_t)I8_STAGES ? issued : (uint32_t)I8_STAGES;
         for (uint32_t i = 0; i < n; ++i) {
-          const uint32_t q = issued - 1 - i;
+          const uint32_t qq = issued - 1 - i;
           volatile int never = 0;
-          wait_bounded(&full[q % I8_STAGES], (q / I8_STAGES) & 1, &never, p.status, ST_TIMEOUT_DRAIN, limit);
+          wait_bounded(&full[qq % I8_STAGES], (qq / I8_STAGES) & 1, &never, p.status, ST_TIMEOUT_DRAIN, limit);
         }
       }
     }

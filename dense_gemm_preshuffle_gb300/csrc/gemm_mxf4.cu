@@ -125,6 +125,28 @@ __global__ void __launch_bounds__(F4_THREADS, 1)
     prefetch_tensormap(&tmC);
   }
   if (warp == 1) tmem_alloc<Cfg::TMEM_COLS>(tmem_slot);
+  const size_t sf_band_bytes = (size_t)p.ktiles * 1024;  // packed B scales of one 128-row band
+  // B data and scales of stage s of this CTA's tile (nb) at K step kt
+  auto load_b = [&](int s, int nb, int kt) {
+#pragma unroll
+    for (int j = 0; j < F4_BN / 128; ++j) {
+      const int band = nb * (F4_BN / 128) + j;
+      bulk_load(s_b + s * Cfg::B_BYTES + j * 16384, p.Bp + ((size_t)band * p.ktiles + kt) * 16384, 16384, &full[s]);
+      bulk_load(s_sfb + s * Cfg::SFB_BYTES + j * 1024, p.Bsf + (size_t)band * sf_band_bytes + (size_t)kt * 1024, 1024,
+                &full[s]);
+    }
+  };
+  // With constant weights the producer requests B (data and scales) for the
+  // first stages of its first tile before the wait on the previous kernel.
+  const int early = (p.b_constant && (int)blockIdx.x < p.num_tiles) ? min(p.ktiles, F4_STAGES) : 0;
+  if (threadIdx.x == 0 && early > 0) {  // the producer thread, which initialised the barriers
+    int mb, nb;
+    f4_tile_coords(blockIdx.x, p.tiles_m, p.tiles_n, mb, nb);
+    for (int kt = 0; kt < early; ++kt) {
+      mbar_arrive_expect_tx(&full[kt], Cfg::STAGE_TX);
+      load_b(kt, nb, kt);
+    }
+  }
   pdl_launch_dependents();
   tc_fence_before();
   __syncthreads();
@@ -139,24 +161,20 @@ __global__ void __launch_bounds__(F4_THREADS, 1)
       uint32_t ph = 0;
       uint32_t issued = 0;
       bool ok = true;
-      const size_t sf_band_bytes = (size_t)p.ktiles * 1024;  // scales of one 128-row band
       for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
         int mb, nb;
         f4_tile_coords(t, p.tiles_m, p.tiles_n, mb, nb);
         for (int kt = 0; kt < p.ktiles; ++kt) {
-          if (!wait_bounded(&empty[s], ph ^ 1, abort_flag, p.status, ST_TIMEOUT_PRODUCER, limit)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(&full[s], Cfg::STAGE_TX);
-          tma_load_2d(s_a + s * Cfg::A_BYTES, &tmA, kt * 128, mb * 128, &full[s]);
-#pragma unroll
-          for (int j = 0; j < F4_BN / 128; ++j) {
-            const int band = nb * (F4_BN / 128) + j;
-            bulk_load(s_b + s * Cfg::B_BYTES + j * 16384, p.Bp + ((size_t)band * p.ktiles + kt) * 16384, 16384,
-                      &full[s]);
-            bulk_load(s_sfb + s * Cfg::SFB_BYTES + j * 1024, p.Bsf + (size_t)band * sf_band_bytes + (size_t)kt * 1024,
-                      1024, &full[s]);
+          if ((int)issued < early) {  // a free stage whose B is already requested
+            tma_load_2d(s_a + s * Cfg::A_BYTES, &tmA, kt * 128, mb * 128, &full[s]);
+          } else {
+            if (!wait_bounded(&empty[s], ph ^ 1, abort_flag, p.status, ST_TIMEOUT_PRODUCER, limit)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&full[s], Cfg::STAGE_TX);
+            tma_load_2d(s_a + s * Cfg::A_BYTES, &tmA, kt * 128, mb * 128, &full[s]);
+            load_b(s, nb, kt);
           }
           ++issued;
           if (++s == F4_STAGES) {

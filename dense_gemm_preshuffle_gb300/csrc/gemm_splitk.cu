@@ -158,6 +158,17 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
         prefetch_l2_bulk(p.Bp + ((size_t)(nb * (SK_BN / 128) + j) * p.ktiles + kt) * 16384, 16384);
     }
   }
+  // With constant weights the producer requests B for the first stages
+  // before the wait on the previous kernel; A follows after.
+  const int early = p.b_constant ? min(ks, SK_STAGES) : 0;
+  if (threadIdx.x == 0) {  // the producer thread, which initialised the barriers
+    for (int i = 0; i < early; ++i) {
+      mbar_arrive_expect_tx(&full[i], SK_STAGE_BYTES);
+      for (int j = 0; j < SK_BN / 128; ++j)
+        bulk_load(s_b + i * SK_B_BYTES + j * 16384,
+                  p.Bp + ((size_t)(nb * (SK_BN / 128) + j) * p.ktiles + k0 + i) * 16384, 16384, &full[i]);
+    }
+  }
   pdl_launch_dependents();
   tc_fence_before();
   cluster_sync_all();  // every peer's barriers are initialised before any remote arrive
@@ -175,6 +186,11 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
         const int s = i % SK_STAGES;
         const uint32_t ph = (uint32_t)(i / SK_STAGES) & 1;
         const int kt = k0 + i;
+        if (i < early) {  // a free stage whose B is already requested
+          tma_load_2d(s_a + s * SK_A_BYTES, &tmA, kt * 128, mb * SK_BM, &full[s]);
+          ++issued;
+          continue;
+        }
         if (!wait_bounded(&empty[s], ph ^ 1, abort_flag, p.status, ST_TIMEOUT_PRODUCER, limit)) {
           ok = false;
           break;

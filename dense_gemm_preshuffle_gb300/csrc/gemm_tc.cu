@@ -122,6 +122,22 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         prefetch_l2_bulk(p.Bp + ((size_t)(nb * (BN / 128) + j) * p.ktiles + kt) * 16384, 16384);
     }
   }
+  // With constant weights the producer requests B for the first stages of
+  // its first tile before the wait on the previous kernel; A follows after.
+  const int early = (p.b_constant && (int)blockIdx.x < p.num_tiles) ? min(p.ktiles, STAGES) : 0;
+  if (threadIdx.x == 0 && early > 0) {  // the producer thread, which initialised the barriers
+    int mb, nb;
+    tile_coords(blockIdx.x, p.tiles_m, p.tiles_n, mb, nb);
+    const uint8_t* bsrc = p.Bp + (size_t)nb * (BN / 128) * p.ktiles * 16384;
+    const uint64_t pol_b = policy_evict_first();
+    for (int kt = 0; kt < early; ++kt) {
+      if (p.debug_skip_load == 1 + kt) continue;
+      mbar_arrive_expect_tx(&full[kt], Cfg::STAGE_BYTES);
+      for (int j = 0; j < BN / 128; ++j)
+        bulk_load_hint(s_b + kt * Cfg::B_BYTES + j * 16384, bsrc + ((size_t)j * p.ktiles + kt) * 16384, 16384,
+                       &full[kt], pol_b);
+    }
+  }
   pdl_launch_dependents();
   tc_fence_before();
   __syncthreads();
@@ -142,13 +158,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         tile_coords(t, p.tiles_m, p.tiles_n, mb, nb);
         const uint8_t* bsrc = p.Bp + (size_t)nb * (BN / 128) * p.ktiles * 16384;
         for (int kt = 0; kt < p.ktiles; ++kt) {
-          if (!wait_bounded(&empty[s], ph ^ 1, abort_flag, p.status, ST_TIMEOUT_PRODUCER, limit)) {
+          // the first `early` stages are free and already hold their B request
+          if ((int)issued >= early &&
+              !wait_bounded(&empty[s], ph ^ 1, abort_flag, p.status, ST_TIMEOUT_PRODUCER, limit)) {
             ok = false;
             break;
           }
           if (p.debug_skip_load == 1 + (int)issued) {
             // Fault injection (host-selected): leave this stage's barrier
             // without its arrival, so the consumer's bounded wait times out.
+          } else if ((int)issued < early) {
+            tma_load_2d(s_a + s * Cfg::A_BYTES, &tmA, kt * 128, mb * BM, &full[s]);
           } else {
             mbar_arrive_expect_tx(&full[s], Cfg::STAGE_BYTES);
             tma_load_2d(s_a + s * Cfg::A_BYTES, &tmA, kt * 128, mb * BM, &full[s]);

@@ -20,6 +20,7 @@ struct TcParams {
   int ktiles;             // row bytes / 128
   int tiles_m, tiles_n, num_tiles;
   int debug_skip_load;    // 0 = off; i > 0: the producer skips its i-th stage load
+  int b_constant;         // 1: B may be read before the previous kernel on the stream completes
 };
 
 struct I8Params {
@@ -31,6 +32,7 @@ struct I8Params {
   int ktiles;             // K / 128
   int strip;              // rows of B per CTA (multiple of 16)
   int stages;
+  int b_constant;         // 1: B may be read before the previous kernel on the stream completes
 };
 
 int tc_tile_m(int64_t M, int64_t N, int num_sms);

@@ -142,6 +142,30 @@ int gemm_run(const void* A, const void* B_packed, int dtype, int64_t M, int64_t 
              int scale_mode, const void* scale_a, const void* scale_b, void* C, int c_dtype,
              void* stream);
 
+/* Flags of gemm_run_ex. */
+typedef enum gp_run_flags {
+  GP_RUN_DEFAULT = 0,
+  /* B_packed holds constant weights: nothing that may still be running on
+   * the GPU when the call is made writes it (pack the weights once and
+   * synchronise, as at model load).  The kernel may then start copying B
+   * into shared memory before the kernel that precedes it on `stream` has
+   * finished, which hides its pipeline start behind that kernel's tail.  A,
+   * the scales and C are still touched only after the preceding kernel
+   * completes.  Breaking the condition gives undefined results. */
+  GP_RUN_B_CONSTANT = 1
+} gp_run_flags;
+
+/*
+ * gemm_run with flags (a bitwise OR of gp_run_flags); gemm_run is
+ * gemm_run_ex with GP_RUN_DEFAULT.  Unknown flag bits return
+ * GP_ERR_INVALID_ARG before any launch.  This is a scheduling option of
+ * this library: the method itself only assumes that the packed weights are
+ * produced once, offline ("GEMM Optimization Guide" section 12).
+ */
+int gemm_run_ex(const void* A, const void* B_packed, int dtype, int64_t M, int64_t N, int64_t K,
+                int scale_mode, const void* scale_a, const void* scale_b, void* C, int c_dtype,
+                unsigned flags, void* stream);
+
 /*
  * Synchronises `stream`, then reads and clears the library's device status
  * word on the current device.  The word is set when a bounded wait in a GEMM

@@ -17,7 +17,7 @@ def lib():
 
 def test_exports_every_declared_symbol(lib):
     names = gp.header_functions()
-    assert set(names) >= {"gemm_packed_b_bytes", "gemm_preshuffle_b", "gemm_unpack_b", "gemm_run",
+    assert set(names) >= {"gemm_packed_b_bytes", "gemm_preshuffle_b", "gemm_unpack_b", "gemm_run", "gemm_run_ex",
                           "gemm_last_device_status", "gemm_status_string", "gemm_debug_skip_load"}
     for n in names:
         assert hasattr(lib, n), n
@@ -88,3 +88,12 @@ def test_empty_problem_is_a_noop(lib):
     # M == 0: nothing to compute, nothing touched, no CUDA call needed
     assert lib.gemm_run(None, None, gp.DTYPES["e4m3"], 0, 256, 512, 0, None, None, None, gp.DTYPES["bf16"], None) == 0
     assert lib.gemm_preshuffle_b(None, None, gp.DTYPES["int8"], 0, 128, None, None) == 0
+
+
+def test_run_ex_rejects_unknown_flags(lib):
+    rc = lib.gemm_run_ex(FAKE, FAKE, gp.DTYPES["e4m3"], 16, 256, 512, 0, None, None, FAKE, gp.DTYPES["bf16"], 2, None)
+    assert rc == 1
+    # the known flag passes validation; a shape error is still reported first-class
+    rc = lib.gemm_run_ex(FAKE, FAKE, gp.DTYPES["e4m3"], 16, 100, 512, 0, None, None, FAKE, gp.DTYPES["bf16"],
+                         gp.GP_RUN_B_CONSTANT, None)
+    assert rc == 3

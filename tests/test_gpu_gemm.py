@@ -244,3 +244,60 @@ def test_repeatable_bitwise():
     f8 = gp.matmul(A8, Bp8, "int8", ops8.N, ops8.K)
     for _ in range(20):
         assert torch.equal(gp.matmul(A8, Bp8, "int8", ops8.N, ops8.K), f8)
+
+
+# ---------------------------------------------------------------- constant-weight scheduling flag
+
+@pytest.mark.parametrize("dtype,M,N,K", [
+    ("int8", 16, 7168, 4096), ("int8", 37, 256, 384), ("int8", 16, 384, 128),
+    ("e4m3", 300, 512, 1024), ("e4m3", 17, 384, 256), ("bf16", 257, 384, 512),
+    ("e2m1", 200, 512, 512), ("e2m1", 129, 256, 256),
+    ("bf16", 400, 4096, 8192),   # split-K cluster path
+    ("e4m3", 4173, 9728, 256),   # 256-row tile path
+], ids=lambda v: str(v))
+def test_b_constant_flag_matches_oracle_and_default(dtype, M, N, K):
+    """GP_RUN_B_CONSTANT only moves the first B requests before the wait on
+    the previous kernel: the result is bit-identical to the default call."""
+    ops = inputs.make_operands(dtype, M, N, K, seed=4000 + M + N + K)
+    A, B, sa, sb = dev(ops)
+    if dtype == "e2m1":
+        Bp = gp.preshuffle_b(B, "e2m1", B_scales=sb)
+        sa_, sb_ = sa, None
+    else:
+        Bp = gp.preshuffle_b(B, dtype)
+        sa_, sb_ = sa, sb
+    torch.cuda.synchronize()   # the weights are complete before any flagged call
+    ref = gp.matmul(A, Bp, dtype, N, K, scale_a=sa_, scale_b=sb_)
+    for _ in range(3):
+        C = gp.matmul(A, Bp, dtype, N, K, scale_a=sa_, scale_b=sb_, b_constant=True)
+    torch.cuda.synchronize()
+    assert gp.gemm_last_device_status() == 0
+    if C.dtype == torch.int32:
+        assert torch.equal(C, ref)
+    else:
+        assert torch.equal(C.view(torch.int16), ref.view(torch.int16))
+    rows = None if M * N <= 1 << 21 else sample_rows(M, 24, seed=5)
+    check(ops, C, rows=rows)
+
+
+@pytest.mark.parametrize("M,N1,K1,N2", [(2048, 2048, 4096, 384), (400, 8192, 2048, 4096)])
+def test_b_constant_reads_a_only_after_previous_kernel(M, N1, K1, N2):
+    """Chain C2 = (A.B1^T).B2^T with the second call flagged: its A is the
+    first call's output, so an early read of A would see the fill value."""
+    ops1 = inputs.make_operands("bf16", M, N1, K1, seed=77)
+    ops2 = inputs.make_operands("bf16", M, N2, N1, seed=78)
+    A1, B1, _, _ = dev(ops1)
+    _, B2, _, _ = dev(ops2)
+    Bp1 = gp.preshuffle_b(B1, "bf16")
+    Bp2 = gp.preshuffle_b(B2, "bf16")
+    torch.cuda.synchronize()
+    for trial in range(3):
+        C1 = torch.full((M, N1), float("nan"), dtype=torch.bfloat16, device="cuda")
+        gp.matmul(A1, Bp1, "bf16", N1, K1, out=C1)
+        C2 = gp.matmul(C1, Bp2, "bf16", N2, N1, b_constant=True)
+        torch.cuda.synchronize()
+        assert torch.isfinite(C2.float()).all()
+        again = gp.matmul(C1, Bp2, "bf16", N2, N1)  # C1 complete: the plain call
+        torch.cuda.synchronize()
+        assert torch.equal(C2.view(torch.int16), again.view(torch.int16))
+    check(ops1, C1, rows=sample_rows(M, 16, seed=6))
