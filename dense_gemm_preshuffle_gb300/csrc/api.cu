@@ -15,6 +15,7 @@
 #include <mutex>
 
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace gp {
 
@@ -132,6 +133,7 @@ const char* gemm_status_string(int status) {
     case GP_ERR_ALIGNMENT: return "GP_ERR_ALIGNMENT: pointer not 16-byte aligned";
     case GP_ERR_CUDA: return "GP_ERR_CUDA: a CUDA call failed";
     case GP_ERR_DEVICE_TIMEOUT: return "GP_ERR_DEVICE_TIMEOUT: a bounded wait inside a kernel gave up";
+    case GP_ERR_DEVICE_CHECK: return "GP_ERR_DEVICE_CHECK: a kernel's launch self-check failed; it computed nothing";
     default: return "unknown gp_status";
   }
 }
@@ -159,7 +161,7 @@ int gemm_preshuffle_b(const void* B, const void* B_scales, int dtype, int64_t N,
   DeviceInfo* d = nullptr;
   if ((rc = device_info(&d)) != GP_OK) return rc;
   return pack_b_launch(static_cast<const uint8_t*>(B), static_cast<const uint8_t*>(B_scales), N, kb, K / 32,
-                       static_cast<uint8_t*>(B_packed), static_cast<cudaStream_t>(stream));
+                       dtype == GP_INT8, static_cast<uint8_t*>(B_packed), static_cast<cudaStream_t>(stream));
 }
 
 int gemm_unpack_b(const void* B_packed, int dtype, int64_t N, int64_t K, void* B_out, void* B_scales_out,
@@ -173,7 +175,8 @@ int gemm_unpack_b(const void* B_packed, int dtype, int64_t N, int64_t K, void* B
   if (!aligned16(B_out) || !aligned16(B_packed)) return GP_ERR_ALIGNMENT;
   DeviceInfo* d = nullptr;
   if ((rc = device_info(&d)) != GP_OK) return rc;
-  return unpack_b_launch(static_cast<const uint8_t*>(B_packed), N, kb, K / 32, static_cast<uint8_t*>(B_out),
+  return unpack_b_launch(static_cast<const uint8_t*>(B_packed), N, kb, K / 32, dtype == GP_INT8,
+                         static_cast<uint8_t*>(B_out),
                          dtype == GP_E2M1 ? static_cast<uint8_t*>(B_scales_out) : nullptr,
                          static_cast<cudaStream_t>(stream));
 }
@@ -247,12 +250,12 @@ int gemm_run_ex(const void* A, const void* B_packed, int dtype, int64_t M, int64
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return GP_ERR_CUDA;
     }
-    // packed B as [bands][K tiles][128 rows][128 B] (4-D view, already
-    // swizzled): one copy brings 8 K tiles of a strip of rows.
+    // packed B as [8-row bands][K tiles][8 rows][128 B] (4-D view, already
+    // swizzled): one copy brings 8 K tiles of a CTA's whole strip of bands.
     {
-      cuuint64_t dims[4] = {128, 128, (cuuint64_t)p.ktiles, (cuuint64_t)(N / 128)};
-      cuuint64_t strides[3] = {128, 16384, (cuuint64_t)p.ktiles * 16384};
-      cuuint32_t box[4] = {128, (cuuint32_t)i8_box_rows_for(p.strip), 8, 1};
+      cuuint64_t dims[4] = {128, 8, (cuuint64_t)p.ktiles, (cuuint64_t)(N / 8)};
+      cuuint64_t strides[3] = {128, 1024, (cuuint64_t)p.ktiles * 1024};
+      cuuint32_t box[4] = {128, 8, 8, (cuuint32_t)(p.strip / 8)};
       cuuint32_t estr[4] = {1, 1, 1, 1};
       if (g_encode(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(B_packed), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -310,7 +313,7 @@ int gemm_last_device_status(void* stream) {
   if (word != 0) {
     const uint32_t zero = 0;
     if (cudaMemcpy(d->status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return GP_ERR_CUDA;
-    return GP_ERR_DEVICE_TIMEOUT;
+    return (word & ST_BAD_LAUNCH) ? GP_ERR_DEVICE_CHECK : GP_ERR_DEVICE_TIMEOUT;
   }
   return GP_OK;
 }

@@ -6,30 +6,38 @@
 // matrix B must stream from HBM once at full bandwidth:
 //
 //   - The grid is one wave.  Each CTA owns a strip of `strip` consecutive
-//     rows of B (a multiple of 16, chosen so the strips roughly fill the
-//     SMs) and all of K, for one group of 16 rows of A.  No split-K, so no
-//     cross-CTA reduction.
-//   - Two producer warps (one lane each: one for B, one for A) stream, per
-//     128-byte K tile:
-//       * the 16 x 128-byte A tile (2-D TMA, 128-byte swizzle, rows >= M
-//         zero-filled);
-//       * the strip's packed-B rows, as one or two contiguous bulk copies
-//         (the packed layout keeps each 128-row band's K tile contiguous).
-//     These go into a deep ring of stages (up to 192 KiB in flight per SM),
-//     with full/empty mbarriers.
-//   - Eight consumer warps take K tiles round-robin.  sm_103a has no
-//     tcgen05 integer MMA and its int8 tensor and dp4a rates (~150 TOPS
-//     measured) cannot keep pace with the weight stream, so the consumers
-//     use the 16-bit MMA:
-//       * int8 values are exact in fp16;
-//       * products are exact;
-//       * a 128-element K tile sums to at most 128 * 128 * 128 = 2^21 in
-//         magnitude, so its fp32 accumulation is exact;
-//       * each K tile's fp32 partials are converted to int32 and added in
-//         int32.
-//     The result is the exact integer product.  The int8 -> fp16
-//     conversion is 5 integer/half ops per 4 values (xor, 2 byte permutes,
-//     2 packed subtracts of the 1024+128 bias).
+//     rows of B (a multiple of 16, chosen so that two strips share an SM
+//     where N allows) and all of K, for one group of 16 rows of A.  No
+//     split-K, so no cross-CTA reduction.  The INT8 packed layout stores
+//     8-row bands, so a strip's rows for 8 K tiles are one 4-D TMA box.
+//   - A CTA takes under half of an SM, so with programmatic dependent
+//     launch the next GEMM's CTAs start beside this one's on the SMs that
+//     hold a single strip: they warm L2 with their weights and, for constant
+//     weights (GP_RUN_B_CONSTANT), fill their ring with B before the wait on
+//     this kernel.
+//   - One producer warp: lane 0 issues the B copies and lane 1 the A copies
+//     (each thread's bulk copies complete one after another, so the two
+//     operands travel in parallel).  Stages of 8 K tiles (up to 48 KiB) go
+//     into a ring of 2, with full/empty mbarriers.
+//   - Eight consumer warps; warp w computes K tile w of every stage.  sm_103a
+//     has no tcgen05 integer MMA and its int8 tensor and dp4a rates (~150
+//     TOPS measured) cannot keep pace with the weight stream, so the
+//     consumers use the 16-bit MMA on exact fp16 images of the integers:
+//       * A (row-major int8 from the caller): a -> fp16 a, 5 integer/half
+//         ops per 4 values (xor, 2 byte permutes into the 0x64XX binade,
+//         2 packed subtracts of 1024 + 128);
+//       * B (packed offline in offset binary, byte u = b + 128): u -> the
+//         fp16 subnormal u * 2^-24, 2 byte permutes per 4 values and no
+//         arithmetic;
+//       * products a * u * 2^-24 are exact, and a 128-element K tile sums
+//         to |sum a*u| <= 128 * 128 * 255 < 2^22 units of 2^-24, so its
+//         fp32 accumulation is exact;
+//       * each K tile's partials are scaled back to integers with one FMA
+//         (x * 2^24 + 1.5 * 2^23 is exact and holds x in its low bits) and
+//         added in int32;
+//       * sum a*b = sum a*u - 128 * sum a, with the row sums of A taken by
+//         dp4a from the same A words.
+//     The result is the exact integer product.
 //   - K is permuted identically for A and B inside each 64-element group,
 //     which leaves the sum unchanged.  Lane t reads bytes
 //     [32t, 32t+32) of a row.  Those bytes sit in 16-byte slots
@@ -44,16 +52,28 @@
 
 namespace gp {
 
-constexpr int I8_CW = 8;                       // consumer warps 0..7
-constexpr int I8_B_WARP = I8_CW;               // issues the B copies
-constexpr int I8_A_WARP = I8_CW + 1;           // issues the A copies
-constexpr int I8_THREADS = 32 * (I8_CW + 2);
-constexpr int I8_KT_PER_STAGE = I8_CW;          // one K tile per consumer warp per stage
+constexpr int I8_CW = 8;                 // consumer warps 0..7
+constexpr int I8_PRODUCER = I8_CW;       // warp 8: lane 0 issues B, lane 1 issues A
+constexpr int I8_THREADS = 32 * (I8_CW + 1);
+constexpr int I8_KT = I8_CW;             // K tiles per stage: one per consumer warp
 constexpr int I8_STAGES = 2;
-// Two CTAs fit on one SM (registers <= 128/thread, shared memory <= 113 KiB),
-// so with programmatic dependent launch the next GEMM's CTAs sit beside this
-// one's and warm L2 with their weights while this one computes.
+// Two CTAs share an SM for strips of up to 32 rows (three for 16 rows).
 constexpr int I8_CTAS_PER_SM = 2;
+__host__ __device__ constexpr int i8_ctas_per_sm(int nb8) { return nb8 <= 2 ? 3 : (nb8 <= 4 ? 2 : 1); }
+
+// Offset-binary bytes u -> fp16 subnormals u * 2^-24 (bit pattern 0x00uu):
+// lo holds bytes 0 and 1, hi bytes 2 and 3.
+__device__ __forceinline__ void u8x4_to_f16x2_sub(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(lo) : "r"(w), "r"(0u));
+  asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(hi) : "r"(w), "r"(0u));
+}
+
+// x = f * 2^24 is an integer with |x| < 2^22: x + 1.5 * 2^23 lies in
+// [2^23, 2^24), where the fp32 ulp is 1, so the FMA is exact and the low
+// bits of the result are x + 0x400000.
+__device__ __forceinline__ int scaled_to_int(float f) {
+  return (int)(__float_as_uint(__fmaf_rn(f, 16777216.0f, 12582912.0f)) - 0x4B400000u);
+}
 
 __device__ __forceinline__ void i8x4_to_f16x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
   const uint32_t u = w ^ 0x80808080u;  // each byte b -> b + 128 in [0, 255]
@@ -75,22 +95,13 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Rows per B copy: the whole strip when it divides the 128-row band of the
-// packed layout (one copy per stage; each TMA copy costs a CTA ~170 ns
-// however large it is), else 16-row pieces, which never cross a band.
-__host__ __device__ constexpr int i8_box_rows(int sn) { return (128 % sn == 0) ? sn : 16; }
-
-// CTAs that fit on one SM for a strip of NB8 * 8 rows (shared memory and
-// registers): 3 for 16-row strips, 2 up to 32 rows, else 1.
-__host__ __device__ constexpr int i8_ctas_per_sm(int nb8) { return nb8 <= 2 ? 3 : (nb8 <= 4 ? 2 : 1); }
-
+// NB8: eight-row units per strip.
 template <int NB8>
 __global__ void __launch_bounds__(I8_THREADS, i8_ctas_per_sm(NB8))
     i8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, I8Params p) {
-  constexpr int SN = NB8 * 8;                    // rows of B per CTA (a multiple of 16)
-  constexpr int BOXR = i8_box_rows(SN);          // rows per B copy
-  constexpr int A_BYTES = I8_KT_PER_STAGE * 16 * 128;
-  constexpr int B_BYTES = I8_KT_PER_STAGE * SN * 128;
+  constexpr int SN = NB8 * 8;                    // rows of B per CTA
+  constexpr int A_BYTES = I8_KT * 16 * 128;      // [kt][16 rows][128 B], 128-byte swizzle
+  constexpr int B_BYTES = I8_KT * SN * 128;      // [unit][kt][8 rows][128 B], packed swizzle
   constexpr int STAGE = A_BYTES + B_BYTES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -100,11 +111,24 @@ __global__ void __launch_bounds__(I8_THREADS, i8_ctas_per_sm(NB8))
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int n0 = blockIdx.x * SN;
-  const int rows = min(SN, p.N - n0);  // valid rows of this strip (a multiple of 16)
+  const int units = p.N >> 3;
+  const int u0 = blockIdx.x * NB8;
+  const int nu = min(NB8, units - u0);  // units of this strip that exist (the last strip may be short)
   const int mg = blockIdx.y;
-  const int nstages = (p.ktiles + I8_KT_PER_STAGE - 1) / I8_KT_PER_STAGE;
+  const int nstages = (p.ktiles + I8_KT - 1) / I8_KT;
   const uint64_t limit = p.wait_limit_ns;
+  {
+    // Launch self-check (uniform over the CTA, before any copy): the strip
+    // exists, the rows of A exist, and the ring fits the dynamic shared
+    // memory.  A mismatch is recorded and the CTA returns.
+    uint32_t dyn;
+    asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
+    const uint32_t need = (uint32_t)(reinterpret_cast<const volatile uint8_t*>(abort_flag + 1) - smem_raw);
+    if (nu < 1 || mg * 16 >= p.M || p.ktiles < 1 || need > dyn || (int)blockDim.x != I8_THREADS) {
+      if (threadIdx.x == 0) atomicOr(p.status, ST_BAD_LAUNCH);
+      return;
+    }
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < I8_STAGES; ++s) {
@@ -116,61 +140,56 @@ __global__ void __launch_bounds__(I8_THREADS, i8_ctas_per_sm(NB8))
     prefetch_tensormap(&tmA);
     prefetch_tensormap(&tmB);
   }
-  if (threadIdx.x == I8_B_WARP * 32) {
-    // Warm L2 with this CTA's whole weight strip while the previous kernel
-    // on the stream may still run: a prefetch is only a cache hint.
-    for (int q = 0; q < nstages; ++q)
-#pragma unroll
-      for (int j = 0; j < SN / BOXR; ++j)
-        if (BOXR * j < rows)
-        asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
-                         reinterpret_cast<uint64_t>(&tmB)),
-                     "r"(0), "r"((n0 + BOXR * j) & 127), "r"(q * I8_KT_PER_STAGE), "r"((n0 + BOXR * j) >> 7)
-                     : "memory");
-  }
-  pdl_launch_dependents();
-  __syncthreads();
-
-  // A: 8 K tiles x 16 rows x 128 B (rows >= M and K tiles >= ktiles read as zeros)
+  // B: NB8 units x I8_KT K tiles of 8 rows; units past N read as zeros
+  auto load_b = [&](int q) {
+    const int s = q % I8_STAGES;
+    mbar_arrive_expect_tx(&full[s], B_BYTES);
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];" ::
+            "r"(smem_u32(base + s * STAGE + A_BYTES)),
+        "l"(reinterpret_cast<uint64_t>(&tmB)), "r"(0), "r"(0), "r"(q * I8_KT), "r"(u0), "r"(smem_u32(&full[s]))
+        : "memory");
+  };
+  // A: I8_KT K tiles x 16 rows x 128 B (rows >= M and K tiles >= ktiles read as zeros)
   auto load_a = [&](int q) {
     const int s = q % I8_STAGES;
+    mbar_arrive_expect_tx(&full[s], A_BYTES);
     asm volatile(
         "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::
             "r"(smem_u32(base + s * STAGE)),
-        "l"(reinterpret_cast<uint64_t>(&tmA)), "r"(0), "r"(mg * 16), "r"(q * I8_KT_PER_STAGE), "r"(smem_u32(&full[s]))
+        "l"(reinterpret_cast<uint64_t>(&tmA)), "r"(0), "r"(mg * 16), "r"(q * I8_KT), "r"(smem_u32(&full[s]))
         : "memory");
   };
-  // B: BOXR-row pieces of the strip, 8 K tiles each (a piece never crosses
-  // a 128-row band of the packed layout)
-  auto load_b = [&](int q) {
-    const int s = q % I8_STAGES;
-#pragma unroll
-    for (int j = 0; j < SN / BOXR; ++j)
-      asm volatile(
-          "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];" ::
-              "r"(smem_u32(base + s * STAGE + A_BYTES + j * (I8_KT_PER_STAGE * BOXR * 128))),
-          "l"(reinterpret_cast<uint64_t>(&tmB)), "r"(0), "r"((n0 + BOXR * j) & 127), "r"(q * I8_KT_PER_STAGE),
-          "r"((n0 + BOXR * j) >> 7), "r"(smem_u32(&full[s]))
-          : "memory");
-  };
   // With constant weights the ring's first stages of B are requested before
-  // the wait on the previous kernel; their A halves follow after it.
+  // the wait on the previous kernel; the rest of the strip is warmed in L2.
   const int early = p.b_constant ? min(nstages, I8_STAGES) : 0;
-  if (warp == I8_B_WARP && lane == 0) {
-    for (int q = 0; q < early; ++q) {
-      mbar_arrive_expect_tx(&full[q], B_BYTES);
-      load_b(q);
-    }
+  if (threadIdx.x == I8_PRODUCER * 32) {
+    // A prefetch is only a cache hint: safe while the previous kernel runs.
+    for (int q = early; q < nstages; ++q)
+      asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                       reinterpret_cast<uint64_t>(&tmB)),
+                   "r"(0), "r"(0), "r"(q * I8_KT), "r"(u0)
+                   : "memory");
   }
+  if (threadIdx.x == 32) {
+    // A is warmed in L2 too (the previous kernel may still write it; L2
+    // stays coherent, so the hint is harmless).
+    for (int q = 0; q < nstages; ++q)
+      asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                       reinterpret_cast<uint64_t>(&tmA)),
+                   "r"(0), "r"(mg * 16), "r"(q * I8_KT)
+                   : "memory");
+  }
+  pdl_launch_dependents();
+  __syncthreads();
+  if (threadIdx.x == I8_PRODUCER * 32)
+    for (int q = 0; q < early; ++q) load_b(q);
   pdl_wait();  // A may be produced, and C read, by the previous kernel
 
-  if (warp >= I8_CW) {
+  if (warp == I8_PRODUCER) {
     // ------------------------------------------------------------ producers
-    // Two issuing warps, one for B and one for A: each thread's bulk copies
-    // complete one after another (about 0.4 us each from L2, whatever their
-    // size), so the two operands of a stage travel in parallel.
-    if (lane == 0) {
-      const bool is_b = warp == I8_B_WARP;
+    if (lane < 2) {
+      const bool is_b = lane == 0;
       int q = is_b ? early : 0;
       bool ok = true;
       for (; q < nstages; ++q) {
@@ -180,21 +199,19 @@ __global__ void __launch_bounds__(I8_THREADS, i8_ctas_per_sm(NB8))
           ok = false;
           break;
         }
-        if (is_b) {
-          mbar_arrive_expect_tx(&full[s], B_BYTES);
+        if (is_b)
           load_b(q);
-        } else {
-          mbar_arrive_expect_tx(&full[s], A_BYTES);
+        else
           load_a(q);
-        }
       }
-      const uint32_t issued = (uint32_t)q;
       if (!ok || *abort_flag) {
-        const uint32_t n = issued < (uint32_t)I8_STAGES ? issued : (uint32_t)I8_STAGES;
-        for (uint32_t i = 0; i < n; ++i) {
-          const uint32_t qq = issued - 1 - i;
+        // wait (bounded) for this thread's copies still in flight
+        const int issued = q;
+        for (int i = 0; i < I8_STAGES && i < issued; ++i) {
+          const int qq = issued - 1 - i;
           volatile int never = 0;
-          wait_bounded(&full[qq % I8_STAGES], (qq / I8_STAGES) & 1, &never, p.status, ST_TIMEOUT_DRAIN, limit);
+          wait_bounded(&full[qq % I8_STAGES], (uint32_t)(qq / I8_STAGES) & 1, &never, p.status, ST_TIMEOUT_DRAIN,
+                       limit);
         }
       }
     }
@@ -202,20 +219,22 @@ __global__ void __launch_bounds__(I8_THREADS, i8_ctas_per_sm(NB8))
   }
 
   // ------------------------------------------------------------ consumers
-  // Warp w takes K tile w of every stage.
-  const int g = lane >> 2;  // mma group id: A rows g, g+8 and B row g of each 8-row block
+  // Every warp sees every stage (warp w takes K tile w), so each waits on
+  // consecutive phases of every barrier.
+  const int g = lane >> 2;  // mma group id: A rows g, g+8 and row g of each 8-row unit
   const int t = lane & 3;
   int acc[NB8][4];
 #pragma unroll
   for (int nb = 0; nb < NB8; ++nb) acc[nb][0] = acc[nb][1] = acc[nb][2] = acc[nb][3] = 0;
+  int rs_lo = 0, rs_hi = 0;  // this lane's share of the row sums of A rows g and g + 8
 
   for (int q = 0; q < nstages; ++q) {
     const int s = q % I8_STAGES;
     const uint32_t ph = (uint32_t)(q / I8_STAGES) & 1;
     if (!wait_bounded(&full[s], ph, abort_flag, p.status, ST_TIMEOUT_CONSUMER, limit)) break;
-    const bool live = q * I8_KT_PER_STAGE + warp < p.ktiles;
+    const bool live = q * I8_KT + warp < p.ktiles;
     const uint8_t* sa = base + s * STAGE + warp * (16 * 128);
-    const uint8_t* sbp = base + s * STAGE + A_BYTES + warp * (BOXR * 128);  // + piece * (8 * BOXR * 128)
+    const uint8_t* sb = base + s * STAGE + A_BYTES + (warp * 8 + g) * 128;  // + unit * (I8_KT * 8 * 128)
     float f[NB8][4];
 #pragma unroll
     for (int nb = 0; nb < NB8; ++nb) f[nb][0] = f[nb][1] = f[nb][2] = f[nb][3] = 0.f;
@@ -226,11 +245,8 @@ __global__ void __launch_bounds__(I8_THREADS, i8_ctas_per_sm(NB8))
       const uint4 ag8 = *reinterpret_cast<const uint4*>(sa + (g + 8) * 128 + slot);
       uint4 bw[NB8];
 #pragma unroll
-      for (int nb = 0; nb < NB8; ++nb) {
-        const int row = nb * 8 + g;  // strip row; piece row / BOXR, row % BOXR within it
-        bw[nb] = *reinterpret_cast<const uint4*>(sbp + (row / BOXR) * (I8_KT_PER_STAGE * BOXR * 128) +
-                                                 (row % BOXR) * 128 + slot);
-      }
+      for (int nb = 0; nb < NB8; ++nb)
+        bw[nb] = *reinterpret_cast<const uint4*>(sb + nb * (I8_KT * 8 * 128) + slot);
       if (h == 1) {
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);  // this warp's reads of the stage are done
@@ -243,15 +259,19 @@ __global__ void __launch_bounds__(I8_THREADS, i8_ctas_per_sm(NB8))
         for (int j = 0; j < 4; ++j) {
           i8x4_to_f16x2(aw[j], alo[j], ahi[j]);
           i8x4_to_f16x2(a8w[j], a8lo[j], a8hi[j]);
+          rs_lo = __dp4a((int)aw[j], 0x01010101, rs_lo);
+          rs_hi = __dp4a((int)a8w[j], 0x01010101, rs_hi);
         }
 #pragma unroll
         for (int nb = 0; nb < NB8; ++nb) {
-          const uint32_t w[4] = {bw[nb].x, bw[nb].y, bw[nb].z, bw[nb].w};
+          if (nb < nu) {  // uniform: units past N are skipped
+            const uint32_t w[4] = {bw[nb].x, bw[nb].y, bw[nb].z, bw[nb].w};
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            uint32_t blo, bhi;
-            i8x4_to_f16x2(w[j], blo, bhi);
-            mma_16816(f[nb], alo[j], a8lo[j], ahi[j], a8hi[j], blo, bhi);
+            for (int j = 0; j < 4; ++j) {
+              uint32_t blo, bhi;
+              u8x4_to_f16x2_sub(w[j], blo, bhi);
+              mma_16816(f[nb], alo[j], a8lo[j], ahi[j], a8hi[j], blo, bhi);
+            }
           }
         }
       }
@@ -259,24 +279,33 @@ __global__ void __launch_bounds__(I8_THREADS, i8_ctas_per_sm(NB8))
 #pragma unroll
     for (int nb = 0; nb < NB8; ++nb) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) acc[nb][i] += __float2int_rn(f[nb][i]);
+      for (int i = 0; i < 4; ++i) acc[nb][i] += scaled_to_int(f[nb][i]);
     }
   }
+  // full row sums over this warp's K tiles (the 4 lanes of a group hold
+  // disjoint 32-byte slices of every K tile)
+  rs_lo += __shfl_xor_sync(0xffffffffu, rs_lo, 1);
+  rs_lo += __shfl_xor_sync(0xffffffffu, rs_lo, 2);
+  rs_hi += __shfl_xor_sync(0xffffffffu, rs_hi, 1);
+  rs_hi += __shfl_xor_sync(0xffffffffu, rs_hi, 2);
 
   // ------------------------------------------------------------ reduction
-  named_bar_sync(1, I8_CW * 32);  // every consumer is done with the ring
+  named_bar_sync(1, I8_CW * 32);  // every consumer is done with the ring (no copy in flight)
   int32_t* red = reinterpret_cast<int32_t*>(base);  // [CW][16][SN]
 #pragma unroll
   for (int nb = 0; nb < NB8; ++nb) {
     const int col = nb * 8 + 2 * t;
-    red[(warp * 16 + g) * SN + col] = acc[nb][0];
-    red[(warp * 16 + g) * SN + col + 1] = acc[nb][1];
-    red[(warp * 16 + g + 8) * SN + col] = acc[nb][2];
-    red[(warp * 16 + g + 8) * SN + col + 1] = acc[nb][3];
+    // sum a*b = sum a*(b + 128) - 128 * sum a
+    red[(warp * 16 + g) * SN + col] = acc[nb][0] - 128 * rs_lo;
+    red[(warp * 16 + g) * SN + col + 1] = acc[nb][1] - 128 * rs_lo;
+    red[(warp * 16 + g + 8) * SN + col] = acc[nb][2] - 128 * rs_hi;
+    red[(warp * 16 + g + 8) * SN + col + 1] = acc[nb][3] - 128 * rs_hi;
   }
   named_bar_sync(1, I8_CW * 32);
-  for (int i = threadIdx.x; i < 16 * rows; i += I8_CW * 32) {
-    const int m = i / rows, n = i - m * rows;
+  const int cols = nu * 8;
+  const int n0 = u0 * 8;
+  for (int i = threadIdx.x; i < 16 * cols; i += I8_CW * 32) {
+    const int m = i / cols, n = i - m * cols;
     int sum = 0;
 #pragma unroll
     for (int w = 0; w < I8_CW; ++w) sum += red[(w * 16 + m) * SN + n];
@@ -286,7 +315,7 @@ __global__ void __launch_bounds__(I8_THREADS, i8_ctas_per_sm(NB8))
 }
 
 // Tuning override, read once per process: GP_I8_STRIP (rows of B per CTA:
-// 16, 32 or 64).
+// 16, 32, 48 or 64).
 static int env_int(const char* name, int dflt) {
   const char* e = std::getenv(name);
   if (e == nullptr) return dflt;
@@ -296,7 +325,7 @@ static int env_int(const char* name, int dflt) {
 
 template <int NB8>
 static int launch_i8(const CUtensorMap& tmA, const CUtensorMap& tmB, I8Params p, dim3 grid, cudaStream_t stream) {
-  constexpr int STAGE = I8_KT_PER_STAGE * (16 + NB8 * 8) * 128;
+  constexpr int STAGE = I8_KT * (16 + NB8 * 8) * 128;
   constexpr int RED = I8_CW * 16 * NB8 * 8 * 4;
   constexpr int RING = I8_STAGES * STAGE;
   constexpr int SMEM = (RING > RED ? RING : RED) + 2 * I8_STAGES * 8 + 16 + 1024;
@@ -326,13 +355,12 @@ static int launch_i8(const CUtensorMap& tmA, const CUtensorMap& tmB, I8Params p,
 }
 
 int i8_strip_rows(int N, int num_sms) {
-  // Rows of B per CTA, a multiple of 16 (every strip is a whole number of
-  // 16-row pieces).  Prefer strips of at most 32 rows, which let two CTAs
-  // share an SM: with programmatic dependent launch the next product's CTAs
-  // then sit beside this one's and stream while it computes (measured 8.5 us
-  // against 9.5 us for one 48-row strip per SM at 16 x 7168 x 4096).  Wider
-  // problems take one strip per SM, at most 64 rows.  GP_I8_STRIP (16, 32,
-  // 48 or 64) overrides.
+  // Rows of B per CTA, a multiple of 16.  Prefer strips of at most 32 rows,
+  // which let two CTAs share an SM: with programmatic dependent launch the
+  // next product's CTAs then sit beside this one's and stream while it
+  // computes (measured 8.5 us against 9.5 us for one 48-row strip per SM at
+  // 16 x 7168 x 4096).  Wider problems take one strip per SM, at most 64
+  // rows.  GP_I8_STRIP (16, 32, 48 or 64) overrides.
   static const int strip_override = env_int("GP_I8_STRIP", 0);
   if (strip_override == 16 || strip_override == 32 || strip_override == 48 || strip_override == 64)
     return strip_override;
@@ -341,8 +369,6 @@ int i8_strip_rows(int N, int num_sms) {
   const int one_per_sm = 16 * ((N + 16 * num_sms - 1) / (16 * num_sms));
   return one_per_sm > 64 ? 64 : one_per_sm;
 }
-
-int i8_box_rows_for(int strip) { return i8_box_rows(strip); }
 
 int i8_gemm_launch(const CUtensorMap& tmA, const CUtensorMap& tmB, I8Params p, int num_sms, cudaStream_t stream) {
   const int strip = p.strip;

@@ -30,7 +30,7 @@ struct I8Params {
   uint64_t wait_limit_ns;
   int M, N, K;
   int ktiles;             // K / 128
-  int strip;              // rows of B per CTA (multiple of 16)
+  int strip;              // rows of B per CTA (multiple of 16), the B box height
   int stages;
   int b_constant;         // 1: B may be read before the previous kernel on the stream completes
 };
@@ -43,12 +43,12 @@ int splitk_gemm_launch(int kind, int split, const CUtensorMap& tmA, const CUtens
                        cudaStream_t stream);
 int mxf4_gemm_launch(const CUtensorMap& tmA, const CUtensorMap& tmC, TcParams p, int num_sms, cudaStream_t stream);
 int i8_strip_rows(int N, int num_sms);
-int i8_box_rows_for(int strip);
 int i8_gemm_launch(const CUtensorMap& tmA, const CUtensorMap& tmB, I8Params p, int num_sms, cudaStream_t stream);
 
-int pack_b_launch(const uint8_t* B, const uint8_t* Bsf, int64_t N, int64_t kbytes, int64_t nblk, uint8_t* out,
-                  cudaStream_t stream);
-int unpack_b_launch(const uint8_t* packed, int64_t N, int64_t kbytes, int64_t nblk, uint8_t* B, uint8_t* Bsf,
-                    cudaStream_t stream);
+// int8: 8-row bands and offset-binary bytes; otherwise 128-row bands, bytes as given
+int pack_b_launch(const uint8_t* B, const uint8_t* Bsf, int64_t N, int64_t kbytes, int64_t nblk, bool int8,
+                  uint8_t* out, cudaStream_t stream);
+int unpack_b_launch(const uint8_t* packed, int64_t N, int64_t kbytes, int64_t nblk, bool int8, uint8_t* B,
+                    uint8_t* Bsf, cudaStream_t stream);
 
 }  // namespace gp

@@ -4,8 +4,13 @@
 //
 // Layout (this library's own; the guide's CDNA layout targets MFMA
 // registers):
-//   - B's bytes [N, Kb] are cut into 128-row x 128-byte tiles.  Tile
-//     (tn, tk) is the 16 KiB block tn*(Kb/128) + tk.
+//   - B's bytes [N, Kb] are cut into R-row x 128-byte tiles: R = 128 for the
+//     tcgen05 element types (BF16, E4M3, E2M1), R = 8 for INT8, whose
+//     weight-streaming kernel gives each SM a strip of whole 8-row units.
+//     Tile (tn, tk) is the R*128-byte block tn*(Kb/128) + tk, so the K tiles
+//     of one band are contiguous.
+//   - INT8 bytes are stored in offset binary (b XOR 0x80 = b + 128 as an
+//     unsigned byte), the form the INT8 kernel hands to the MMA.
 //   - Row r of a tile lives at r*128.  Its 16-byte chunk c is stored at slot
 //     c ^ (r % 8).  This is the 128-byte-swizzled K-major image that tcgen05
 //     descriptors and TMA use, so one bulk copy lands a tile in shared memory
@@ -19,10 +24,11 @@
 
 namespace gp {
 
-__device__ __forceinline__ int64_t packed_chunk_offset(int64_t n, int64_t cc, int64_t ktiles) {
-  const int64_t tn = n >> 7, r = n & 127;
+// rshift = log2(R)
+__device__ __forceinline__ int64_t packed_chunk_offset(int64_t n, int64_t cc, int64_t ktiles, int rshift) {
+  const int64_t tn = n >> rshift, r = n & ((int64_t(1) << rshift) - 1);
   const int64_t tk = cc >> 3, c = cc & 7;
-  return (((tn * ktiles + tk) << 7) + r) * 128 + ((c ^ (r & 7)) << 4);
+  return (((tn * ktiles + tk) << rshift) + r) * 128 + ((c ^ (r & 7)) << 4);
 }
 
 __device__ __forceinline__ int64_t packed_scale_offset(int64_t n, int64_t j, int64_t nblk) {
@@ -34,23 +40,35 @@ __device__ __forceinline__ int64_t packed_scale_offset(int64_t n, int64_t j, int
 }
 
 // One thread per 16-byte chunk of B.
-__global__ void pack_data_kernel(const uint4* __restrict__ B, int64_t N, int64_t kbytes, uint8_t* __restrict__ out) {
+__global__ void pack_data_kernel(const uint4* __restrict__ B, int64_t N, int64_t kbytes, int rshift, uint32_t bias,
+                                 uint8_t* __restrict__ out) {
   const int64_t chunks_per_row = kbytes >> 4;
   const int64_t total = N * chunks_per_row;
   const int64_t ktiles = kbytes >> 7;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t n = i / chunks_per_row, cc = i - n * chunks_per_row;
-    *reinterpret_cast<uint4*>(out + packed_chunk_offset(n, cc, ktiles)) = B[i];
+    uint4 v = B[i];
+    v.x ^= bias;
+    v.y ^= bias;
+    v.z ^= bias;
+    v.w ^= bias;
+    *reinterpret_cast<uint4*>(out + packed_chunk_offset(n, cc, ktiles, rshift)) = v;
   }
 }
 
-__global__ void unpack_data_kernel(const uint8_t* __restrict__ in, int64_t N, int64_t kbytes, uint4* __restrict__ B) {
+__global__ void unpack_data_kernel(const uint8_t* __restrict__ in, int64_t N, int64_t kbytes, int rshift,
+                                   uint32_t bias, uint4* __restrict__ B) {
   const int64_t chunks_per_row = kbytes >> 4;
   const int64_t total = N * chunks_per_row;
   const int64_t ktiles = kbytes >> 7;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t n = i / chunks_per_row, cc = i - n * chunks_per_row;
-    B[i] = *reinterpret_cast<const uint4*>(in + packed_chunk_offset(n, cc, ktiles));
+    uint4 v = *reinterpret_cast<const uint4*>(in + packed_chunk_offset(n, cc, ktiles, rshift));
+    v.x ^= bias;
+    v.y ^= bias;
+    v.z ^= bias;
+    v.w ^= bias;
+    B[i] = v;
   }
 }
 
@@ -77,19 +95,25 @@ static int grid_for(int64_t total, int threads) {
   return (int)g;
 }
 
-int pack_b_launch(const uint8_t* B, const uint8_t* Bsf, int64_t N, int64_t kbytes, int64_t nblk, uint8_t* out,
-                  cudaStream_t stream) {
+int pack_b_launch(const uint8_t* B, const uint8_t* Bsf, int64_t N, int64_t kbytes, int64_t nblk, bool int8,
+                  uint8_t* out, cudaStream_t stream) {
   const int64_t chunks = N * (kbytes >> 4);
-  pack_data_kernel<<<grid_for(chunks, 256), 256, 0, stream>>>(reinterpret_cast<const uint4*>(B), N, kbytes, out);
+  const int rshift = int8 ? 3 : 7;
+  const uint32_t bias = int8 ? 0x80808080u : 0u;
+  pack_data_kernel<<<grid_for(chunks, 256), 256, 0, stream>>>(reinterpret_cast<const uint4*>(B), N, kbytes, rshift,
+                                                              bias, out);
   if (Bsf != nullptr)
     pack_scale_kernel<<<grid_for(N * nblk, 256), 256, 0, stream>>>(Bsf, N, nblk, out + N * kbytes);
   return cudaGetLastError() == cudaSuccess ? GP_OK : GP_ERR_CUDA;
 }
 
-int unpack_b_launch(const uint8_t* packed, int64_t N, int64_t kbytes, int64_t nblk, uint8_t* B, uint8_t* Bsf,
-                    cudaStream_t stream) {
+int unpack_b_launch(const uint8_t* packed, int64_t N, int64_t kbytes, int64_t nblk, bool int8, uint8_t* B,
+                    uint8_t* Bsf, cudaStream_t stream) {
   const int64_t chunks = N * (kbytes >> 4);
-  unpack_data_kernel<<<grid_for(chunks, 256), 256, 0, stream>>>(packed, N, kbytes, reinterpret_cast<uint4*>(B));
+  const int rshift = int8 ? 3 : 7;
+  const uint32_t bias = int8 ? 0x80808080u : 0u;
+  unpack_data_kernel<<<grid_for(chunks, 256), 256, 0, stream>>>(packed, N, kbytes, rshift, bias,
+                                                                reinterpret_cast<uint4*>(B));
   if (Bsf != nullptr)
     unpack_scale_kernel<<<grid_for(N * nblk, 256), 256, 0, stream>>>(packed + N * kbytes, N, nblk, Bsf);
   return cudaGetLastError() == cudaSuccess ? GP_OK : GP_ERR_CUDA;

@@ -19,6 +19,7 @@ enum : uint32_t {
   ST_TIMEOUT_EPILOGUE = 1u << 2,
   ST_TIMEOUT_CONSUMER = 1u << 3,
   ST_TIMEOUT_DRAIN = 1u << 4,
+  ST_BAD_LAUNCH = 1u << 5,  // a kernel's launch shape did not match its arguments
 };
 
 // A wait longer than this is treated as a hang (ns of %globaltimer).

@@ -44,7 +44,8 @@ typedef enum gp_status {
   GP_ERR_SHAPE = 3,           /* dimension rule violated (see gemm_run) */
   GP_ERR_ALIGNMENT = 4,       /* a pointer is not 16-byte aligned */
   GP_ERR_CUDA = 5,            /* a CUDA runtime/driver call failed */
-  GP_ERR_DEVICE_TIMEOUT = 6   /* a bounded in-kernel wait gave up (see gemm_last_device_status) */
+  GP_ERR_DEVICE_TIMEOUT = 6,  /* a bounded in-kernel wait gave up (see gemm_last_device_status) */
+  GP_ERR_DEVICE_CHECK = 7     /* a kernel's launch self-check failed (see gemm_last_device_status) */
 } gp_status;
 
 /* Element types.  E4M3 is OCP E4M3FN.  E2M1 packs two codes per byte, with
@@ -87,13 +88,17 @@ int gemm_packed_b_bytes(int dtype, int64_t N, int64_t K, size_t* bytes_out);
  * B_packed  : device, gemm_packed_b_bytes() bytes, written entirely.
  *
  * Layout of the packed buffer (a bijection of B's bytes):
- *   - B's bytes are cut into tiles of 128 rows x 128 bytes.  The tile of
- *     (row band tn, byte column tk) is the 16 KiB block with index
- *     tn*(Kb/128)+tk, where Kb = row bytes.
+ *   - B's bytes are cut into tiles of R rows x 128 bytes, with R = 128 for
+ *     BF16, E4M3 and E2M1 and R = 8 for INT8.  The tile of (row band tn,
+ *     byte column tk) is the R*128-byte block with index tn*(Kb/128)+tk,
+ *     where Kb = row bytes.
+ *   - INT8 bytes are stored in offset binary: b XOR 0x80, i.e. b + 128 as
+ *     an unsigned byte.
  *   - Inside a tile, row r sits at r*128.  Its 16-byte chunk c is stored at
  *     chunk slot c ^ (r % 8).  That is the 128-byte-swizzled K-major image
- *     that tcgen05 and TMA use, so one bulk copy moves a tile into shared
- *     memory ready for the MMA.
+ *     that tcgen05 and TMA use, so one bulk copy moves a 128-row tile into
+ *     shared memory ready for the MMA; the INT8 kernel's TMA copies take
+ *     any run of whole 8-row bands.
  *   - For E2M1, the block scales follow the data.  They are packed per
  *     (row band, 128-byte K tile) in two 512-byte groups of four K blocks.
  *     In a group, the byte for (row r, block j) is at
@@ -169,7 +174,9 @@ int gemm_run_ex(const void* A, const void* B_packed, int dtype, int64_t M, int64
 /*
  * Synchronises `stream`, then reads and clears the library's device status
  * word on the current device.  The word is set when a bounded wait in a GEMM
- * kernel times out.  Returns GP_OK, GP_ERR_DEVICE_TIMEOUT or GP_ERR_CUDA.
+ * kernel times out, or when a kernel's check of its own launch shape against
+ * its arguments fails (the kernel then returns before touching memory).
+ * Returns GP_OK, GP_ERR_DEVICE_TIMEOUT, GP_ERR_DEVICE_CHECK or GP_ERR_CUDA.
  */
 int gemm_last_device_status(void* stream);
 

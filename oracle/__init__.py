@@ -223,14 +223,17 @@ FLOAT_TOL = 8e-3
 
 
 # ----------------------------------------------------------------------------
-# Packed-B layout model (this library's own layout; see DESIGN.md)
+# Packed-B layout model (this library's own layout)
 #
 # B is a byte matrix [N, Kb] (Kb = K * element bytes; E2M1 packs two per
-# byte).  It is cut into tiles of 128 rows x 128 bytes; tile (tn, tk) is
-# stored at tile index tn * (Kb/128) + tk, i.e. all K-tiles of one 128-row
-# band are contiguous.  Inside a tile, row r occupies 128 bytes at r*128 and
-# its eight 16-byte chunks are permuted: chunk c of the row is stored at
-# chunk position c XOR (r mod 8).
+# byte).  It is cut into tiles of R rows x 128 bytes, where the band height R
+# is 128 for BF16, E4M3 and E2M1 (the tcgen05 tiles) and 8 for INT8 (the
+# weight-streaming kernel, whose per-SM strips are whole 8-row units).
+# Tile (tn, tk) is stored at tile index tn * (Kb/128) + tk, i.e. all K tiles
+# of one R-row band are contiguous.  Inside a tile, row r occupies 128 bytes
+# at r*128 and its eight 16-byte chunks are permuted: chunk c of the row is
+# stored at chunk position c XOR (r mod 8).  INT8 bytes are stored in offset
+# binary (b XOR 0x80 = b + 128 unsigned), the form its kernel feeds the MMA.
 # ----------------------------------------------------------------------------
 
 TILE_ROWS = 128
@@ -241,32 +244,37 @@ def elem_bits(dtype: str) -> int:
     return {"bf16": 16, "e4m3": 8, "int8": 8, "e2m1": 4}[dtype]
 
 
-def packed_offset(n: np.ndarray, kb: np.ndarray, Kb: int) -> np.ndarray:
-    """Byte offset in the packed buffer of byte (n, kb) of B."""
+def band_rows(dtype: str) -> int:
+    """Rows per packed tile: 8 for INT8, 128 for the tcgen05 element types."""
+    return 8 if dtype == "int8" else TILE_ROWS
+
+
+def packed_offset(n: np.ndarray, kb: np.ndarray, Kb: int, rows: int = TILE_ROWS) -> np.ndarray:
+    """Byte offset in the packed buffer of byte (n, kb) of B, for tiles of `rows` rows."""
     n = np.asarray(n, np.int64)
     kb = np.asarray(kb, np.int64)
     tiles_k = Kb // TILE_BYTES
-    tn, r = n // TILE_ROWS, n % TILE_ROWS
+    tn, r = n // rows, n % rows
     tk, col = kb // TILE_BYTES, kb % TILE_BYTES
     chunk, byte = col // 16, col % 16
     tile_index = tn * tiles_k + tk
-    return tile_index * (TILE_ROWS * TILE_BYTES) + r * TILE_BYTES + ((chunk ^ (r % 8)) * 16) + byte
+    return tile_index * (rows * TILE_BYTES) + r * TILE_BYTES + ((chunk ^ (r % 8)) * 16) + byte
 
 
-def pack_b_bytes(b_bytes: np.ndarray) -> np.ndarray:
+def pack_b_bytes(b_bytes: np.ndarray, rows: int = TILE_ROWS) -> np.ndarray:
     """Scatter every byte of B [N, Kb] to its packed offset."""
     b = np.ascontiguousarray(b_bytes).view(np.uint8)
     N, Kb = b.shape
     nn, kk = np.meshgrid(np.arange(N), np.arange(Kb), indexing="ij")
     out = np.zeros(N * Kb, dtype=np.uint8)
-    out[packed_offset(nn, kk, Kb).ravel()] = b.ravel()
+    out[packed_offset(nn, kk, Kb, rows).ravel()] = b.ravel()
     return out
 
 
-def unpack_b_bytes(packed: np.ndarray, N: int, Kb: int) -> np.ndarray:
+def unpack_b_bytes(packed: np.ndarray, N: int, Kb: int, rows: int = TILE_ROWS) -> np.ndarray:
     """Gather B [N, Kb] back from the packed buffer."""
     nn, kk = np.meshgrid(np.arange(N), np.arange(Kb), indexing="ij")
-    return np.asarray(packed, np.uint8)[packed_offset(nn, kk, Kb)]
+    return np.asarray(packed, np.uint8)[packed_offset(nn, kk, Kb, rows)]
 
 
 # Block scales of an MXFP4 B ([N, K/32] UE8M0) are packed per (128-row band,
@@ -300,9 +308,16 @@ def unpack_b_scales(packed: np.ndarray, N: int, nblk: int) -> np.ndarray:
     return np.asarray(packed, np.uint8)[packed_scale_offset(nn, jj, nblk)]
 
 
+def byte_bias(dtype: str) -> int:
+    """XOR applied to every packed data byte: INT8 is stored in offset binary
+    (b + 128 as an unsigned byte), the other element types unchanged."""
+    return 0x80 if dtype == "int8" else 0
+
+
 def pack_b(b: np.ndarray, dtype: str, scales: Optional[np.ndarray] = None) -> np.ndarray:
     """Whole packed buffer for B (data region, then the scale region for E2M1)."""
-    data = pack_b_bytes(np.ascontiguousarray(b).view(np.uint8).reshape(b.shape[0], -1))
+    raw = np.ascontiguousarray(b).view(np.uint8).reshape(b.shape[0], -1) ^ np.uint8(byte_bias(dtype))
+    data = pack_b_bytes(raw, band_rows(dtype))
     if dtype == "e2m1":
         return np.concatenate([data, pack_b_scales(scales)])
     return data

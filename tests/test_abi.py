@@ -24,7 +24,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for code in range(7):
+    for code in range(8):
         assert gp.gemm_status_string(code).startswith("GP_")
     assert "unknown" in gp.gemm_status_string(99)
 

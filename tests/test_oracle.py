@@ -289,35 +289,58 @@ def test_tflops_formula():
 
 # ---------------------------------------------------------------- pack model
 
+@pytest.mark.parametrize("rows", [128, 8])
 @pytest.mark.parametrize("N,Kb", [(128, 128), (256, 512), (384, 256)])
-def test_pack_roundtrip_and_permutation(N, Kb):
+def test_pack_roundtrip_and_permutation(N, Kb, rows):
     rng = np.random.default_rng(N + Kb)
     b = rng.integers(0, 256, size=(N, Kb), dtype=np.uint8)
-    p = oracle.pack_b_bytes(b)
+    p = oracle.pack_b_bytes(b, rows)
     assert p.size == b.size
-    assert np.array_equal(oracle.unpack_b_bytes(p, N, Kb), b)
-    offs = oracle.packed_offset(*np.meshgrid(np.arange(N), np.arange(Kb), indexing="ij"), Kb)
+    assert np.array_equal(oracle.unpack_b_bytes(p, N, Kb, rows), b)
+    offs = oracle.packed_offset(*np.meshgrid(np.arange(N), np.arange(Kb), indexing="ij"), Kb, rows)
     assert np.array_equal(np.sort(offs.ravel()), np.arange(N * Kb))  # a bijection
 
 
-def test_pack_layout_invariants():
+@pytest.mark.parametrize("rows", [128, 8])
+def test_pack_layout_invariants(rows):
+    check_pack_layout(rows)
+
+
+def check_pack_layout(rows):
     N, Kb = 256, 384
-    # index-encode: byte value identifies (row mod 128, 16-byte chunk) etc.
+    tile_bytes = rows * 128
+    # index-encode: byte value identifies (row mod rows, 16-byte chunk) etc.
     n, k = np.meshgrid(np.arange(N), np.arange(Kb), indexing="ij")
-    off = oracle.packed_offset(n, k, Kb)
-    tile = off // 16384
-    # each 16 KiB tile holds exactly one 128-row x 128-byte block of B
-    assert np.all(tile == (n // 128) * (Kb // 128) + k // 128)
+    off = oracle.packed_offset(n, k, Kb, rows)
+    tile = off // tile_bytes
+    # each tile holds exactly one rows x 128-byte block of B, K tiles of a band adjacent
+    assert np.all(tile == (n // rows) * (Kb // 128) + k // 128)
     # a 16-byte chunk of a row stays contiguous and in order
     assert np.all(off[:, 1:][k[:, 1:] % 16 != 0] == off[:, :-1][k[:, 1:] % 16 != 0] + 1)
     # rows sit at a 128-byte pitch inside their tile
-    assert np.all((off % 16384) // 128 == n % 128)
+    assert np.all((off % tile_bytes) // 128 == n % rows)
     # any 8 consecutive rows (aligned) reading the same logical chunk hit 8
     # distinct 16-byte positions: no shared-memory bank conflicts
     pos = (off % 128) // 16
     for c in range(8):
         for g in range(0, N, 8):
             assert len(set(pos[g:g + 8, c * 16].tolist())) == 8
+
+
+def test_pack_band_rows_per_dtype():
+    # INT8 packs 8-row bands: a band's K tiles are 1 KiB apart
+    assert oracle.band_rows("int8") == 8
+    assert all(oracle.band_rows(d) == 128 for d in ("bf16", "e4m3", "e2m1"))
+    b = np.arange(16 * 256, dtype=np.int64).astype(np.uint8).reshape(16, 256)
+    p = oracle.pack_b(b.view(np.int8), "int8") ^ np.uint8(0x80)  # undo the offset binary
+    assert np.array_equal(p[:128], b[0, :128])            # row 0, K tile 0
+    assert np.array_equal(p[1024:1024 + 128], b[0, 128:])  # row 0, K tile 1 follows the 8-row tile
+    assert np.array_equal(p[2048:2048 + 16], b[8, 0:16])  # row 8 opens band 1
+    # offset binary: -128 -> 0x00, 0 -> 0x80, 127 -> 0xff; other types untouched
+    q = oracle.pack_b(np.array([[-128, 0, 127, -1] * 32] * 8, np.int8), "int8")
+    assert q[0] == 0x00 and q[1] == 0x80 and q[2] == 0xFF and q[3] == 0x7F
+    e = np.arange(128 * 128, dtype=np.int64).astype(np.uint8).reshape(128, 128)
+    assert np.array_equal(oracle.pack_b(e, "e4m3"), oracle.pack_b_bytes(e))
 
 
 def test_pack_scale_roundtrip():
@@ -380,9 +403,11 @@ def test_planted_missing_column_scale_is_caught(monkeypatch):
 def test_planted_pack_swizzle_bug_is_caught(monkeypatch):
     good = oracle.packed_offset
 
-    def bad(n, kb, Kb):
-        o = good(n, kb, Kb)
+    def bad(n, kb, Kb, rows=128):
+        o = good(n, kb, Kb, rows)
         return o - (o % 128) + (np.asarray(kb) % 128)  # forgets the chunk permutation
     monkeypatch.setattr(oracle, "packed_offset", bad)
     with pytest.raises(AssertionError):
-        test_pack_layout_invariants()
+        check_pack_layout(128)
+    with pytest.raises(AssertionError):
+        check_pack_layout(8)
