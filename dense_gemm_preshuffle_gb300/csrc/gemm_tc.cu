@@ -10,11 +10,13 @@
 // This kernel is the Blackwell form of those steps.
 //   - One persistent CTA per SM walks BM x BN output tiles in a grouped
 //     order, so that concurrent CTAs share A rows and B columns in L2.
-//   - Warp 0, one lane, is the producer.  Each K step it issues one 2-D TMA
+//   - Warp 0 is the producer.  Each K step its lane 1 issues one 2-D TMA
 //     load for the BM x 128-byte A tile (128-byte swizzle, rows >= M
-//     zero-filled) and BN/128 plain bulk copies of 16 KiB packed-B tiles,
-//     which already hold the swizzled image.  Data lands in an S-stage
-//     shared-memory ring with full/empty mbarriers.
+//     zero-filled) and its lane 0 issues BN/128 plain bulk copies of 16 KiB
+//     packed-B tiles, which already hold the swizzled image.  One thread's
+//     copies complete one after another, so two issuers let A and B travel
+//     in parallel.  Data lands in an S-stage shared-memory ring with
+//     full/empty mbarriers.
 //   - Warp 1, one lane, issues tcgen05.mma.  Each 128-row half of the tile
 //     has its own fp32 accumulator in tensor memory, and both halves
 //     multiply the same B tile.
@@ -96,7 +98,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], 2);  // the A and the B issuer
       mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -132,7 +134,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const uint64_t pol_b = policy_evict_first();
     for (int kt = 0; kt < early; ++kt) {
       if (p.debug_skip_load == 1 + kt) continue;
-      mbar_arrive_expect_tx(&full[kt], Cfg::STAGE_BYTES);
+      mbar_arrive_expect_tx(&full[kt], Cfg::B_BYTES);
       for (int j = 0; j < BN / 128; ++j)
         bulk_load_hint(s_b + kt * Cfg::B_BYTES + j * 16384, bsrc + ((size_t)j * p.ktiles + kt) * 16384, 16384,
                        &full[kt], pol_b);
@@ -146,8 +148,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    // ------------------------------------------------------------ producers
+    // Lane 0 issues the B copies and lane 1 the A copies: one thread's bulk
+    // copies complete one after another, so the operands travel in parallel.
+    if (lane < 2) {
+      const bool is_b = lane == 0;
       int s = 0;
       uint32_t ph = 0;
       uint32_t issued = 0;
@@ -158,20 +163,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         tile_coords(t, p.tiles_m, p.tiles_n, mb, nb);
         const uint8_t* bsrc = p.Bp + (size_t)nb * (BN / 128) * p.ktiles * 16384;
         for (int kt = 0; kt < p.ktiles; ++kt) {
-          // the first `early` stages are free and already hold their B request
-          if ((int)issued >= early &&
-              !wait_bounded(&empty[s], ph ^ 1, abort_flag, p.status, ST_TIMEOUT_PRODUCER, limit)) {
+          // B's first `early` stages are free and already requested
+          const bool b_done = is_b && (int)issued < early;
+          if (!b_done && !wait_bounded(&empty[s], ph ^ 1, abort_flag, p.status, ST_TIMEOUT_PRODUCER, limit)) {
             ok = false;
             break;
           }
           if (p.debug_skip_load == 1 + (int)issued) {
             // Fault injection (host-selected): leave this stage's barrier
-            // without its arrival, so the consumer's bounded wait times out.
-          } else if ((int)issued < early) {
+            // without its arrivals, so the consumer's bounded wait times out.
+          } else if (!is_b) {
+            mbar_arrive_expect_tx(&full[s], Cfg::A_BYTES);
             tma_load_2d(s_a + s * Cfg::A_BYTES, &tmA, kt * 128, mb * BM, &full[s]);
-          } else {
-            mbar_arrive_expect_tx(&full[s], Cfg::STAGE_BYTES);
-            tma_load_2d(s_a + s * Cfg::A_BYTES, &tmA, kt * 128, mb * BM, &full[s]);
+          } else if (!b_done) {
+            mbar_arrive_expect_tx(&full[s], Cfg::B_BYTES);
             for (int j = 0; j < BN / 128; ++j)
               bulk_load_hint(s_b + s * Cfg::B_BYTES + j * 16384, bsrc + ((size_t)j * p.ktiles + kt) * 16384, 16384,
                              &full[s], pol_b);

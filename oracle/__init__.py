@@ -29,6 +29,13 @@ Contents:
 * Tile bookkeeping from the guide: section 1.2 (derived tile parameters),
   section 1.5 (MFMA count per tile), sections 8.1-8.2 (flops, bytes moved) and
   section 14 (worked example).
+* The fused epilogues the guide names for the preshuffle GEMM ("Kernel
+  Tuning Guide", section 6, Epilogue Strategies: "none", "bias",
+  "bias_relu", "bias_silu", "bias_gelu"), in fp64: the bias (one value per
+  output column) is added to the scaled product, then the activation.
+  ReLU max(x, 0); SiLU x / (1 + e^-x); GELU 0.5 x (1 + erf(x / sqrt 2)),
+  the exact (erf) form.  The guide names the epilogues without formulas;
+  these are the standard definitions.
 * The float parity metric max |C - C_ref| / (|C_ref| + 1e-2).
 
 Parity pins (tests/test_oracle.py): brute force in exact rational arithmetic,
@@ -209,6 +216,29 @@ def gemm_operands(ops, rows: Optional[np.ndarray] = None, cols: Optional[np.ndar
 # ----------------------------------------------------------------------------
 # Output rounding model and the parity metric
 # ----------------------------------------------------------------------------
+
+EPILOGUES = ("none", "bias", "bias_relu", "bias_silu", "bias_gelu")
+
+
+def apply_epilogue(c: np.ndarray, epilogue: str, bias: Optional[np.ndarray] = None) -> np.ndarray:
+    """The named epilogue applied to an fp64 product C [M, N]: C + bias[n],
+    then the activation ("Kernel Tuning Guide", section 6)."""
+    if epilogue not in EPILOGUES:
+        raise ValueError(f"unknown epilogue {epilogue!r}")
+    x = np.asarray(c, dtype=np.float64)
+    if epilogue == "none":
+        return x.copy()
+    x = x + np.asarray(bias, dtype=np.float64)[None, :]
+    if epilogue == "bias":
+        return x
+    if epilogue == "bias_relu":
+        return np.maximum(x, 0.0)
+    if epilogue == "bias_silu":
+        with np.errstate(over="ignore"):
+            return x / (1.0 + np.exp(-x))
+    from scipy.special import erf
+    return 0.5 * x * (1.0 + erf(x / np.sqrt(2.0)))
+
 
 def max_rel_err(c: np.ndarray, c_ref: np.ndarray) -> float:
     """max over all elements of |C - C_ref| / (|C_ref| + 1e-2)."""

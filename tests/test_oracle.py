@@ -411,3 +411,54 @@ def test_planted_pack_swizzle_bug_is_caught(monkeypatch):
         check_pack_layout(128)
     with pytest.raises(AssertionError):
         check_pack_layout(8)
+
+
+# ---------------------------------------------------------------- fused epilogues
+
+def test_epilogue_closed_forms_and_identities():
+    x = np.linspace(-30, 30, 2001)[None, :]
+    zero = np.zeros(x.shape[1])
+    relu = oracle.apply_epilogue(x, "bias_relu", zero)
+    silu = oracle.apply_epilogue(x, "bias_silu", zero)
+    gelu = oracle.apply_epilogue(x, "bias_gelu", zero)
+    # each activation f has f(x) - f(-x) = x (odd part x/2)
+    for f in (relu, silu, gelu):
+        assert np.allclose(f - f[:, ::-1], x, rtol=0, atol=1e-12)
+    assert relu[0, 1000] == 0 and silu[0, 1000] == 0 and gelu[0, 1000] == 0
+    assert silu[0, -1] == pytest.approx(30.0, rel=1e-12)          # sigmoid(30) = 1 - 9.4e-14
+    assert gelu[0, -1] == pytest.approx(30.0, rel=1e-15)
+    assert silu[0, 1000 + 66] == pytest.approx(x[0, 1066] / (1 + np.exp(-x[0, 1066])), rel=1e-15)
+    # GELU(1) = Phi(1) = 0.8413447460685429 (standard normal CDF at 1)
+    assert oracle.apply_epilogue(np.array([[1.0]]), "bias_gelu", np.zeros(1))[0, 0] == pytest.approx(
+        0.8413447460685429, rel=1e-14)
+
+
+def test_epilogue_vs_torch_library_routines():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(17)
+    c = rng.standard_normal((64, 96)) * 4
+    bias = rng.standard_normal(96)
+    x = torch.from_numpy(c + bias[None, :])
+    assert np.allclose(oracle.apply_epilogue(c, "bias_silu", bias), torch.nn.functional.silu(x).numpy(),
+                       rtol=1e-13, atol=1e-15)
+    assert np.allclose(oracle.apply_epilogue(c, "bias_gelu", bias),
+                       torch.nn.functional.gelu(x, approximate="none").numpy(), rtol=1e-13, atol=1e-15)
+    assert np.array_equal(oracle.apply_epilogue(c, "bias_relu", bias), torch.relu(x).numpy())
+    # bias is added exactly, per output column
+    assert np.array_equal(oracle.apply_epilogue(c, "bias", bias), c + bias[None, :])
+    assert np.array_equal(oracle.apply_epilogue(c, "none"), c)
+    with pytest.raises(ValueError):
+        oracle.apply_epilogue(c, "bias_tanh", bias)
+
+
+def test_planted_tanh_gelu_is_caught(monkeypatch):
+    good = oracle.apply_epilogue
+
+    def tanh_gelu(c, epilogue, bias=None):
+        if epilogue != "bias_gelu":
+            return good(c, epilogue, bias)
+        x = np.asarray(c, np.float64) + np.asarray(bias, np.float64)[None, :]
+        return 0.5 * x * (1 + np.tanh(np.sqrt(2 / np.pi) * (x + 0.044715 * x ** 3)))
+    monkeypatch.setattr(oracle, "apply_epilogue", tanh_gelu)
+    with pytest.raises(AssertionError):
+        test_epilogue_vs_torch_library_routines()
