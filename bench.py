@@ -26,6 +26,8 @@ it once per weight, not per product.
     sample.
   - "others": the other workloads, each with its own device-timed TFLOP/s
     and roofline fraction.
+  - "epilogues": each float workload with the fused bias + GELU epilogue,
+    beside the plain product's time.
 """
 from __future__ import annotations
 
@@ -235,11 +237,13 @@ class Problem:
         # the packed weights are complete (synchronised above) and never
         # rewritten: every step may pass GP_RUN_B_CONSTANT
         self.flags = gp.GP_RUN_DEFAULT if B_DEFAULT_FLAGS else gp.GP_RUN_B_CONSTANT
+        self.epilogue, self.bias = "none", None
 
     def step(self, i: int, stream=None):
         j = i % self.copies
         self.gp.gemm_run_ex(self.A[j], self.Bp[j], self.dtype, self.M, self.N, self.K, self.mode,
-                            self.sa, self.sb, self.C[j % len(self.C)], self.c_dtype, self.flags, stream)
+                            self.sa, self.sb, self.epilogue, self.bias, self.C[j % len(self.C)], self.c_dtype,
+                            self.flags, stream)
 
 
 def time_device(prob: Problem, steps: int, warmup: int, pg, device, graph_len: int = 100):
@@ -290,7 +294,7 @@ def time_e2e(prob: Problem, steps: int, warmup: int, device):
         if hsa is not None:
             prob.sa.copy_(hsa, non_blocking=True)
         prob.gp.gemm_run_ex(prob.A[j], prob.Bp[j], prob.dtype, prob.M, prob.N, prob.K, prob.mode, prob.sa,
-                            prob.sb, prob.C[0], prob.c_dtype, prob.flags)
+                            prob.sb, prob.epilogue, prob.bias, prob.C[0], prob.c_dtype, prob.flags)
         hc.copy_(prob.C[0], non_blocking=True)
     for i in range(max(3, warmup)):
         one(i)
@@ -437,6 +441,29 @@ def run_ours(args):
             except Exception as e:  # a workload whose kernel is not built yet
                 others[name] = {"unavailable": f"{type(e).__name__}: {e}"[:200]}
         out["others"] = others
+        # the fused bias + GELU epilogue on each float workload, against the plain product
+        epi = {}
+        for name in inputs.WORKLOADS:
+            if name.startswith("int8"):
+                continue
+            try:
+                p3 = Problem(name, device)
+                steps3 = max(20, min(args.steps, 400))
+                s_plain = time_device(p3, steps3, args.warmup, pg, device)
+                gen = torch.Generator().manual_seed(99)
+                p3.epilogue = "bias_gelu"
+                p3.bias = torch.randn(p3.N, generator=gen).to(device)
+                s_epi = time_device(p3, steps3, args.warmup, pg, device)
+                s_plain = max_over_ranks(pg, s_plain, device)
+                s_epi = max_over_ranks(pg, s_epi, device)
+                epi[name] = {"epilogue": "bias_gelu", "us_per_step": round(s_epi / steps3 * 1e6, 3),
+                             "plain_us_per_step": round(s_plain / steps3 * 1e6, 3),
+                             "TFLOP/s": round(p3.flops * steps3 / s_epi / 1e12, 2), "steps": steps3}
+                del p3
+                torch.cuda.empty_cache()
+            except Exception as e:
+                epi[name] = {"unavailable": f"{type(e).__name__}: {e}"[:200]}
+        out["epilogues"] = epi
     if rank == 0:
         if not args.no_cpu:
             out["cpu_baseline"] = cpu_baseline(args.workload)

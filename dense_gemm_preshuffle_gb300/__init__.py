@@ -32,6 +32,7 @@ DTYPES = {"bf16": 0, "e4m3": 1, "int8": 2, "e2m1": 3, "int32": 4}
 SCALE_MODES = {"none": 0, "rowcol_f32": 1, "block32_ue8m0": 2}
 GP_RUN_DEFAULT = 0
 GP_RUN_B_CONSTANT = 1
+EPILOGUES = {"none": 0, "bias": 1, "bias_relu": 2, "bias_silu": 3, "bias_gelu": 4}
 
 _lib = None
 
@@ -61,7 +62,7 @@ def load_library():
     lib.gemm_preshuffle_b.argtypes = [vp, vp, i32, i64, i64, vp, vp]
     lib.gemm_unpack_b.argtypes = [vp, i32, i64, i64, vp, vp, vp]
     lib.gemm_run.argtypes = [vp, vp, i32, i64, i64, i64, i32, vp, vp, vp, i32, vp]
-    lib.gemm_run_ex.argtypes = [vp, vp, i32, i64, i64, i64, i32, vp, vp, vp, i32, ctypes.c_uint, vp]
+    lib.gemm_run_ex.argtypes = [vp, vp, i32, i64, i64, i64, i32, vp, vp, i32, vp, vp, i32, ctypes.c_uint, vp]
     lib.gemm_last_device_status.argtypes = [vp]
     lib.gemm_status_string.argtypes = [i32]
     lib.gemm_status_string.restype = ctypes.c_char_p
@@ -139,11 +140,15 @@ def gemm_run(A, B_packed, dtype, M: int, N: int, K: int, scale_mode, scale_a, sc
                                    _ptr(scale_b), _ptr(C), _dt(c_dtype), _stream(stream)), "gemm_run")
 
 
-def gemm_run_ex(A, B_packed, dtype, M: int, N: int, K: int, scale_mode, scale_a, scale_b, C, c_dtype,
-                flags: int = GP_RUN_DEFAULT, stream=None) -> None:
+def _epi(x) -> int:
+    return EPILOGUES[x] if isinstance(x, str) else int(x)
+
+
+def gemm_run_ex(A, B_packed, dtype, M: int, N: int, K: int, scale_mode, scale_a, scale_b, epilogue, bias, C,
+                c_dtype, flags: int = GP_RUN_DEFAULT, stream=None) -> None:
     _check(load_library().gemm_run_ex(_ptr(A), _ptr(B_packed), _dt(dtype), M, N, K, _sm(scale_mode),
-                                      _ptr(scale_a), _ptr(scale_b), _ptr(C), _dt(c_dtype), int(flags),
-                                      _stream(stream)), "gemm_run_ex")
+                                      _ptr(scale_a), _ptr(scale_b), _epi(epilogue), _ptr(bias), _ptr(C),
+                                      _dt(c_dtype), int(flags), _stream(stream)), "gemm_run_ex")
 
 
 def gemm_last_device_status(stream=None) -> int:
@@ -167,9 +172,11 @@ def preshuffle_b(B, dtype, B_scales=None, stream=None):
 
 
 def matmul(A, B_packed, dtype, N: int, K: int, scale_a=None, scale_b=None, out=None, stream=None,
-           b_constant: bool = False):
+           b_constant: bool = False, epilogue: str = "none", bias=None):
     """C = A . B^T with B packed; returns bf16 [M, N] (int32 for int8).
 
+    epilogue: "none", "bias", "bias_relu", "bias_silu" or "bias_gelu", with
+    bias an fp32 [N] device tensor for all but "none".
     b_constant=True passes GP_RUN_B_CONSTANT: B_packed must not be written
     by any GPU work still in flight (pack once, then synchronise)."""
     import torch
@@ -185,6 +192,6 @@ def matmul(A, B_packed, dtype, N: int, K: int, scale_a=None, scale_b=None, out=N
         c_dtype, mode, tdt = "bf16", "none", torch.bfloat16
     if out is None:
         out = torch.empty((M, N), dtype=tdt, device=A.device)
-    gemm_run_ex(A, B_packed, d, M, N, K, mode, scale_a, scale_b, out, c_dtype,
+    gemm_run_ex(A, B_packed, d, M, N, K, mode, scale_a, scale_b, epilogue, bias, out, c_dtype,
                 GP_RUN_B_CONSTANT if b_constant else GP_RUN_DEFAULT, stream)
     return out

@@ -10,11 +10,13 @@
 // It owns no per-call memory.  Each device gets a 4-byte status word (a
 // __device__ variable) and a cached SM count.
 #include <atomic>
+#include <cuda_bf16.h>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
 
 #include "kernels.h"
+#include "epilogue.cuh"
 #include "ptx.cuh"
 
 namespace gp {
@@ -122,6 +124,14 @@ std::atomic<int> g_debug_skip_load{0};
 
 using namespace gp;
 
+// C[m, n] = bf16(act(bias[n])): the fused epilogue of an empty (K = 0) sum.
+__global__ void epilogue_broadcast_kernel(const float* __restrict__ bias, int act, int64_t M, int64_t N,
+                                          __nv_bfloat16* __restrict__ C) {
+  const int64_t total = M * N;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x)
+    C[i] = __float2bfloat16_rn(epi_act(bias[i % N], act));
+}
+
 extern "C" {
 
 const char* gemm_status_string(int status) {
@@ -183,13 +193,18 @@ int gemm_unpack_b(const void* B_packed, int dtype, int64_t N, int64_t K, void* B
 
 int gemm_run(const void* A, const void* B_packed, int dtype, int64_t M, int64_t N, int64_t K, int scale_mode,
              const void* scale_a, const void* scale_b, void* C, int c_dtype, void* stream) {
-  return gemm_run_ex(A, B_packed, dtype, M, N, K, scale_mode, scale_a, scale_b, C, c_dtype, GP_RUN_DEFAULT, stream);
+  return gemm_run_ex(A, B_packed, dtype, M, N, K, scale_mode, scale_a, scale_b, GP_EPI_NONE, nullptr, C, c_dtype,
+                     GP_RUN_DEFAULT, stream);
 }
 
 int gemm_run_ex(const void* A, const void* B_packed, int dtype, int64_t M, int64_t N, int64_t K, int scale_mode,
-                const void* scale_a, const void* scale_b, void* C, int c_dtype, unsigned flags, void* stream) {
+                const void* scale_a, const void* scale_b, int epilogue, const void* bias, void* C, int c_dtype,
+                unsigned flags, void* stream) {
   if ((flags & ~(unsigned)GP_RUN_B_CONSTANT) != 0) return GP_ERR_INVALID_ARG;
   const int b_constant = (flags & GP_RUN_B_CONSTANT) ? 1 : 0;
+  if (epilogue < GP_EPI_NONE || epilogue > GP_EPI_BIAS_GELU) return GP_ERR_INVALID_ARG;
+  if ((epilogue == GP_EPI_NONE) != (bias == nullptr)) return GP_ERR_INVALID_ARG;
+  if (epilogue != GP_EPI_NONE && c_dtype != GP_BF16) return GP_ERR_UNSUPPORTED;  // float outputs only
   // ---- combination
   const bool combo_ok = (dtype == GP_BF16 && scale_mode == GP_SCALE_NONE && c_dtype == GP_BF16) ||
                         (dtype == GP_E4M3 && scale_mode == GP_SCALE_ROWCOL_F32 && c_dtype == GP_BF16) ||
@@ -217,12 +232,23 @@ int gemm_run_ex(const void* A, const void* B_packed, int dtype, int64_t M, int64
   if (!aligned16(C) || (K > 0 && (!aligned16(A) || !aligned16(B_packed)))) return GP_ERR_ALIGNMENT;
   if (scale_mode == GP_SCALE_ROWCOL_F32 && (!aligned16(scale_a) || !aligned16(scale_b))) return GP_ERR_ALIGNMENT;
   if (scale_mode == GP_SCALE_BLOCK32_UE8M0 && !aligned16(scale_a)) return GP_ERR_ALIGNMENT;
+  if (bias != nullptr && !aligned16(bias)) return GP_ERR_ALIGNMENT;
 
   DeviceInfo* d = nullptr;
   if ((rc = device_info(&d)) != GP_OK) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (K == 0) {  // empty sum: C = 0
-    return cudaMemsetAsync(C, 0, (size_t)M * (size_t)N * c_elem, st) == cudaSuccess ? GP_OK : GP_ERR_CUDA;
+  if (K == 0) {  // empty sum: C = 0, or act(bias[n]) on every row with an epilogue
+    if (epilogue == GP_EPI_NONE)
+      return cudaMemsetAsync(C, 0, (size_t)M * (size_t)N * c_elem, st) == cudaSuccess ? GP_OK : GP_ERR_CUDA;
+    const int act = epilogue == GP_EPI_BIAS_RELU ? EPI_ACT_RELU
+                    : epilogue == GP_EPI_BIAS_SILU ? EPI_ACT_SILU
+                    : epilogue == GP_EPI_BIAS_GELU ? EPI_ACT_GELU
+                                                   : EPI_ACT_NONE;
+    const int64_t total = M * N;
+    const int blocks = (int)((total + 255) / 256 < 65536 ? (total + 255) / 256 : 65536);
+    epilogue_broadcast_kernel<<<blocks, 256, 0, st>>>(static_cast<const float*>(bias), act, M, N,
+                                                      static_cast<__nv_bfloat16*>(C));
+    return cudaGetLastError() == cudaSuccess ? GP_OK : GP_ERR_CUDA;
   }
 
   if (dtype == GP_INT8) {
@@ -287,6 +313,11 @@ int gemm_run_ex(const void* A, const void* B_packed, int dtype, int64_t M, int64
   p.ktiles = (int)(kb / 128);
   p.debug_skip_load = g_debug_skip_load.exchange(0);
   p.b_constant = b_constant;
+  p.bias = static_cast<const float*>(bias);
+  p.act = epilogue == GP_EPI_BIAS_RELU ? EPI_ACT_RELU
+          : epilogue == GP_EPI_BIAS_SILU ? EPI_ACT_SILU
+          : epilogue == GP_EPI_BIAS_GELU ? EPI_ACT_GELU
+                                         : EPI_ACT_NONE;
   if (scale_mode == GP_SCALE_ROWCOL_F32) {
     p.sa = static_cast<const float*>(scale_a);
     p.sb = static_cast<const float*>(scale_b);

@@ -31,6 +31,7 @@
 //     and tcgen05.mma issued by the same thread execute in order, so a
 //     stage's scale copy always lands before its MMAs read it.
 #include "kernels.h"
+#include "epilogue.cuh"
 #include "ptx.cuh"
 
 namespace gp {
@@ -313,9 +314,11 @@ __global__ void __launch_bounds__(F4_THREADS, 1)
           uint32_t r[32];
           tmem_ld_32x32b_x32(tbase + (uint32_t)(c * 64 + h * 32), r);
           tmem_ld_wait();
-          uint32_t pk[16];
+          float v[32];
 #pragma unroll
-          for (int q = 0; q < 16; ++q) pk[q] = pack_bf16x2(__uint_as_float(r[2 * q]), __uint_as_float(r[2 * q + 1]));
+          for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]);
+          uint32_t pk[16];
+          epi_row32(v, 1.0f, nullptr, p.bias != nullptr ? p.bias + n0 + h * 32 : nullptr, p.act, pk);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const int chunk = h * 4 + q;

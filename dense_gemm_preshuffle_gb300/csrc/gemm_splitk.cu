@@ -32,6 +32,7 @@
 #include <cstdlib>
 
 #include "kernels.h"
+#include "epilogue.cuh"
 #include "ptx.cuh"
 
 namespace gp {
@@ -332,18 +333,8 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
             }
           }
           uint32_t pk[16];
-          if (p.sb != nullptr) {
-            const float4* sb4 = reinterpret_cast<const float4*>(p.sb + n0 + h * 32);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              const float4 s4 = __ldg(sb4 + q);
-              pk[2 * q] = pack_bf16x2(v[4 * q] * sa * s4.x, v[4 * q + 1] * sa * s4.y);
-              pk[2 * q + 1] = pack_bf16x2(v[4 * q + 2] * sa * s4.z, v[4 * q + 3] * sa * s4.w);
-            }
-          } else {
-#pragma unroll
-            for (int q = 0; q < 16; ++q) pk[q] = pack_bf16x2(v[2 * q], v[2 * q + 1]);
-          }
+          epi_row32(v, sa, p.sb != nullptr ? p.sb + n0 + h * 32 : nullptr,
+                    p.bias != nullptr ? p.bias + n0 + h * 32 : nullptr, p.act, pk);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const int chunk = h * 4 + q;

@@ -24,11 +24,15 @@
 //     <= 512 columns), so the epilogue of one tile overlaps the main loop of
 //     the next.  tcgen05.commit releases each ring stage and signals a
 //     finished accumulator.
-//   - Warps 2-5 are the epilogue.  Each warp reads its 32 TMEM lanes (in each
-//     half) with tcgen05.ld and forms acc * scale_a[m] * scale_b[n] in fp32.
-//     It rounds to bf16 (RNE) and writes 32 x 64 staging tiles with the
-//     128-byte swizzle, so the shared-memory stores are free of bank
-//     conflicts.  A TMA store writes the tiles out and clips rows >= M.
+//   - Warps 2-9 are the epilogue, two per 32-lane quarter of TMEM (a warp
+//     may only read the quarter warp % 4), taking alternate 64-column
+//     chunks.  Each reads its 32 TMEM lanes with tcgen05.ld and forms
+//     acc * scale_a[m] * scale_b[n] (+ bias[n], then the activation of a
+//     fused epilogue) in fp32.  It rounds to bf16 (RNE) and writes 32 x 64
+//     staging tiles with the 128-byte swizzle, so the shared-memory stores
+//     are free of bank conflicts.  A TMA store writes the tiles out and
+//     clips rows >= M.  With the single 512-column accumulator of 256 x 256
+//     tiles the epilogue is not overlapped, so eight warps halve it.
 //
 // Why BM = 256: on GB300 each SM takes in operands at about 110 GB/s from
 // L2.  For the 128 x 256 tile that bound caps FP8 near 2.9 PFLOP/s.
@@ -40,11 +44,13 @@
 // step moves 128 bytes of each row (64 bf16 or 128 e4m3 elements), and one
 // MMA instruction consumes 32 bytes of K.
 #include "kernels.h"
+#include "epilogue.cuh"
 #include "ptx.cuh"
 
 namespace gp {
 
-constexpr int TC_THREADS = 192;
+constexpr int TC_EPI_WARPS = 8;  // warps 2..9: two per TMEM lane quarter, alternate 64-column chunks
+constexpr int TC_THREADS = 32 * (2 + TC_EPI_WARPS);
 
 template <int BM, int BN, int STAGES>
 struct TcCfg {
@@ -52,7 +58,7 @@ struct TcCfg {
   static constexpr int A_BYTES = BM * 128;
   static constexpr int B_BYTES = BN * 128;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int EPI_BYTES = 4 * 32 * 128;
+  static constexpr int EPI_BYTES = TC_EPI_WARPS * 32 * 128;  // one 32 x 64 bf16 staging tile per warp
   static constexpr int ACC_COLS = MH * BN;  // one accumulator buffer
   static constexpr int NBUF = (2 * ACC_COLS <= 512) ? 2 : 1;
   static constexpr int TMEM_NEED = NBUF * ACC_COLS;
@@ -103,7 +109,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&accf[b], 1);
-      mbar_init(&acce[b], 4);
+      mbar_init(&acce[b], TC_EPI_WARPS);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -253,6 +259,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int quad = warp & 3;  // TMEM lanes this warp may access: quad*32 .. +31
+    const int chalf = (warp - 2) / 4;  // this warp takes the 64-column chunks c with c % 2 == chalf
     uint8_t* stg = s_epi + (warp - 2) * 4096;
     const uint32_t stg_row = smem_u32(stg) + lane * 128;
     int local = 0;
@@ -270,7 +277,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const float sa = (p.sa != nullptr && m < p.M) ? __ldg(p.sa + m) : 1.0f;
         const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(buf * Cfg::ACC_COLS + mh * BN);
 #pragma unroll 1
-        for (int c = 0; c < BN / 64; ++c) {
+        for (int c = chalf; c < BN / 64; c += 2) {
           const int n0 = nb * BN + c * 64;
           // the previous TMA store from this staging tile must have read it
           if (lane == 0) bulk_wait_group_read<0>();
@@ -280,22 +287,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             uint32_t r[32];
             tmem_ld_32x32b_x32(tbase + (uint32_t)(c * 64 + h * 32), r);
             tmem_ld_wait();
+            float v[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]);
             uint32_t pk[16];
-            if (p.sb != nullptr) {
-              const float4* sb4 = reinterpret_cast<const float4*>(p.sb + n0 + h * 32);
-#pragma unroll
-              for (int q = 0; q < 8; ++q) {
-                const float4 s4 = __ldg(sb4 + q);
-                pk[2 * q] =
-                    pack_bf16x2(__uint_as_float(r[4 * q]) * sa * s4.x, __uint_as_float(r[4 * q + 1]) * sa * s4.y);
-                pk[2 * q + 1] = pack_bf16x2(__uint_as_float(r[4 * q + 2]) * sa * s4.z,
-                                            __uint_as_float(r[4 * q + 3]) * sa * s4.w);
-              }
-            } else {
-#pragma unroll
-              for (int q = 0; q < 16; ++q)
-                pk[q] = pack_bf16x2(__uint_as_float(r[2 * q]), __uint_as_float(r[2 * q + 1]));
-            }
+            epi_row32(v, sa, p.sb != nullptr ? p.sb + n0 + h * 32 : nullptr,
+                      p.bias != nullptr ? p.bias + n0 + h * 32 : nullptr, p.act, pk);
             // 128-byte swizzle: 16-byte chunk j of row `lane` goes to slot j ^ (lane % 8)
 #pragma unroll
             for (int q = 0; q < 4; ++q) {

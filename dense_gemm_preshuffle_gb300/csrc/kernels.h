@@ -14,6 +14,8 @@ struct TcParams {
   const uint8_t* sfa;     // A scales, UE8M0 [M, K/32] row-major (E2M1 only)
   const float* sa;        // fp32 [M] row scales or null
   const float* sb;        // fp32 [N] column scales or null
+  const float* bias;      // fp32 [N] epilogue bias or null (no epilogue)
+  int act;                // epilogue activation after the bias (EpiAct)
   uint32_t* status;       // device status word
   uint64_t wait_limit_ns; // bounded-wait limit
   int M, N, K;            // K in elements

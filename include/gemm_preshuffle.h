@@ -147,6 +147,20 @@ int gemm_run(const void* A, const void* B_packed, int dtype, int64_t M, int64_t 
              int scale_mode, const void* scale_a, const void* scale_b, void* C, int c_dtype,
              void* stream);
 
+/* Fused epilogues of the float-output products ("Kernel Tuning Guide",
+ * section 6, Epilogue Strategies, names "none", "bias", "bias_relu",
+ * "bias_silu" and "bias_gelu").  After the scales, v = acc * scale_a[m] *
+ * scale_b[n] + bias[n] with bias fp32 [N], then the activation: ReLU
+ * max(v, 0); SiLU v / (1 + e^-v); GELU 0.5 v (1 + erf(v / sqrt 2)) (the
+ * exact form).  The result is rounded to bf16. */
+typedef enum gp_epilogue {
+  GP_EPI_NONE = 0,
+  GP_EPI_BIAS = 1,
+  GP_EPI_BIAS_RELU = 2,
+  GP_EPI_BIAS_SILU = 3,
+  GP_EPI_BIAS_GELU = 4
+} gp_epilogue;
+
 /* Flags of gemm_run_ex. */
 typedef enum gp_run_flags {
   GP_RUN_DEFAULT = 0,
@@ -161,15 +175,25 @@ typedef enum gp_run_flags {
 } gp_run_flags;
 
 /*
- * gemm_run with flags (a bitwise OR of gp_run_flags); gemm_run is
- * gemm_run_ex with GP_RUN_DEFAULT.  Unknown flag bits return
- * GP_ERR_INVALID_ARG before any launch.  This is a scheduling option of
- * this library: the method itself only assumes that the packed weights are
- * produced once, offline ("GEMM Optimization Guide" section 12).
+ * gemm_run with a fused epilogue and flags; gemm_run is gemm_run_ex with
+ * GP_EPI_NONE, bias NULL and GP_RUN_DEFAULT.
+ *
+ * epilogue : a gp_epilogue.  Any value but GP_EPI_NONE needs c_dtype
+ *            GP_BF16 (else GP_ERR_UNSUPPORTED; the INT8 product keeps its
+ *            exact int32 output).
+ * bias     : device, fp32 [N], 16-byte aligned; required for every epilogue
+ *            but GP_EPI_NONE, and NULL with it (else GP_ERR_INVALID_ARG).
+ * flags    : a bitwise OR of gp_run_flags.  Unknown bits return
+ *            GP_ERR_INVALID_ARG before any launch.  GP_RUN_B_CONSTANT is a
+ *            scheduling option of this library: the method itself only
+ *            assumes that the packed weights are produced once, offline
+ *            ("GEMM Optimization Guide" section 12).
+ * The other arguments are as for gemm_run.  With K == 0 the product is
+ * zero, so every row of C is act(bias[n]) (a broadcast kernel).
  */
 int gemm_run_ex(const void* A, const void* B_packed, int dtype, int64_t M, int64_t N, int64_t K,
-                int scale_mode, const void* scale_a, const void* scale_b, void* C, int c_dtype,
-                unsigned flags, void* stream);
+                int scale_mode, const void* scale_a, const void* scale_b, int epilogue,
+                const void* bias, void* C, int c_dtype, unsigned flags, void* stream);
 
 /*
  * Synchronises `stream`, then reads and clears the library's device status

@@ -91,9 +91,25 @@ def test_empty_problem_is_a_noop(lib):
 
 
 def test_run_ex_rejects_unknown_flags(lib):
-    rc = lib.gemm_run_ex(FAKE, FAKE, gp.DTYPES["e4m3"], 16, 256, 512, 0, None, None, FAKE, gp.DTYPES["bf16"], 2, None)
+    rc = lib.gemm_run_ex(FAKE, FAKE, gp.DTYPES["e4m3"], 16, 256, 512, 0, None, None, 0, None, FAKE,
+                         gp.DTYPES["bf16"], 2, None)
     assert rc == 1
     # the known flag passes validation; a shape error is still reported first-class
-    rc = lib.gemm_run_ex(FAKE, FAKE, gp.DTYPES["e4m3"], 16, 100, 512, 0, None, None, FAKE, gp.DTYPES["bf16"],
-                         gp.GP_RUN_B_CONSTANT, None)
+    rc = lib.gemm_run_ex(FAKE, FAKE, gp.DTYPES["e4m3"], 16, 100, 512, 0, None, None, 0, None, FAKE,
+                         gp.DTYPES["bf16"], gp.GP_RUN_B_CONSTANT, None)
     assert rc == 3
+
+
+@pytest.mark.parametrize("epi,bias,dtype,c_dtype,code", [
+    (5, FAKE, "e4m3", "bf16", 1),        # unknown epilogue
+    (-1, FAKE, "e4m3", "bf16", 1),
+    (1, None, "e4m3", "bf16", 1),        # an epilogue needs a bias
+    (0, FAKE, "e4m3", "bf16", 1),        # no epilogue takes no bias
+    (2, FAKE, "int8", "int32", 2),       # float outputs only
+    (4, FAKE + 4, "e4m3", "bf16", 4),    # bias must be 16-byte aligned
+])
+def test_run_ex_epilogue_validation(lib, epi, bias, dtype, c_dtype, code):
+    mode = 0
+    rc = lib.gemm_run_ex(FAKE, FAKE, gp.DTYPES[dtype], 16, 256, 512, mode, None, None, epi, bias, FAKE,
+                         gp.DTYPES[c_dtype], 0, None)
+    assert rc == code

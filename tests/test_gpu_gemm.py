@@ -301,3 +301,51 @@ def test_b_constant_reads_a_only_after_previous_kernel(M, N1, K1, N2):
         torch.cuda.synchronize()
         assert torch.equal(C2.view(torch.int16), again.view(torch.int16))
     check(ops1, C1, rows=sample_rows(M, 16, seed=6))
+
+
+# ---------------------------------------------------------------- fused epilogues
+
+EPI_SHAPES = [("bf16", 257, 384, 512), ("e4m3", 300, 512, 1024), ("e2m1", 200, 512, 512), ("e4m3", 17, 256, 256),
+              ("e4m3", 4173, 9728, 256),   # 256-row tile path
+              ("bf16", 400, 4096, 8192)]   # split-K cluster path
+
+
+@pytest.mark.parametrize("epilogue", ["bias", "bias_relu", "bias_silu", "bias_gelu"])
+@pytest.mark.parametrize("dtype,M,N,K", EPI_SHAPES, ids=lambda v: str(v))
+def test_fused_epilogue(dtype, M, N, K, epilogue):
+    """C = act(A.B^T scaled + bias[n]) against the oracle's fp64 epilogue."""
+    ops = inputs.make_operands(dtype, M, N, K, seed=5000 + M + N + K)
+    rows = None if M * N <= 1 << 21 else np.unique(np.concatenate([sample_rows(M, 24, seed=7), [M - 1]]))
+    plain = oracle.gemm_operands(ops, rows=rows)
+    rng = np.random.default_rng(M + N)
+    bias = (rng.standard_normal(N) * plain.std()).astype(np.float32)
+    A, B, sa, sb = dev(ops)
+    if dtype == "e2m1":
+        Bp = gp.preshuffle_b(B, "e2m1", B_scales=sb)
+        C = gp.matmul(A, Bp, "e2m1", N, K, scale_a=sa, epilogue=epilogue, bias=torch.from_numpy(bias).cuda())
+    else:
+        Bp = gp.preshuffle_b(B, dtype)
+        C = gp.matmul(A, Bp, dtype, N, K, scale_a=sa, scale_b=sb, epilogue=epilogue,
+                      bias=torch.from_numpy(bias).cuda())
+    torch.cuda.synchronize()
+    assert gp.gemm_last_device_status() == 0
+    c = as_host(C)
+    if rows is not None:
+        c = c[rows]
+    ref = oracle.apply_epilogue(plain, epilogue, bias.astype(np.float64))
+    err = oracle.max_rel_err(c, ref)
+    assert err <= TOL, f"max rel err {err:.3e}"
+
+
+@pytest.mark.parametrize("epilogue", ["bias", "bias_relu", "bias_silu", "bias_gelu"])
+def test_fused_epilogue_empty_sum(epilogue):
+    # K == 0: the product is zero, every row is act(bias)
+    M, N = 5, 256
+    bias = np.linspace(-6, 6, N).astype(np.float32)
+    C = torch.full((M, N), 7.0, dtype=torch.bfloat16, device="cuda")
+    dummy = torch.empty(16, dtype=torch.uint8, device="cuda")
+    gp.gemm_run_ex(dummy, dummy, "bf16", M, N, 0, "none", None, None, epilogue, torch.from_numpy(bias).cuda(), C,
+                   "bf16")
+    torch.cuda.synchronize()
+    ref = oracle.apply_epilogue(np.zeros((M, N)), epilogue, bias.astype(np.float64))
+    assert oracle.max_rel_err(as_host(C), ref) <= TOL
