@@ -14,6 +14,7 @@ Recipes (the workloads' stated distributions):
   A row whose amax is 0 gets s = 1.
 * INT8: integers uniform in [-127, 127].
 * BF16: x = N(0,1)/sqrt(K) in fp32, rounded to bf16 (torch cast, RNE).
+* FP16: the same draws rounded to IEEE binary16 (torch cast, RNE).
 * MXFP4: x ~ N(0,1) fp32; per (row, 32-element K block) the shared exponent
   e is the smallest integer with amax <= 6 * 2^e (i.e. ceil(log2(amax/6))
   evaluated exactly), clamped to [-127, 127], stored biased (e + 127) as
@@ -36,7 +37,7 @@ import torch
 SEED_BASE = 20261202
 
 # dtype names used across the package, the binding and the tests
-BF16, E4M3, INT8, E2M1 = "bf16", "e4m3", "int8", "e2m1"
+BF16, E4M3, INT8, E2M1, FP16 = "bf16", "e4m3", "int8", "e2m1", "fp16"
 
 
 @dataclass
@@ -69,7 +70,8 @@ class Operands:
     """Encoded operands.  Arrays are host numpy arrays, row-major.
 
     a, b       : codes.  uint8 [rows, K] for e4m3 / int8 (int8 viewed as
-                 int8), uint16 [rows, K] bf16 bits, uint8 [rows, K/2] for e2m1.
+                 int8), uint16 [rows, K] bf16 or fp16 bits, uint8 [rows, K/2]
+                 for e2m1.
     scale_a/b  : float32 [rows] (e4m3) or uint8 [rows, K/32] UE8M0 (e2m1),
                  None otherwise.
     """
@@ -119,6 +121,16 @@ def bf16_rows(rows: int, K: int, g: torch.Generator, chunk: int = 2048):
         r1 = min(rows, r0 + chunk)
         x = torch.randn((r1 - r0, K), generator=g, dtype=torch.float32) / math.sqrt(K)
         out[r0:r1] = x.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    return out
+
+
+def fp16_rows(rows: int, K: int, g: torch.Generator, chunk: int = 2048):
+    """N(0,1)/sqrt(K) rounded to IEEE binary16; returned as uint16 bit patterns."""
+    out = np.empty((rows, K), dtype=np.uint16)
+    for r0 in range(0, rows, chunk):
+        r1 = min(rows, r0 + chunk)
+        x = torch.randn((r1 - r0, K), generator=g, dtype=torch.float32) / math.sqrt(K)
+        out[r0:r1] = x.to(torch.float16).view(torch.int16).numpy().view(np.uint16)
     return out
 
 
@@ -183,6 +195,8 @@ def make_operands(dtype: str, M: int, N: int, K: int, seed: int) -> Operands:
         return Operands(dtype, M, N, K, int8_rows(M, K, g), int8_rows(N, K, g))
     if dtype == BF16:
         return Operands(dtype, M, N, K, bf16_rows(M, K, g), bf16_rows(N, K, g))
+    if dtype == FP16:
+        return Operands(dtype, M, N, K, fp16_rows(M, K, g), fp16_rows(N, K, g))
     if dtype == E2M1:
         a, ea = mxfp4_rows(M, K, g)
         b, eb = mxfp4_rows(N, K, g)

@@ -13,10 +13,11 @@ Contents:
     is NaN)
   - E2M1 and UE8M0 (OCP Microscaling formats v1.0)
   - BF16 (the upper half of an IEEE binary32)
+  - FP16 (IEEE 754 binary16: bias 15, 10 fraction bits, subnormals)
 * GEMMs in fp64 / int64.  The triple loops live in ``gemm_oracle.c``, built
   by ``oracle/build.py``:
   - INT8: C = sum_k a*b, exact in int64.
-  - BF16: C = sum_k a*b, fp64.
+  - BF16 and FP16: C = sum_k a*b, fp64.
   - E4M3 with per-row/per-column fp32 scales: C = (sum_k qa*qb) * sa[m] * sb[n].
     "GEMM Optimization Guide", section 7.1 (direct store): the epilogue forms
     acc * scale_a * scale_b.  Every E4M3 product is a multiple of 2^-18 and
@@ -129,6 +130,20 @@ def decode_bf16(bits: np.ndarray) -> np.ndarray:
     return b.view(np.float32).astype(np.float64)
 
 
+def decode_fp16(bits: np.ndarray) -> np.ndarray:
+    """IEEE 754 binary16 bit pattern -> value (fp64): sign, 5 exponent bits
+    (bias 15), 10 fraction bits; exponent 0 is subnormal (2^-14 * f/1024),
+    exponent 31 is infinity (f = 0) or NaN."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.int64)
+    sign = np.where(b >> 15, -1.0, 1.0)
+    e = (b >> 10) & 0x1F
+    f = (b & 0x3FF).astype(np.float64)
+    normal = sign * (1.0 + f / 1024.0) * np.exp2(e.astype(np.float64) - 15.0)
+    sub = sign * (f / 1024.0) * 2.0 ** -14
+    special = np.where(f == 0, sign * np.inf, np.nan)
+    return np.where(e == 0, sub, np.where(e == 31, special, normal))
+
+
 def unpack_e2m1_rows(packed: np.ndarray, K: int) -> np.ndarray:
     """[rows, K/2] bytes (low nibble = even k) -> [rows, K] codes."""
     p = np.asarray(packed, dtype=np.uint8)
@@ -166,6 +181,10 @@ def gemm_f64(a: np.ndarray, b: np.ndarray) -> np.ndarray:
 
 def gemm_bf16(a_bits: np.ndarray, b_bits: np.ndarray) -> np.ndarray:
     return gemm_f64(decode_bf16(a_bits), decode_bf16(b_bits))
+
+
+def gemm_fp16(a_bits: np.ndarray, b_bits: np.ndarray) -> np.ndarray:
+    return gemm_f64(decode_fp16(a_bits), decode_fp16(b_bits))
 
 
 def gemm_e4m3_rowcol(qa: np.ndarray, qb: np.ndarray, sa: np.ndarray, sb: np.ndarray) -> np.ndarray:
@@ -206,6 +225,8 @@ def gemm_operands(ops, rows: Optional[np.ndarray] = None, cols: Optional[np.ndar
         return gemm_int8(a, b)
     if ops.dtype == "bf16":
         return gemm_bf16(a, b)
+    if ops.dtype == "fp16":
+        return gemm_fp16(a, b)
     if ops.dtype == "e4m3":
         return gemm_e4m3_rowcol(a, b, sa, sb)
     if ops.dtype == "e2m1":
@@ -271,7 +292,7 @@ TILE_BYTES = 128
 
 
 def elem_bits(dtype: str) -> int:
-    return {"bf16": 16, "e4m3": 8, "int8": 8, "e2m1": 4}[dtype]
+    return {"bf16": 16, "fp16": 16, "e4m3": 8, "int8": 8, "e2m1": 4}[dtype]
 
 
 def band_rows(dtype: str) -> int:

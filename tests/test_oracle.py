@@ -462,3 +462,47 @@ def test_planted_tanh_gelu_is_caught(monkeypatch):
     monkeypatch.setattr(oracle, "apply_epilogue", tanh_gelu)
     with pytest.raises(AssertionError):
         test_epilogue_vs_torch_library_routines()
+
+
+# ---------------------------------------------------------------- FP16 operands
+
+def test_fp16_decode_all_codes_vs_numpy():
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)   # a library decode of the same codes
+    got = oracle.decode_fp16(bits)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    # hand-checked codes: 1.0, -2.0, 65504 (max), 2^-24 (smallest subnormal), 2^-14 (smallest normal)
+    assert list(oracle.decode_fp16(np.array([0x3C00, 0xC000, 0x7BFF, 0x0001, 0x0400], np.uint16))) == [
+        1.0, -2.0, 65504.0, 2.0 ** -24, 2.0 ** -14]
+
+
+@pytest.mark.parametrize("M,N,K", [(3, 4, 16), (4, 2, 40)])
+def test_fp16_vs_fraction(M, N, K):
+    ops = inputs.make_operands("fp16", M, N, K, seed=12)
+    av = ops.a.view(np.float16).astype(np.float64)
+    bv = ops.b.view(np.float16).astype(np.float64)
+    exact = frac_gemm(to_frac(av), to_frac(bv))
+    got = oracle.gemm_operands(ops)
+    for m in range(M):
+        for n in range(N):
+            # fp16 products are exact in fp64 and the sums of K of them round at most K times
+            bound = sum(abs(Fraction(float(av[m, k])) * Fraction(float(bv[n, k]))) for k in range(K))
+            assert abs(Fraction(got[m, n]) - exact[m][n]) <= bound * K * Fraction(1, 2 ** 52)
+
+
+def test_fp16_identity_operand():
+    K = 64
+    b = inputs.fp16_rows(48, K, inputs._gen(3))
+    eye = np.where(np.eye(K, dtype=bool), np.uint16(0x3C00), np.uint16(0))   # 0x3C00 is 1.0
+    assert np.array_equal(oracle.gemm_fp16(eye, b), oracle.decode_fp16(b).T)
+
+
+def test_fp16_recipe():
+    ops = inputs.make_operands("fp16", 64, 32, 256, seed=4)
+    v = ops.a.view(np.float16).astype(np.float64)
+    assert ops.a.dtype == np.uint16 and ops.a.shape == (64, 256)
+    assert abs(v.std() * np.sqrt(256) - 1.0) < 0.1       # N(0,1)/sqrt(K)
+    again = inputs.make_operands("fp16", 64, 32, 256, seed=4)
+    assert np.array_equal(ops.a, again.a) and np.array_equal(ops.b, again.b)
