@@ -51,7 +51,7 @@ DEFAULT_WORKLOAD = "int8_16x7168x4096"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # nominal dense tensor-rate ratios to bf16 (2.25 PF): fp8 4.5, fp4 13.5
-DTYPE_RATIO = {"bf16": 1.0, "e4m3": 2.0, "e2m1": 6.0}
+DTYPE_RATIO = {"bf16": 1.0, "fp16": 1.0, "e4m3": 2.0, "e2m1": 6.0}
 B_DEFAULT_FLAGS = False  # --b-default: time gemm_run without GP_RUN_B_CONSTANT
 
 
@@ -71,7 +71,7 @@ def algorithmic_bytes(dtype: str, M: int, N: int, K: int) -> int:
         return M * K + N * K + M * N * 4
     if dtype == "e4m3":
         return M * K + N * K + M * N * 2 + (M + N) * 4
-    if dtype == "bf16":
+    if dtype in ("bf16", "fp16"):
         return 2 * M * K + 2 * N * K + 2 * M * N
     if dtype == "e2m1":
         return M * K // 2 + N * K // 2 + M * N * 2 + (M + N) * (K // 32)
@@ -228,10 +228,11 @@ class Problem:
         self.A = [A] + [A.clone() for _ in range(copies - 1)]
         self.sa = self.host_sa.to(device) if self.host_sa is not None else None
         self.sb = sb if self.dtype == "e4m3" else None
-        cdt = torch.int32 if self.dtype == "int8" else torch.bfloat16
+        cdt = torch.int32 if self.dtype == "int8" else (torch.float16 if self.dtype == "fp16" else torch.bfloat16)
         self.C = [torch.empty((self.M, self.N), dtype=cdt, device=device) for _ in range(min(copies, 4))]
-        self.c_dtype = "int32" if self.dtype == "int8" else "bf16"
-        self.mode = {"int8": "none", "bf16": "none", "e4m3": "rowcol_f32", "e2m1": "block32_ue8m0"}[self.dtype]
+        self.c_dtype = {"int8": "int32", "fp16": "fp16"}.get(self.dtype, "bf16")
+        self.mode = {"int8": "none", "bf16": "none", "fp16": "none", "e4m3": "rowcol_f32",
+                     "e2m1": "block32_ue8m0"}[self.dtype]
         self.flops = 2 * self.M * self.N * self.K
         self.bytes = algorithmic_bytes(self.dtype, self.M, self.N, self.K)
         # the packed weights are complete (synchronised above) and never
@@ -423,7 +424,7 @@ def run_ours(args):
     if not args.no_others:
         others = {}
         from dense_gemm_preshuffle_gb300 import inputs
-        for name in inputs.WORKLOADS:
+        for name in inputs.ALL_WORKLOADS:
             if name == args.workload:
                 continue
             try:

@@ -28,7 +28,7 @@ _LIB_PATH = os.path.join(_HERE, "_lib", "libgemm_preshuffle.so")
 _HEADER = os.path.join(os.path.dirname(_HERE), "include", "gemm_preshuffle.h")
 
 GP_OK = 0
-DTYPES = {"bf16": 0, "e4m3": 1, "int8": 2, "e2m1": 3, "int32": 4}
+DTYPES = {"bf16": 0, "e4m3": 1, "int8": 2, "e2m1": 3, "int32": 4, "fp16": 5}
 SCALE_MODES = {"none": 0, "rowcol_f32": 1, "block32_ue8m0": 2}
 GP_RUN_DEFAULT = 0
 GP_RUN_B_CONSTANT = 1
@@ -172,8 +172,10 @@ def preshuffle_b(B, dtype, B_scales=None, stream=None):
 
 
 def matmul(A, B_packed, dtype, N: int, K: int, scale_a=None, scale_b=None, out=None, stream=None,
-           b_constant: bool = False, epilogue: str = "none", bias=None):
-    """C = A . B^T with B packed; returns bf16 [M, N] (int32 for int8).
+           b_constant: bool = False, epilogue: str = "none", bias=None, out_dtype: Optional[str] = None):
+    """C = A . B^T with B packed; returns [M, N] in out_dtype ("bf16" or
+    "fp16"; default fp16 for fp16 operands, bf16 for the other float types),
+    int32 for int8.
 
     epilogue: "none", "bias", "bias_relu", "bias_silu" or "bias_gelu", with
     bias an fp32 [N] device tensor for all but "none".
@@ -182,14 +184,17 @@ def matmul(A, B_packed, dtype, N: int, K: int, scale_a=None, scale_b=None, out=N
     import torch
     d = _dt(dtype)
     M = A.shape[0]
+    if out_dtype is None:
+        out_dtype = "fp16" if d == DTYPES["fp16"] else "bf16"
+    fdt = torch.float16 if out_dtype == "fp16" else torch.bfloat16
     if d == DTYPES["int8"]:
         c_dtype, mode, tdt = "int32", "none", torch.int32
     elif d == DTYPES["e2m1"]:
-        c_dtype, mode, tdt = "bf16", "block32_ue8m0", torch.bfloat16
+        c_dtype, mode, tdt = out_dtype, "block32_ue8m0", fdt
     elif scale_a is not None:
-        c_dtype, mode, tdt = "bf16", "rowcol_f32", torch.bfloat16
+        c_dtype, mode, tdt = out_dtype, "rowcol_f32", fdt
     else:
-        c_dtype, mode, tdt = "bf16", "none", torch.bfloat16
+        c_dtype, mode, tdt = out_dtype, "none", fdt
     if out is None:
         out = torch.empty((M, N), dtype=tdt, device=A.device)
     gemm_run_ex(A, B_packed, d, M, N, K, mode, scale_a, scale_b, epilogue, bias, out, c_dtype,

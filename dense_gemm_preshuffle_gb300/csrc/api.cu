@@ -11,6 +11,7 @@
 // __device__ variable) and a cached SM count.
 #include <atomic>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -69,6 +70,7 @@ int device_info(DeviceInfo** out) {
 int elem_bits(int dtype) {
   switch (dtype) {
     case GP_BF16: return 16;
+    case GP_FP16: return 16;
     case GP_E4M3: return 8;
     case GP_INT8: return 8;
     case GP_E2M1: return 4;
@@ -124,12 +126,15 @@ std::atomic<int> g_debug_skip_load{0};
 
 using namespace gp;
 
-// C[m, n] = bf16(act(bias[n])): the fused epilogue of an empty (K = 0) sum.
-__global__ void epilogue_broadcast_kernel(const float* __restrict__ bias, int act, int64_t M, int64_t N,
-                                          __nv_bfloat16* __restrict__ C) {
+// C[m, n] = act(bias[n]) rounded to bf16 or fp16: the fused epilogue of an
+// empty (K = 0) sum.
+__global__ void epilogue_broadcast_kernel(const float* __restrict__ bias, int act, int64_t M, int64_t N, int out_f16,
+                                          uint16_t* __restrict__ C) {
   const int64_t total = M * N;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x)
-    C[i] = __float2bfloat16_rn(epi_act(bias[i % N], act));
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const float v = epi_act(bias[i % N], act);
+    C[i] = out_f16 ? __half_as_ushort(__float2half_rn(v)) : __bfloat16_as_ushort(__float2bfloat16_rn(v));
+  }
 }
 
 extern "C" {
@@ -204,15 +209,17 @@ int gemm_run_ex(const void* A, const void* B_packed, int dtype, int64_t M, int64
   const int b_constant = (flags & GP_RUN_B_CONSTANT) ? 1 : 0;
   if (epilogue < GP_EPI_NONE || epilogue > GP_EPI_BIAS_GELU) return GP_ERR_INVALID_ARG;
   if ((epilogue == GP_EPI_NONE) != (bias == nullptr)) return GP_ERR_INVALID_ARG;
-  if (epilogue != GP_EPI_NONE && c_dtype != GP_BF16) return GP_ERR_UNSUPPORTED;  // float outputs only
+  const bool float_out = c_dtype == GP_BF16 || c_dtype == GP_FP16;
+  if (epilogue != GP_EPI_NONE && !float_out) return GP_ERR_UNSUPPORTED;  // float outputs only
   // ---- combination
-  const bool combo_ok = (dtype == GP_BF16 && scale_mode == GP_SCALE_NONE && c_dtype == GP_BF16) ||
-                        (dtype == GP_E4M3 && scale_mode == GP_SCALE_ROWCOL_F32 && c_dtype == GP_BF16) ||
-                        (dtype == GP_E4M3 && scale_mode == GP_SCALE_NONE && c_dtype == GP_BF16) ||
-                        (dtype == GP_E2M1 && scale_mode == GP_SCALE_BLOCK32_UE8M0 && c_dtype == GP_BF16) ||
+  const bool combo_ok = (dtype == GP_BF16 && scale_mode == GP_SCALE_NONE && float_out) ||
+                        (dtype == GP_FP16 && scale_mode == GP_SCALE_NONE && float_out) ||
+                        (dtype == GP_E4M3 && scale_mode == GP_SCALE_ROWCOL_F32 && float_out) ||
+                        (dtype == GP_E4M3 && scale_mode == GP_SCALE_NONE && float_out) ||
+                        (dtype == GP_E2M1 && scale_mode == GP_SCALE_BLOCK32_UE8M0 && float_out) ||
                         (dtype == GP_INT8 && scale_mode == GP_SCALE_NONE && c_dtype == GP_INT32);
   if (elem_bits(dtype) == 0 || scale_mode < GP_SCALE_NONE || scale_mode > GP_SCALE_BLOCK32_UE8M0 ||
-      (c_dtype != GP_BF16 && c_dtype != GP_INT32))
+      (!float_out && c_dtype != GP_INT32))
     return GP_ERR_INVALID_ARG;
   if (!combo_ok) return GP_ERR_UNSUPPORTED;
   // ---- shapes
@@ -247,7 +254,7 @@ int gemm_run_ex(const void* A, const void* B_packed, int dtype, int64_t M, int64
     const int64_t total = M * N;
     const int blocks = (int)((total + 255) / 256 < 65536 ? (total + 255) / 256 : 65536);
     epilogue_broadcast_kernel<<<blocks, 256, 0, st>>>(static_cast<const float*>(bias), act, M, N,
-                                                      static_cast<__nv_bfloat16*>(C));
+                                                      c_dtype == GP_FP16 ? 1 : 0, static_cast<uint16_t*>(C));
     return cudaGetLastError() == cudaSuccess ? GP_OK : GP_ERR_CUDA;
   }
 
@@ -295,12 +302,18 @@ int gemm_run_ex(const void* A, const void* B_packed, int dtype, int64_t M, int64
   // still gives every SM several tiles, or when K is split over a cluster
   // (few tiles); the E2M1 kernel uses 128.
   const int split = dtype == GP_E2M1 ? 1 : splitk_choice(M, N, kb / 128, d->num_sms);
-  const int bm = dtype == GP_E2M1 ? 128 : (split > 1 ? 256 : tc_tile_m(M, N, d->num_sms));
+  int bm = 128, bn = 256;
+  if (dtype != GP_E2M1) {
+    if (split > 1)
+      bm = 256;
+    else
+      tc_tile_choice(M, N, d->num_sms, &bm, &bn);
+  }
   CUtensorMap tmA, tmC;
   if ((rc = encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, (uint64_t)kb, (uint64_t)M, (uint64_t)kb, 128,
                       (uint32_t)bm, CU_TENSOR_MAP_SWIZZLE_128B)) != GP_OK)
     return rc;
-  if ((rc = encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, C, (uint64_t)N, (uint64_t)M, (uint64_t)N * 2, 64, 32,
+  if ((rc = encode_2d(&tmC, c_dtype == GP_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, C, (uint64_t)N, (uint64_t)M, (uint64_t)N * 2, 64, 32,
                       CU_TENSOR_MAP_SWIZZLE_128B)) != GP_OK)
     return rc;
   TcParams p{};
@@ -314,6 +327,7 @@ int gemm_run_ex(const void* A, const void* B_packed, int dtype, int64_t M, int64
   p.debug_skip_load = g_debug_skip_load.exchange(0);
   p.b_constant = b_constant;
   p.bias = static_cast<const float*>(bias);
+  p.out_f16 = c_dtype == GP_FP16 ? 1 : 0;
   p.act = epilogue == GP_EPI_BIAS_RELU ? EPI_ACT_RELU
           : epilogue == GP_EPI_BIAS_SILU ? EPI_ACT_SILU
           : epilogue == GP_EPI_BIAS_GELU ? EPI_ACT_GELU
@@ -328,10 +342,9 @@ int gemm_run_ex(const void* A, const void* B_packed, int dtype, int64_t M, int64
     p.sfa = static_cast<const uint8_t*>(scale_a);
     return mxf4_gemm_launch(tmA, tmC, p, d->num_sms, st);
   }
-  if (split > 1) return splitk_gemm_launch(dtype == GP_BF16 ? 0 : 1, split, tmA, tmC, p, st);
-  const int64_t tiles_256 = ((M + 127) / 128) * (N / 256);
-  const int bn = bm == 256 ? 256 : ((N % 256 == 0 && tiles_256 >= d->num_sms) ? 256 : 128);
-  return tc_gemm_launch(dtype == GP_BF16 ? 0 : 1, bm, bn, tmA, tmC, p, d->num_sms, st);
+  const int kind = dtype == GP_BF16 ? 0 : dtype == GP_E4M3 ? 1 : 2;  // 2: fp16
+  if (split > 1) return splitk_gemm_launch(kind, split, tmA, tmC, p, st);
+  return tc_gemm_launch(kind, bm, bn, tmA, tmC, p, d->num_sms, st);
 }
 
 int gemm_last_device_status(void* stream) {

@@ -7,7 +7,7 @@
 //                                       GELU 0.5 v (1 + erf(v / sqrt 2)),
 //                                       erf by a published rational
 //                                       approximation (|error| <= 1.5e-7)
-// then rounded to bf16 (RNE) in pairs.
+// then rounded to bf16 or fp16 (RNE) in pairs.
 #pragma once
 #include <cstdint>
 
@@ -45,9 +45,10 @@ __device__ __forceinline__ float epi_act(float x, int act) {
 }
 
 // v: the row's 32 fp32 values; sb, bias: the same 32 columns (16-byte
-// aligned) or null; sa: the row scale (1 when absent).
+// aligned) or null; sa: the row scale (1 when absent); out_f16: round to
+// IEEE binary16 instead of bf16 (both RNE).
 __device__ __forceinline__ void epi_row32(float (&v)[32], float sa, const float* sb, const float* bias, int act,
-                                          uint32_t (&pk)[16]) {
+                                          bool out_f16, uint32_t (&pk)[16]) {
   if (sb != nullptr) {
     const float4* sb4 = reinterpret_cast<const float4*>(sb);
 #pragma unroll
@@ -74,8 +75,13 @@ __device__ __forceinline__ void epi_row32(float (&v)[32], float sa, const float*
       for (int e = 0; e < 32; ++e) v[e] = epi_act(v[e], act);
     }
   }
+  if (out_f16) {
 #pragma unroll
-  for (int q = 0; q < 16; ++q) pk[q] = pack_bf16x2(v[2 * q], v[2 * q + 1]);
+    for (int q = 0; q < 16; ++q) pk[q] = pack_f16x2(v[2 * q], v[2 * q + 1]);
+  } else {
+#pragma unroll
+    for (int q = 0; q < 16; ++q) pk[q] = pack_bf16x2(v[2 * q], v[2 * q + 1]);
+  }
 }
 
 }  // namespace gp

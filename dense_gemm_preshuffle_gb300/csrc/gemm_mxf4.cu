@@ -318,7 +318,7 @@ __global__ void __launch_bounds__(F4_THREADS, 1)
 #pragma unroll
           for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]);
           uint32_t pk[16];
-          epi_row32(v, 1.0f, nullptr, p.bias != nullptr ? p.bias + n0 + h * 32 : nullptr, p.act, pk);
+          epi_row32(v, 1.0f, nullptr, p.bias != nullptr ? p.bias + n0 + h * 32 : nullptr, p.act, p.out_f16 != 0, pk);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const int chunk = h * 4 + q;

@@ -214,7 +214,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t fmt = (KIND == 0) ? 1u : 0u;
+      constexpr uint32_t fmt = (KIND == 0) ? 1u : 0u;  // bf16; fp16 (KIND 2) and e4m3 (KIND 1) are format 0
       constexpr uint32_t idesc = idesc_dense(fmt, fmt, 128, SK_BN);
       bool ok = true;
       for (int i = 0; i < ks; ++i) {
@@ -334,7 +334,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
           }
           uint32_t pk[16];
           epi_row32(v, sa, p.sb != nullptr ? p.sb + n0 + h * 32 : nullptr,
-                    p.bias != nullptr ? p.bias + n0 + h * 32 : nullptr, p.act, pk);
+                    p.bias != nullptr ? p.bias + n0 + h * 32 : nullptr, p.act, p.out_f16 != 0, pk);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const int chunk = h * 4 + q;
@@ -415,8 +415,14 @@ int splitk_gemm_launch(int kind, int split, const CUtensorMap& tmA, const CUtens
   p.tiles_m = (p.M + SK_BM - 1) / SK_BM;
   p.tiles_n = p.N / SK_BN;
   p.num_tiles = p.tiles_m * p.tiles_n;
-  if (split == 4) return kind == 0 ? launch_splitk<0, 4>(tmA, tmC, p, stream) : launch_splitk<1, 4>(tmA, tmC, p, stream);
-  if (split == 2) return kind == 0 ? launch_splitk<0, 2>(tmA, tmC, p, stream) : launch_splitk<1, 2>(tmA, tmC, p, stream);
+  if (split == 4)
+    return kind == 0 ? launch_splitk<0, 4>(tmA, tmC, p, stream)
+           : kind == 1 ? launch_splitk<1, 4>(tmA, tmC, p, stream)
+                       : launch_splitk<2, 4>(tmA, tmC, p, stream);
+  if (split == 2)
+    return kind == 0 ? launch_splitk<0, 2>(tmA, tmC, p, stream)
+           : kind == 1 ? launch_splitk<1, 2>(tmA, tmC, p, stream)
+                       : launch_splitk<2, 2>(tmA, tmC, p, stream);
   return GP_ERR_UNSUPPORTED;
 }
 

@@ -40,9 +40,13 @@
 // instead of 2 x 48 KiB.  The cost is a single-buffered 512-column
 // accumulator.
 //
-// KIND: 0 = bf16 x bf16 (kind::f16), 1 = e4m3 x e4m3 (kind::f8f6f4).  One K
+// KIND: 0 = bf16 x bf16 (kind::f16), 1 = e4m3 x e4m3 (kind::f8f6f4),
+// 2 = fp16 x fp16 (kind::f16 with the f16 operand format).  One K
 // step moves 128 bytes of each row (64 bf16 or 128 e4m3 elements), and one
 // MMA instruction consumes 32 bytes of K.
+#include <cstdlib>
+#include <cstring>
+
 #include "kernels.h"
 #include "epilogue.cuh"
 #include "ptx.cuh"
@@ -211,7 +215,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t fmt = (KIND == 0) ? 1u /*bf16*/ : 0u /*e4m3*/;
+      constexpr uint32_t fmt = (KIND == 0) ? 1u /*bf16*/ : 0u /*fp16 (kind::f16) or e4m3 (kind::f8f6f4)*/;
       constexpr uint32_t idesc = idesc_dense(fmt, fmt, 128, BN);
       int s = 0;
       uint32_t ph = 0;
@@ -292,7 +296,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]);
             uint32_t pk[16];
             epi_row32(v, sa, p.sb != nullptr ? p.sb + n0 + h * 32 : nullptr,
-                      p.bias != nullptr ? p.bias + n0 + h * 32 : nullptr, p.act, pk);
+                      p.bias != nullptr ? p.bias + n0 + h * 32 : nullptr, p.act, p.out_f16 != 0, pk);
             // 128-byte swizzle: 16-byte chunk j of row `lane` goes to slot j ^ (lane % 8)
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
@@ -354,11 +358,49 @@ static int launch_tc(const CUtensorMap& tmA, const CUtensorMap& tmC, const TcPar
   return cudaGetLastError() == cudaSuccess ? GP_OK : GP_ERR_CUDA;
 }
 
-int tc_tile_m(int64_t M, int64_t N, int num_sms) {
-  // 256-row tiles when there are enough of them to fill every SM
-  // (at least 4 tiles per SM), else 128.
-  const int64_t tiles = ((M + 255) / 256) * (N / 256);
-  return (N % 256 == 0 && tiles >= 4 * (int64_t)num_sms) ? 256 : 128;
+void tc_tile_choice(int64_t M, int64_t N, int num_sms, int* bm, int* bn) {
+  // The tile shape with the least estimated time: waves (ceil(tiles / SMs))
+  // x tile area / the shape's relative throughput, measured on GB300 with
+  // full waves (FP8 8192^3): 256 x 256 1.0, 128 x 256 0.90, 128 x 128 0.645
+  // (smaller tiles bring fewer flops per operand byte, and each SM takes in
+  // operands at ~110 GB/s).  Ties go to the larger tile.  GP_TC_TILE
+  // (256x256, 128x256 or 128x128) overrides, for sweeps, where N allows.
+  static const int forced = [] {
+    const char* e = std::getenv("GP_TC_TILE");
+    if (e == nullptr) return 0;
+    if (std::strcmp(e, "256x256") == 0) return 1;
+    if (std::strcmp(e, "128x256") == 0) return 2;
+    if (std::strcmp(e, "128x128") == 0) return 3;
+    return 0;
+  }();
+  if (forced == 1 && N % 256 == 0) {
+    *bm = 256, *bn = 256;
+    return;
+  }
+  if (forced == 2 && N % 256 == 0) {
+    *bm = 128, *bn = 256;
+    return;
+  }
+  if (forced == 3) {
+    *bm = 128, *bn = 128;
+    return;
+  }
+  struct Shape {
+    int bm, bn;
+    double rate;
+  };
+  const Shape shapes[3] = {{256, 256, 1.0}, {128, 256, 0.90}, {128, 128, 0.645}};
+  double best = 0.0;
+  for (const Shape& t : shapes) {
+    if (N % t.bn != 0) continue;
+    const int64_t tiles = ((M + t.bm - 1) / t.bm) * (N / t.bn);
+    const int64_t waves = (tiles + num_sms - 1) / num_sms;
+    const double cost = (double)waves * t.bm * t.bn / t.rate;
+    if (best == 0.0 || cost < best * (1.0 - 1e-9)) {
+      best = cost;
+      *bm = t.bm, *bn = t.bn;
+    }
+  }
 }
 
 int tc_gemm_launch(int kind, int bm, int bn, const CUtensorMap& tmA, const CUtensorMap& tmC, TcParams p, int num_sms,
@@ -369,14 +411,23 @@ int tc_gemm_launch(int kind, int bm, int bn, const CUtensorMap& tmA, const CUten
   const int grid = p.num_tiles < num_sms ? p.num_tiles : num_sms;
   if (bm == 256) {
     if (bn != 256) return GP_ERR_UNSUPPORTED;
-    return kind == 0 ? launch_tc<0, 256, 256, 3>(tmA, tmC, p, grid, stream)
-                     : launch_tc<1, 256, 256, 3>(tmA, tmC, p, grid, stream);
+    switch (kind) {
+      case 0: return launch_tc<0, 256, 256, 3>(tmA, tmC, p, grid, stream);
+      case 1: return launch_tc<1, 256, 256, 3>(tmA, tmC, p, grid, stream);
+      default: return launch_tc<2, 256, 256, 3>(tmA, tmC, p, grid, stream);
+    }
   }
-  if (kind == 0)
-    return bn == 256 ? launch_tc<0, 128, 256, 4>(tmA, tmC, p, grid, stream)
-                     : launch_tc<0, 128, 128, 6>(tmA, tmC, p, grid, stream);
-  return bn == 256 ? launch_tc<1, 128, 256, 4>(tmA, tmC, p, grid, stream)
-                   : launch_tc<1, 128, 128, 6>(tmA, tmC, p, grid, stream);
+  switch (kind) {
+    case 0:
+      return bn == 256 ? launch_tc<0, 128, 256, 4>(tmA, tmC, p, grid, stream)
+                       : launch_tc<0, 128, 128, 6>(tmA, tmC, p, grid, stream);
+    case 1:
+      return bn == 256 ? launch_tc<1, 128, 256, 4>(tmA, tmC, p, grid, stream)
+                       : launch_tc<1, 128, 128, 6>(tmA, tmC, p, grid, stream);
+    default:
+      return bn == 256 ? launch_tc<2, 128, 256, 4>(tmA, tmC, p, grid, stream)
+                       : launch_tc<2, 128, 128, 6>(tmA, tmC, p, grid, stream);
+  }
 }
 
 }  // namespace gp

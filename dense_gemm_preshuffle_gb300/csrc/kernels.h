@@ -16,6 +16,7 @@ struct TcParams {
   const float* sb;        // fp32 [N] column scales or null
   const float* bias;      // fp32 [N] epilogue bias or null (no epilogue)
   int act;                // epilogue activation after the bias (EpiAct)
+  int out_f16;            // 1: C is IEEE fp16, 0: bf16
   uint32_t* status;       // device status word
   uint64_t wait_limit_ns; // bounded-wait limit
   int M, N, K;            // K in elements
@@ -37,7 +38,7 @@ struct I8Params {
   int b_constant;         // 1: B may be read before the previous kernel on the stream completes
 };
 
-int tc_tile_m(int64_t M, int64_t N, int num_sms);
+void tc_tile_choice(int64_t M, int64_t N, int num_sms, int* bm, int* bn);
 int tc_gemm_launch(int kind, int bm, int bn, const CUtensorMap& tmA, const CUtensorMap& tmC, TcParams p, int num_sms,
                    cudaStream_t stream);
 int splitk_choice(int64_t M, int64_t N, int64_t ktiles, int num_sms);

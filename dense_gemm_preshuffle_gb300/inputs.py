@@ -64,6 +64,15 @@ WORKLOADS = {
     "mxfp4_4096x8192x8192": Workload("mxfp4_4096x8192x8192", E2M1, 4096, 8192, 8192, 4),
 }
 
+# Further shapes, timed beside the five: the GEMM Optimization Guide's
+# worked example (section 14: 5120 x 5120 x 8320 FP8 with per-token scales),
+# and FP16 operands at the BF16 shape.
+EXTRA_WORKLOADS = {
+    "fp8_5120x5120x8320": Workload("fp8_5120x5120x8320", E4M3, 5120, 5120, 8320, 5),
+    "fp16_512x4096x4096": Workload("fp16_512x4096x4096", FP16, 512, 4096, 4096, 6),
+}
+ALL_WORKLOADS = {**WORKLOADS, **EXTRA_WORKLOADS}
+
 
 @dataclass
 class Operands:
@@ -205,5 +214,5 @@ def make_operands(dtype: str, M: int, N: int, K: int, seed: int) -> Operands:
 
 
 def workload_operands(name: str) -> Operands:
-    w = WORKLOADS[name]
+    w = ALL_WORKLOADS[name]
     return make_operands(w.dtype, w.M, w.N, w.K, w.seed)

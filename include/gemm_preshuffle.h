@@ -55,7 +55,8 @@ typedef enum gp_dtype {
   GP_E4M3 = 1,
   GP_INT8 = 2,
   GP_E2M1 = 3,
-  GP_INT32 = 4
+  GP_INT32 = 4,
+  GP_FP16 = 5                 /* IEEE binary16 */
 } gp_dtype;
 
 /* How operand scales enter the product. */
@@ -75,7 +76,7 @@ typedef enum gp_scale_mode {
  * scales for E2M1, with no padding.
  *
  * Shape rules: N % 128 == 0 and K*element_bits/8 % 128 == 0.  For the
- * element types that means K % 128 (E4M3, INT8), K % 64 (BF16) and K % 256
+ * element types that means K % 128 (E4M3, INT8), K % 64 (BF16, FP16) and K % 256
  * (E2M1).  Returns GP_ERR_SHAPE otherwise.  Host-only call.
  */
 int gemm_packed_b_bytes(int dtype, int64_t N, int64_t K, size_t* bytes_out);
@@ -128,18 +129,22 @@ int gemm_unpack_b(const void* B_packed, int dtype, int64_t N, int64_t K, void* B
  *            in B_packed.
  * C        : device, [M, N] row-major in `c_dtype`, written entirely.
  *
- * Supported (dtype, scale_mode, c_dtype) combinations:
- *   (GP_BF16, GP_SCALE_NONE,          GP_BF16)   fp32 accumulation in TMEM
- *   (GP_E4M3, GP_SCALE_ROWCOL_F32,    GP_BF16)   fp32 accumulation, scales in epilogue
- *   (GP_E4M3, GP_SCALE_NONE,          GP_BF16)
- *   (GP_E2M1, GP_SCALE_BLOCK32_UE8M0, GP_BF16)   block scales applied inside the MMA
+ * Supported (dtype, scale_mode, c_dtype) combinations, where FOUT is
+ * GP_BF16 or GP_FP16:
+ *   (GP_BF16, GP_SCALE_NONE,          FOUT)      fp32 accumulation in TMEM
+ *   (GP_FP16, GP_SCALE_NONE,          FOUT)      fp32 accumulation in TMEM
+ *   (GP_E4M3, GP_SCALE_ROWCOL_F32,    FOUT)      fp32 accumulation, scales in epilogue
+ *   (GP_E4M3, GP_SCALE_NONE,          FOUT)
+ *   (GP_E2M1, GP_SCALE_BLOCK32_UE8M0, FOUT)      block scales applied inside the MMA
  *   (GP_INT8, GP_SCALE_NONE,          GP_INT32)  exact integer result
  * Other combinations return GP_ERR_UNSUPPORTED.
  *
  * Shape rules: M >= 1 (any value), N and K as for gemm_packed_b_bytes, and
- * M, N, K < 2^31.  E2M1 also needs N % 256 == 0 (its tiles are 256 wide).  For INT8 the exact result must fit int32, which holds for
- * every input when K <= 131072.
- * Float outputs are rounded to nearest-even from the fp32 value.
+ * M, N, K < 2^31.  E2M1 also needs N % 256 == 0 (its tiles are 256 wide).
+ * For INT8 the exact result must fit int32, which holds for every input
+ * when K <= 131072.
+ * Float outputs are rounded to nearest-even from the fp32 value (an fp16
+ * output saturates to infinity beyond 65504, as IEEE rounding does).
  * The call launches one kernel and allocates no memory.  K == 0 writes
  * zeros to C with an async memset.  M == 0 or N == 0 is a no-op.
  */
@@ -178,9 +183,9 @@ typedef enum gp_run_flags {
  * gemm_run with a fused epilogue and flags; gemm_run is gemm_run_ex with
  * GP_EPI_NONE, bias NULL and GP_RUN_DEFAULT.
  *
- * epilogue : a gp_epilogue.  Any value but GP_EPI_NONE needs c_dtype
- *            GP_BF16 (else GP_ERR_UNSUPPORTED; the INT8 product keeps its
- *            exact int32 output).
+ * epilogue : a gp_epilogue.  Any value but GP_EPI_NONE needs a float
+ *            c_dtype (GP_BF16 or GP_FP16; else GP_ERR_UNSUPPORTED: the
+ *            INT8 product keeps its exact int32 output).
  * bias     : device, fp32 [N], 16-byte aligned; required for every epilogue
  *            but GP_EPI_NONE, and NULL with it (else GP_ERR_INVALID_ARG).
  * flags    : a bitwise OR of gp_run_flags.  Unknown bits return

@@ -36,6 +36,7 @@ def test_status_strings(lib):
     ("e2m1", 8192, 8192, 8192 * 4096 + 8192 * 256),
     ("bf16", 128, 64, 128 * 128),
     ("e4m3", 0, 0, 0),
+    ("fp16", 256, 64, 256 * 64 * 2),
 ])
 def test_packed_bytes(lib, dtype, N, K, expect):
     assert gp.gemm_packed_b_bytes(dtype, N, K) == expect
@@ -62,6 +63,8 @@ FAKE = 0x10000  # an aligned, never-dereferenced address: validation fails befor
     (dict(dtype="int8", scale_mode="none", c_dtype="bf16"), 2),
     (dict(dtype="bf16", scale_mode="rowcol_f32", c_dtype="bf16"), 2),
     (dict(dtype="e2m1", scale_mode="none", c_dtype="bf16"), 2),
+    (dict(dtype="fp16", scale_mode="rowcol_f32", c_dtype="fp16", scale_a=FAKE, scale_b=FAKE), 2),
+    (dict(dtype="int8", scale_mode="none", c_dtype="fp16"), 2),
     # shape rules
     (dict(N=100), 3),
     (dict(K=96), 3),

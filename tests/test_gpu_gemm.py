@@ -72,7 +72,7 @@ def check(ops, C, rows=None):
 # ---------------------------------------------------------------- packing
 
 @pytest.mark.parametrize("dtype,N,K", [("e4m3", 256, 512), ("int8", 384, 1024), ("bf16", 128, 192),
-                                       ("e2m1", 256, 1024), ("int8", 7168, 4096)])
+                                       ("e2m1", 256, 1024), ("int8", 7168, 4096), ("fp16", 256, 320)])
 def test_pack_matches_oracle_layout_and_roundtrips(dtype, N, K):
     ops = inputs.make_operands(dtype, 1, N, K, seed=123)
     _, B, _, sb = dev(ops)
@@ -97,6 +97,7 @@ SMALL = [
     ("int8", 1, 128, 128), ("int8", 37, 256, 384), ("int8", 16, 384, 256), ("int8", 100, 1152, 1280),
     ("int8", 16, 7168, 4096),
     ("e2m1", 1, 256, 256), ("e2m1", 200, 512, 512), ("e2m1", 129, 256, 1024), ("e2m1", 300, 768, 2048),
+    ("fp16", 1, 128, 64), ("fp16", 257, 384, 512), ("fp16", 64, 256, 4096), ("fp16", 700, 640, 320),
 ]
 
 
@@ -148,7 +149,8 @@ def test_workload_full_compare(name):
     check(ops, gpu_gemm(ops))
 
 
-@pytest.mark.parametrize("name", ["fp8_8192x8192x8192", "mxfp4_4096x8192x8192"])
+@pytest.mark.parametrize("name", ["fp8_8192x8192x8192", "mxfp4_4096x8192x8192", "fp8_5120x5120x8320",
+                                  "fp16_512x4096x4096"])
 def test_workload_sampled_rows(name):
     ops = inputs.workload_operands(name)
     C = gpu_gemm(ops)
@@ -157,7 +159,7 @@ def test_workload_sampled_rows(name):
     assert torch.isfinite(C.float()).all()
 
 
-@pytest.mark.parametrize("dtype", ["e4m3", "bf16"])
+@pytest.mark.parametrize("dtype", ["e4m3", "bf16", "fp16"])
 def test_tile256_path_ragged(dtype):
     # enough 256 x 256 tiles (17 x 38 >= 4 per SM) to take the 256-row tile
     # path, with a ragged last row band
@@ -167,7 +169,8 @@ def test_tile256_path_ragged(dtype):
     check(ops, C, rows=np.unique(rows))
 
 
-@pytest.mark.parametrize("dtype,M,N,K", [("bf16", 400, 4096, 8192), ("e4m3", 300, 8192, 8192)])
+@pytest.mark.parametrize("dtype,M,N,K", [("bf16", 400, 4096, 8192), ("e4m3", 300, 8192, 8192),
+                                         ("fp16", 400, 4096, 8192)])
 def test_split_k_cluster_path_ragged(dtype, M, N, K):
     # few 256 x 256 tiles and a long K: K is split across a 4- (bf16) or
     # 2-CTA (e4m3) cluster and reduced over distributed shared memory
@@ -349,3 +352,45 @@ def test_fused_epilogue_empty_sum(epilogue):
     torch.cuda.synchronize()
     ref = oracle.apply_epilogue(np.zeros((M, N)), epilogue, bias.astype(np.float64))
     assert oracle.max_rel_err(as_host(C), ref) <= TOL
+
+
+
+# ---------------------------------------------------------------- fp16 output
+
+@pytest.mark.parametrize("dtype,M,N,K", [("fp16", 300, 512, 1024), ("bf16", 200, 384, 512), ("e4m3", 129, 256, 512),
+                                         ("e2m1", 200, 512, 512), ("fp16", 4173, 9728, 256)])
+def test_fp16_output(dtype, M, N, K):
+    """IEEE fp16 output (RNE from fp32) from every float path."""
+    ops = inputs.make_operands(dtype, M, N, K, seed=6000 + M + N + K)
+    A, B, sa, sb = dev(ops)
+    if dtype == "e2m1":
+        Bp = gp.preshuffle_b(B, "e2m1", B_scales=sb)
+        C = gp.matmul(A, Bp, "e2m1", N, K, scale_a=sa, out_dtype="fp16")
+    else:
+        Bp = gp.preshuffle_b(B, dtype)
+        C = gp.matmul(A, Bp, dtype, N, K, scale_a=sa, scale_b=sb, out_dtype="fp16")
+    torch.cuda.synchronize()
+    assert C.dtype == torch.float16 and gp.gemm_last_device_status() == 0
+    rows = None if M * N <= 1 << 21 else sample_rows(M, 24, seed=8)
+    check(ops, C, rows=rows)
+
+
+@pytest.mark.parametrize("epilogue", ["bias_gelu", "bias_silu"])
+def test_fp16_output_with_epilogue(epilogue):
+    ops = inputs.make_operands("fp16", 257, 384, 512, seed=71)
+    plain = oracle.gemm_operands(ops)
+    bias = (np.random.default_rng(3).standard_normal(384) * plain.std()).astype(np.float32)
+    A, B, _, _ = dev(ops)
+    Bp = gp.preshuffle_b(B, "fp16")
+    C = gp.matmul(A, Bp, "fp16", 384, 512, epilogue=epilogue, bias=torch.from_numpy(bias).cuda())
+    torch.cuda.synchronize()
+    ref = oracle.apply_epilogue(plain, epilogue, bias.astype(np.float64))
+    assert oracle.max_rel_err(as_host(C), ref) <= TOL
+    # K = 0 broadcast into fp16
+    Cz = torch.full((3, 384), 7.0, dtype=torch.float16, device="cuda")
+    dummy = torch.empty(16, dtype=torch.uint8, device="cuda")
+    gp.gemm_run_ex(dummy, dummy, "fp16", 3, 384, 0, "none", None, None, epilogue, torch.from_numpy(bias).cuda(), Cz,
+                   "fp16")
+    torch.cuda.synchronize()
+    assert oracle.max_rel_err(as_host(Cz), oracle.apply_epilogue(np.zeros((3, 384)), epilogue,
+                                                                 bias.astype(np.float64))) <= TOL
