@@ -37,6 +37,12 @@ Contents:
   ReLU max(x, 0); SiLU x / (1 + e^-x); GELU 0.5 x (1 + erf(x / sqrt 2)),
   the exact (erf) form.  The guide names the epilogues without formulas;
   these are the standard definitions.
+* The activation quantisers in front of the GEMM (the workloads' operand
+  recipes: per-token E4M3 with s = amax/448; MXFP4 with one UE8M0 exponent
+  per 32 K-elements, "GEMM Optimization Guide" section 8.2).  Encoders
+  written from the format definitions, round to nearest even, saturating.
+  The float steps that decide a code are taken in fp32 as the kernel takes
+  them: s = fp32(amax / 448) and x / s are IEEE fp32 divisions.
 * The float parity metric max |C - C_ref| / (|C_ref| + 1e-2).
 
 Parity pins (tests/test_oracle.py): brute force in exact rational arithmetic,
@@ -237,6 +243,79 @@ def gemm_operands(ops, rows: Optional[np.ndarray] = None, cols: Optional[np.ndar
 # ----------------------------------------------------------------------------
 # Output rounding model and the parity metric
 # ----------------------------------------------------------------------------
+
+# ----------------------------------------------------------------------------
+# Activation quantisers (encoders from the OCP format definitions)
+# ----------------------------------------------------------------------------
+
+def encode_e4m3(v: np.ndarray) -> np.ndarray:
+    """Values -> E4M3FN codes, round to nearest even, saturating at +-448
+    (no infinities; 448 is S.1111.110).  NaN -> 0x7F."""
+    v = np.asarray(v, dtype=np.float64)
+    a = np.abs(v)
+    sign = np.signbit(v).astype(np.uint8) << 7
+    f, ex = np.frexp(np.where(a > 0, a, 1.0))          # a = f * 2^ex, f in [0.5, 1)
+    e = np.maximum(ex.astype(np.int64) - 1, -6)         # floor(log2 a), subnormals below 2^-6
+    quantum = np.ldexp(1.0, e - 3)                       # 3 fraction bits
+    n = np.rint(a / quantum).astype(np.int64)            # exact quotient, ties to even
+    carry = n >= 16                                      # rounded up to the next binade
+    e = np.where(carry, e + 1, e)
+    n = np.where(carry, n // 2, n)
+    normal = n >= 8
+    code = np.where(normal, ((e + 7) << 3) | (n - 8), n)
+    code = np.where(a == 0, 0, code)
+    code = np.where((code > 0x7E) | (a >= 448.0), 0x7E, code)  # satfinite
+    code = code.astype(np.uint8) | sign
+    return np.where(np.isnan(v), np.uint8(0x7F), code)
+
+
+def encode_e2m1(v: np.ndarray) -> np.ndarray:
+    """Values -> E2M1 codes (4-bit, uint8), round to nearest even on the grid
+    {0, .5, 1, 1.5, 2, 3, 4, 6}, saturating at +-6."""
+    v = np.asarray(v, dtype=np.float64)
+    a = np.abs(v)
+    sign = np.signbit(v).astype(np.uint8) << 3
+    # spacing 0.5 below 2, 1 in [2, 4), 2 from 4
+    quantum = np.where(a < 2.0, 0.5, np.where(a < 4.0, 1.0, 2.0))
+    n = np.rint(a / quantum).astype(np.int64)
+    val = np.minimum(n * quantum, 6.0)                   # a tie that crosses a binade edge lands on it
+    code = np.select([val < 2.0, val < 4.0], [(val * 2).astype(np.int64), (val + 2).astype(np.int64)],
+                     (val / 2 + 4).astype(np.int64))
+    return code.astype(np.uint8) | sign
+
+
+def quantize_e4m3_rows(x: np.ndarray):
+    """Per-row (per-token) E4M3 quantisation of fp32 x [M, K]:
+    s = fp32(amax / 448) (1 where amax = 0), q = E4M3(fp32(x / s)).
+    Returns (codes uint8 [M, K], s fp32 [M])."""
+    x = np.asarray(x, dtype=np.float32)
+    amax = np.abs(x).max(axis=1)
+    s = np.where(amax > 0, amax / np.float32(448.0), np.float32(1.0)).astype(np.float32)
+    return encode_e4m3((x / s[:, None]).astype(np.float64)), s
+
+
+def mx_block_exponent(amax: np.ndarray) -> np.ndarray:
+    """The smallest integer e with amax <= 6 * 2^e (0 for amax = 0), clamped
+    to [-127, 127].  With amax = f * 2^x (f in [0.5, 1)): 6 * 2^e = 0.75 *
+    2^(e + 3), so e = x - 3 when f <= 0.75, else x - 2.  Exact."""
+    a = np.asarray(amax, dtype=np.float64)
+    f, x = np.frexp(a)
+    e = np.where(f <= 0.75, x - 3, x - 2).astype(np.int64)
+    return np.clip(np.where(a > 0, e, 0), -127, 127)
+
+
+def quantize_mxfp4_rows(x: np.ndarray):
+    """MXFP4 quantisation of fp32 x [M, K] in blocks of 32 along K: e from
+    the block's amax, q = E2M1(x * 2^-e).  Returns (packed codes uint8
+    [M, K/2], even k in the low nibble; UE8M0 exponents e + 127, uint8
+    [M, K/32])."""
+    x = np.asarray(x, dtype=np.float32)
+    M, K = x.shape
+    xb = x.reshape(M, K // 32, 32).astype(np.float64)
+    e = mx_block_exponent(np.abs(xb).max(axis=2))
+    c = encode_e2m1((xb * np.ldexp(1.0, -e)[:, :, None]).reshape(M, K))
+    return (c[:, 0::2] | (c[:, 1::2] << 4)).astype(np.uint8), (e + 127).astype(np.uint8)
+
 
 EPILOGUES = ("none", "bias", "bias_relu", "bias_silu", "bias_gelu")
 

@@ -506,3 +506,90 @@ def test_fp16_recipe():
     assert abs(v.std() * np.sqrt(256) - 1.0) < 0.1       # N(0,1)/sqrt(K)
     again = inputs.make_operands("fp16", 64, 32, 256, seed=4)
     assert np.array_equal(ops.a, again.a) and np.array_equal(ops.b, again.b)
+
+
+# ---------------------------------------------------------------- activation quantisers
+
+def test_encode_e4m3_definition():
+    codes = np.arange(256, dtype=np.uint8)
+    vals = oracle.decode_e4m3(codes)
+    finite = ~np.isnan(vals)
+    assert np.array_equal(oracle.encode_e4m3(vals[finite]), codes[finite])   # every finite code round-trips
+    assert oracle.encode_e4m3(np.array([np.nan]))[0] == 0x7F
+    # saturation to +-448 (0x7E / 0xFE), never NaN
+    assert list(oracle.encode_e4m3(np.array([448.0, 460.0, 464.0, 1e9, -500.0]))) == [0x7E, 0x7E, 0x7E, 0x7E, 0xFE]
+    # ties go to the even fraction: 1.0625 -> 1.0, 1.1875 -> 1.25; subnormal 2^-10 -> 0, 1.5*2^-9 -> 2*2^-9
+    got = oracle.encode_e4m3(np.array([1.0625, 1.1875, 2.0 ** -10, 1.5 * 2.0 ** -9, -2.0 ** -12]))
+    assert list(got) == [0x38, 0x3A, 0x00, 0x02, 0x80]
+
+
+def test_encode_e4m3_vs_torch_cast():
+    x = torch.randn(1_000_000, generator=torch.Generator().manual_seed(5), dtype=torch.float32) * 100
+    x = x[x.abs() < 448]
+    ref = x.to(torch.float8_e4m3fn).view(torch.uint8).numpy()     # a library encoder
+    assert np.array_equal(oracle.encode_e4m3(x.double().numpy()), ref)
+
+
+def test_encode_e2m1_definition():
+    codes = np.arange(16, dtype=np.uint8)
+    assert np.array_equal(oracle.encode_e2m1(oracle.decode_e2m1(codes)), codes)
+    ties = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0])
+    assert list(oracle.decode_e2m1(oracle.encode_e2m1(ties))) == [0.0, 1.0, 1.0, 2.0, 2.0, 4.0, 4.0]
+    assert list(oracle.encode_e2m1(np.array([6.0, 7.0, 1e9, -1e9, -0.1]))) == [7, 7, 7, 15, 8]
+
+
+def test_mx_block_exponent_edges():
+    f32 = np.float32
+    a = np.array([6.0, np.nextafter(f32(6.0), f32(7.0)), 3.0, 4.0, 0.0, 1e-38, 3e38, 0.75], dtype=np.float32)
+    e = oracle.mx_block_exponent(a)
+    assert list(e[:5]) == [0, 1, -1, 0, 0]
+    for ai, ei in zip(a.astype(np.float64), e):               # smallest e with amax <= 6 * 2^e
+        if ai > 0 and -127 < ei < 127:
+            assert ai <= 6 * 2.0 ** ei and ai > 6 * 2.0 ** (ei - 1)
+    rng = np.random.default_rng(8)
+    r = np.abs(rng.standard_normal(100000).astype(np.float32)) * np.float32(2.0) ** rng.integers(-30, 30, 100000)
+    assert np.array_equal(oracle.mx_block_exponent(r), inputs.ue8m0_block_exponent(r))
+
+
+@pytest.mark.parametrize("R,K", [(64, 256), (300, 1024)])
+def test_quantizers_match_the_input_recipes(R, K):
+    """The oracle's quantisers and the input recipes (torch casts and their
+    own encoders) give the same bytes on the same draws."""
+    codes, s = inputs.e4m3_rows(R, K, inputs._gen(41))
+    x = torch.randn((R, K), generator=inputs._gen(41), dtype=torch.float32).numpy()
+    q, s2 = oracle.quantize_e4m3_rows(x)
+    assert np.array_equal(q, codes) and np.array_equal(s2.view(np.uint32), s.view(np.uint32))
+    packed, exps = inputs.mxfp4_rows(R, K, inputs._gen(42))
+    x = torch.randn((R, K), generator=inputs._gen(42), dtype=torch.float32).numpy()
+    p2, e2 = oracle.quantize_mxfp4_rows(x)
+    assert np.array_equal(p2, packed) and np.array_equal(e2, exps)
+
+
+def test_quantizer_error_bounds():
+    x = (torch.randn((8, 512), generator=torch.Generator().manual_seed(3)) * 7).numpy()
+    q, s = oracle.quantize_e4m3_rows(x)
+    deq = oracle.decode_e4m3(q) * s[:, None].astype(np.float64)
+    # half an ulp: 2^-4 relative for normals, half the subnormal step 2^-10 * s below 2^-6 * s
+    assert np.all(np.abs(deq - x) <= np.maximum(np.abs(x) * 2.0 ** -4, 2.0 ** -10 * s[:, None]) * (1 + 1e-6))
+    p, e = oracle.quantize_mxfp4_rows(x)
+    vals = oracle.decode_e2m1(oracle.unpack_e2m1_rows(p, 512)) * np.repeat(oracle.decode_ue8m0(e), 32, axis=1)
+    step = np.repeat(np.ldexp(1.0, e.astype(np.int64) - 127), 32, axis=1)   # spacing 0.5 .. 2 times 2^e
+    assert np.all(np.abs(vals - x) <= step * 1.0 + 1e-12)
+    zero = np.zeros((2, 64), np.float32)
+    q0, s0 = oracle.quantize_e4m3_rows(zero)
+    assert np.all(q0 == 0) and np.all(s0 == 1.0)
+    p0, e0 = oracle.quantize_mxfp4_rows(zero)
+    assert np.all(p0 == 0) and np.all(e0 == 127)
+
+
+def test_planted_truncating_e4m3_is_caught(monkeypatch):
+    good = oracle.encode_e4m3
+
+    def trunc(v):
+        v = np.asarray(v, np.float64)
+        f, ex = np.frexp(np.abs(v))
+        q = np.ldexp(1.0, ex - 4)
+        return good(np.sign(v) * np.floor(np.abs(v) / q) * q)
+    monkeypatch.setattr(oracle, "encode_e4m3", trunc)
+    with pytest.raises(AssertionError):
+        test_encode_e4m3_vs_torch_cast()
