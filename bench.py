@@ -28,6 +28,8 @@ it once per weight, not per product.
     and roofline fraction.
   - "epilogues": each float workload with the fused bias + GELU epilogue,
     beside the plain product's time.
+  - "quantize": the activation quantiser (gemm_quantize_a) on the FP8 and
+    MXFP4 workloads' A shapes, against the HBM roofline.
 """
 from __future__ import annotations
 
@@ -280,6 +282,55 @@ def time_device(prob: Problem, steps: int, warmup: int, pg, device, graph_len: i
     return e0.elapsed_time(e1) / 1e3
 
 
+class QuantProblem:
+    """gemm_quantize_a on an activation matrix [M, K] (rotating copies past L2)."""
+
+    def __init__(self, q: str, xd: str, M: int, K: int, device):
+        import torch
+        import dense_gemm_preshuffle_gb300 as gp
+        self.gp, self.q, self.xd, self.M, self.K = gp, q, xd, M, K
+        tdt = torch.bfloat16 if xd == "bf16" else torch.float32
+        x = torch.randn((M, K), generator=torch.Generator().manual_seed(5), dtype=torch.float32).to(tdt).to(device)
+        xbytes = x.numel() * x.element_size()
+        self.copies = max(1, math.ceil(2 * L2_BYTES / xbytes) + 1)
+        self.X = [x] + [x.clone() for _ in range(self.copies - 1)]
+        self.A, self.S = gp.quantize(x, q)
+        code_bytes = M * K if q == "e4m3" else M * K // 2
+        scale_bytes = M * 4 if q == "e4m3" else M * K // 32
+        self.bytes = xbytes + code_bytes + scale_bytes
+
+    def step(self, i: int, stream=None):
+        self.gp.gemm_quantize_a(self.X[i % self.copies], self.xd, self.M, self.K, self.q, self.A, self.S, stream)
+
+
+def time_quantizers(args, pg, device, peaks, peak_kind):
+    """The activation quantiser on the FP8 and MXFP4 workloads' A shapes, from
+    fp32 and bf16: device time against the HBM roofline (read x, write codes
+    and scales)."""
+    import torch
+    res = {}
+    for q, M, K in (("e4m3", 8192, 8192), ("e2m1", 4096, 8192)):
+        for xd in ("fp32", "bf16"):
+            name = f"{q}_{M}x{K}_from_{xd}"
+            try:
+                p = QuantProblem(q, xd, M, K, device)
+                steps = max(20, min(args.steps, 400))
+                sec = max_over_ranks(pg, time_device(p, steps, args.warmup, pg, device), device)
+                per = sec / steps
+                achieved = p.bytes / per / 1e9
+                peak = peaks["hbm_gbs"]
+                res[name] = {"us_per_call": round(per * 1e6, 3), "GB/s": round(achieved, 1),
+                             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                                          "unit": "GB/s", "frac": round(achieved / peak, 4),
+                                          "algorithmic_bytes_per_launch": p.bytes,
+                                          "peak_source": f"hbm_gbs ({peak_kind})"}}
+                del p
+                torch.cuda.empty_cache()
+            except Exception as e:
+                res[name] = {"unavailable": f"{type(e).__name__}: {e}"[:200]}
+    return res
+
+
 def time_e2e(prob: Problem, steps: int, warmup: int, device):
     """Through the public call with pinned host buffers: H2D of A (+ its
     scales), gemm_run, D2H of C, every step.  Returns (seconds, h2d, d2h)."""
@@ -465,6 +516,7 @@ def run_ours(args):
             except Exception as e:
                 epi[name] = {"unavailable": f"{type(e).__name__}: {e}"[:200]}
         out["epilogues"] = epi
+        out["quantize"] = time_quantizers(args, pg, device, peaks, peak_kind)
     if rank == 0:
         if not args.no_cpu:
             out["cpu_baseline"] = cpu_baseline(args.workload)

@@ -28,7 +28,7 @@ _LIB_PATH = os.path.join(_HERE, "_lib", "libgemm_preshuffle.so")
 _HEADER = os.path.join(os.path.dirname(_HERE), "include", "gemm_preshuffle.h")
 
 GP_OK = 0
-DTYPES = {"bf16": 0, "e4m3": 1, "int8": 2, "e2m1": 3, "int32": 4, "fp16": 5}
+DTYPES = {"bf16": 0, "e4m3": 1, "int8": 2, "e2m1": 3, "int32": 4, "fp16": 5, "fp32": 6}
 SCALE_MODES = {"none": 0, "rowcol_f32": 1, "block32_ue8m0": 2}
 GP_RUN_DEFAULT = 0
 GP_RUN_B_CONSTANT = 1
@@ -63,11 +63,13 @@ def load_library():
     lib.gemm_unpack_b.argtypes = [vp, i32, i64, i64, vp, vp, vp]
     lib.gemm_run.argtypes = [vp, vp, i32, i64, i64, i64, i32, vp, vp, vp, i32, vp]
     lib.gemm_run_ex.argtypes = [vp, vp, i32, i64, i64, i64, i32, vp, vp, i32, vp, vp, i32, ctypes.c_uint, vp]
+    lib.gemm_quantize_a.argtypes = [vp, i32, i64, i64, i32, vp, vp, vp]
     lib.gemm_last_device_status.argtypes = [vp]
     lib.gemm_status_string.argtypes = [i32]
     lib.gemm_status_string.restype = ctypes.c_char_p
     lib.gemm_debug_skip_load.argtypes = [i32]
     for name in ("gemm_packed_b_bytes", "gemm_preshuffle_b", "gemm_unpack_b", "gemm_run", "gemm_run_ex",
+                 "gemm_quantize_a",
                  "gemm_last_device_status", "gemm_debug_skip_load"):
         getattr(lib, name).restype = i32
     _lib = lib
@@ -149,6 +151,28 @@ def gemm_run_ex(A, B_packed, dtype, M: int, N: int, K: int, scale_mode, scale_a,
     _check(load_library().gemm_run_ex(_ptr(A), _ptr(B_packed), _dt(dtype), M, N, K, _sm(scale_mode),
                                       _ptr(scale_a), _ptr(scale_b), _epi(epilogue), _ptr(bias), _ptr(C),
                                       _dt(c_dtype), int(flags), _stream(stream)), "gemm_run_ex")
+
+
+def gemm_quantize_a(X, x_dtype, M: int, K: int, q_dtype, A_out, scales_out, stream=None) -> None:
+    _check(load_library().gemm_quantize_a(_ptr(X), _dt(x_dtype), M, K, _dt(q_dtype), _ptr(A_out), _ptr(scales_out),
+                                          _stream(stream)), "gemm_quantize_a")
+
+
+def quantize(X, q_dtype, stream=None):
+    """Quantise a device tensor X [M, K] (fp32 or bf16) for gemm_run's A.
+    Returns (A codes, scale_a): E4M3 -> (uint8 [M, K], fp32 [M]);
+    E2M1 -> (uint8 [M, K/2], uint8 [M, K/32])."""
+    import torch
+    M, K = X.shape
+    xd = "bf16" if X.dtype == torch.bfloat16 else "fp32"
+    if _dt(q_dtype) == DTYPES["e4m3"]:
+        A = torch.empty((M, K), dtype=torch.uint8, device=X.device)
+        S = torch.empty((M,), dtype=torch.float32, device=X.device)
+    else:
+        A = torch.empty((M, K // 2), dtype=torch.uint8, device=X.device)
+        S = torch.empty((M, K // 32), dtype=torch.uint8, device=X.device)
+    gemm_quantize_a(X, xd, M, K, q_dtype, A, S, stream)
+    return A, S
 
 
 def gemm_last_device_status(stream=None) -> int:

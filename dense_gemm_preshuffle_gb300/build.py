@@ -21,6 +21,9 @@ LIB = os.path.join(OUT_DIR, "libgemm_preshuffle.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--use_fast_math",
          "-Xptxas", "-warn-spills"]
+# Files whose arithmetic decides integer codes build with IEEE semantics
+# (no approximate division, no flush of denormals to zero).
+IEEE_SOURCES = {"quant.cu"}
 
 
 def _nvcc() -> str:
@@ -59,7 +62,8 @@ def build(verbose: bool = False, force: bool = False, extra_flags=()) -> str:
 
     def compile_one(src):
         obj = os.path.join(OUT_DIR, os.path.basename(src)[:-3] + ".o")
-        cmd = [nvcc, *ARCH, *FLAGS, *extra_flags, "-c", src, "-o", obj]
+        flags = [f for f in FLAGS if not (os.path.basename(src) in IEEE_SOURCES and f == "--use_fast_math")]
+        cmd = [nvcc, *ARCH, *flags, *extra_flags, "-c", src, "-o", obj]
         if verbose:
             print(" ".join(cmd), flush=True)
         r = subprocess.run(cmd, capture_output=True, text=True)

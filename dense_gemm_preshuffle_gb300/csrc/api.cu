@@ -362,6 +362,21 @@ int gemm_last_device_status(void* stream) {
   return GP_OK;
 }
 
+int gemm_quantize_a(const void* X, int x_dtype, int64_t M, int64_t K, int q_dtype, void* A_out, void* scales_out,
+                    void* stream) {
+  if ((x_dtype != GP_FP32 && x_dtype != GP_BF16) || (q_dtype != GP_E4M3 && q_dtype != GP_E2M1))
+    return GP_ERR_INVALID_ARG;
+  if (M < 0 || K < 0 || M >= (int64_t(1) << 31) || K >= (int64_t(1) << 31) || K % 32 != 0) return GP_ERR_SHAPE;
+  if (M == 0 || K == 0) return GP_OK;
+  if (X == nullptr || A_out == nullptr || scales_out == nullptr) return GP_ERR_INVALID_ARG;
+  if (!aligned16(X) || !aligned16(A_out) || !aligned16(scales_out)) return GP_ERR_ALIGNMENT;
+  DeviceInfo* d = nullptr;
+  int rc = device_info(&d);
+  if (rc != GP_OK) return rc;
+  return quant_launch(X, x_dtype == GP_BF16, M, K, q_dtype == GP_E2M1, A_out, scales_out,
+                      static_cast<cudaStream_t>(stream));
+}
+
 // Test hook: the next tcgen05 GEMM launch skips the producer's `index`-th
 // stage load (1-based), so its bounded waits time out.  0 disables it.
 int gemm_debug_skip_load(int index) {

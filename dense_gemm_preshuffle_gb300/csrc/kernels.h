@@ -49,6 +49,9 @@ int i8_strip_rows(int N, int num_sms);
 int i8_gemm_launch(const CUtensorMap& tmA, const CUtensorMap& tmB, I8Params p, int num_sms, cudaStream_t stream);
 
 // int8: 8-row bands and offset-binary bytes; otherwise 128-row bands, bytes as given
+int quant_launch(const void* X, bool x_bf16, int64_t M, int64_t K, bool to_e2m1, void* Q, void* S,
+                 cudaStream_t stream);
+
 int pack_b_launch(const uint8_t* B, const uint8_t* Bsf, int64_t N, int64_t kbytes, int64_t nblk, bool int8,
                   uint8_t* out, cudaStream_t stream);
 int unpack_b_launch(const uint8_t* packed, int64_t N, int64_t kbytes, int64_t nblk, bool int8, uint8_t* B,

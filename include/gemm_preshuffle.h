@@ -56,7 +56,8 @@ typedef enum gp_dtype {
   GP_INT8 = 2,
   GP_E2M1 = 3,
   GP_INT32 = 4,
-  GP_FP16 = 5                 /* IEEE binary16 */
+  GP_FP16 = 5,                /* IEEE binary16 */
+  GP_FP32 = 6                 /* IEEE binary32 (quantiser input only) */
 } gp_dtype;
 
 /* How operand scales enter the product. */
@@ -208,6 +209,32 @@ int gemm_run_ex(const void* A, const void* B_packed, int dtype, int64_t M, int64
  * Returns GP_OK, GP_ERR_DEVICE_TIMEOUT, GP_ERR_DEVICE_CHECK or GP_ERR_CUDA.
  */
 int gemm_last_device_status(void* stream);
+
+/*
+ * The activation quantiser in front of the GEMM: the operand recipes of the
+ * FP8 and MXFP4 products ("GEMM Optimization Guide" section 8.2: per-token
+ * fp32 scales; one UE8M0 byte per 32 K-elements).
+ *
+ * X          : device, [M, K] row-major, x_dtype GP_FP32 or GP_BF16.
+ * q_dtype    : GP_E4M3 or GP_E2M1.
+ * A_out      : device.  E4M3: uint8 codes [M, K].  E2M1: uint8 [M, K/2],
+ *              two codes per byte, even k in the low nibble.  Ready to be
+ *              gemm_run's A.
+ * scales_out : device.  E4M3: fp32 [M], s[m] = amax_k |X[m,k]| / 448 (1 for
+ *              an all-zero row), with codes E4M3FN(X / s).  E2M1: UE8M0
+ *              [M, K/32], e + 127 where e is the smallest integer with
+ *              amax over the block <= 6 * 2^e (0 for an all-zero block), with
+ *              codes E2M1(X * 2^-e).  Ready to be gemm_run's scale_a.
+ * Codes round to nearest even and saturate (+-448, +-6).  The divisions
+ * are IEEE fp32, so the result is bit-exact for given inputs.  NaN or
+ * infinite inputs are not supported.
+ * Shape rules: K % 32 == 0; M, K < 2^31.  M == 0 or K == 0 is a no-op.
+ * Pointers must be 16-byte aligned (GP_ERR_ALIGNMENT).  One kernel on
+ * `stream`; nothing is allocated.  This step precedes the method's GEMM;
+ * the pages do it on the host for their inputs.
+ */
+int gemm_quantize_a(const void* X, int x_dtype, int64_t M, int64_t K, int q_dtype, void* A_out,
+                    void* scales_out, void* stream);
 
 /* Static, human-readable name of a gp_status value. */
 const char* gemm_status_string(int status);

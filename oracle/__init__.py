@@ -252,7 +252,7 @@ def encode_e4m3(v: np.ndarray) -> np.ndarray:
     """Values -> E4M3FN codes, round to nearest even, saturating at +-448
     (no infinities; 448 is S.1111.110).  NaN -> 0x7F."""
     v = np.asarray(v, dtype=np.float64)
-    a = np.abs(v)
+    a = np.where(np.isnan(v), 0.0, np.abs(v))           # NaN is coded separately below
     sign = np.signbit(v).astype(np.uint8) << 7
     f, ex = np.frexp(np.where(a > 0, a, 1.0))          # a = f * 2^ex, f in [0.5, 1)
     e = np.maximum(ex.astype(np.int64) - 1, -6)         # floor(log2 a), subnormals below 2^-6

@@ -116,3 +116,16 @@ def test_run_ex_epilogue_validation(lib, epi, bias, dtype, c_dtype, code):
     rc = lib.gemm_run_ex(FAKE, FAKE, gp.DTYPES[dtype], 16, 256, 512, mode, None, None, epi, bias, FAKE,
                          gp.DTYPES[c_dtype], 0, None)
     assert rc == code
+
+
+@pytest.mark.parametrize("xd,qd,M,K,X,A,S,code", [
+    ("e4m3", "e4m3", 4, 64, FAKE, FAKE, FAKE, 1),     # input must be fp32 or bf16
+    ("fp32", "bf16", 4, 64, FAKE, FAKE, FAKE, 1),     # output must be e4m3 or e2m1
+    ("fp32", "e4m3", 4, 48, FAKE, FAKE, FAKE, 3),     # K % 32
+    ("fp32", "e2m1", -1, 64, FAKE, FAKE, FAKE, 3),
+    ("fp32", "e4m3", 4, 64, None, FAKE, FAKE, 1),
+    ("bf16", "e2m1", 4, 64, FAKE, FAKE + 8, FAKE, 4),
+    ("fp32", "e4m3", 0, 64, None, None, None, 0),     # empty: no-op, nothing touched
+])
+def test_quantize_validation(lib, xd, qd, M, K, X, A, S, code):
+    assert lib.gemm_quantize_a(X, gp.DTYPES[xd], M, K, gp.DTYPES[qd], A, S, None) == code
