@@ -322,6 +322,7 @@ def time_quantizers(args, pg, device, peaks, peak_kind):
                 res[name] = {"us_per_call": round(per * 1e6, 3), "GB/s": round(achieved, 1),
                              "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                                           "unit": "GB/s", "frac": round(achieved / peak, 4),
+                                          "traffic": traffic_from_profiles("quantize_" + name),
                                           "algorithmic_bytes_per_launch": p.bytes,
                                           "peak_source": f"hbm_gbs ({peak_kind})"}}
                 del p
