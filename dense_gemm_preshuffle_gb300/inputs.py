@@ -13,6 +13,8 @@ Recipes (the workloads' stated distributions):
   (saturating values in [448, 480) to 448; |x/s| <= 448*(1+2^-24) here).
   A row whose amax is 0 gets s = 1.
 * INT8: integers uniform in [-127, 127].
+* W4A8: A as INT8; B integers uniform in [-8, 7] (int4), two per byte in
+  two's complement, even k in the low nibble.
 * BF16: x = N(0,1)/sqrt(K) in fp32, rounded to bf16 (torch cast, RNE).
 * FP16: the same draws rounded to IEEE binary16 (torch cast, RNE).
 * MXFP4: x ~ N(0,1) fp32; per (row, 32-element K block) the shared exponent
@@ -37,7 +39,7 @@ import torch
 SEED_BASE = 20261202
 
 # dtype names used across the package, the binding and the tests
-BF16, E4M3, INT8, E2M1, FP16 = "bf16", "e4m3", "int8", "e2m1", "fp16"
+BF16, E4M3, INT8, E2M1, FP16, W4A8 = "bf16", "e4m3", "int8", "e2m1", "fp16", "w4a8"
 
 
 @dataclass
@@ -70,6 +72,7 @@ WORKLOADS = {
 EXTRA_WORKLOADS = {
     "fp8_5120x5120x8320": Workload("fp8_5120x5120x8320", E4M3, 5120, 5120, 8320, 5),
     "fp16_512x4096x4096": Workload("fp16_512x4096x4096", FP16, 512, 4096, 4096, 6),
+    "w4a8_16x7168x4096": Workload("w4a8_16x7168x4096", W4A8, 16, 7168, 4096, 7),
 }
 ALL_WORKLOADS = {**WORKLOADS, **EXTRA_WORKLOADS}
 
@@ -121,6 +124,14 @@ def int8_rows(rows: int, K: int, g: torch.Generator):
     """Integers uniform in [-127, 127] as int8 [rows, K]."""
     x = torch.randint(-127, 128, (rows, K), generator=g, dtype=torch.int16)
     return x.to(torch.int8).numpy()
+
+
+def int4_rows(rows: int, K: int, g: torch.Generator):
+    """Integers uniform in [-8, 7], packed two per byte (two's complement
+    nibbles, even k low): uint8 [rows, K/2]."""
+    x = torch.randint(-8, 8, (rows, K), generator=g, dtype=torch.int16).numpy()
+    nib = (x & 0xF).astype(np.uint8)
+    return nib[:, 0::2] | (nib[:, 1::2] << 4)
 
 
 def bf16_rows(rows: int, K: int, g: torch.Generator, chunk: int = 2048):
@@ -202,6 +213,8 @@ def make_operands(dtype: str, M: int, N: int, K: int, seed: int) -> Operands:
         return Operands(dtype, M, N, K, a, b, sa, sb)
     if dtype == INT8:
         return Operands(dtype, M, N, K, int8_rows(M, K, g), int8_rows(N, K, g))
+    if dtype == W4A8:
+        return Operands(dtype, M, N, K, int8_rows(M, K, g), int4_rows(N, K, g))
     if dtype == BF16:
         return Operands(dtype, M, N, K, bf16_rows(M, K, g), bf16_rows(N, K, g))
     if dtype == FP16:

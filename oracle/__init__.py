@@ -17,6 +17,9 @@ Contents:
 * GEMMs in fp64 / int64.  The triple loops live in ``gemm_oracle.c``, built
   by ``oracle/build.py``:
   - INT8: C = sum_k a*b, exact in int64.
+  - W4A8 (int4 weights B, int8 activations A; "GEMM Optimization Guide"
+    section 8.2 counts N*K//2 bytes for such a B): C = sum_k a*b, exact in
+    int64.
   - BF16 and FP16: C = sum_k a*b, fp64.
   - E4M3 with per-row/per-column fp32 scales: C = (sum_k qa*qb) * sa[m] * sb[n].
     "GEMM Optimization Guide", section 7.1 (direct store): the epilogue forms
@@ -174,6 +177,23 @@ def gemm_int8(a: np.ndarray, b: np.ndarray) -> np.ndarray:
     return c
 
 
+def unpack_int4_rows(packed: np.ndarray, K: int) -> np.ndarray:
+    """int4 B [rows, K/2] bytes (two's complement nibbles, even k in the low
+    nibble) -> int8 [rows, K] values in [-8, 7]."""
+    p = np.asarray(packed, dtype=np.uint8)
+    out = np.empty((p.shape[0], K), dtype=np.int16)
+    lo = (p & 0xF).astype(np.int16)
+    hi = (p >> 4).astype(np.int16)
+    out[:, 0::2] = np.where(lo >= 8, lo - 16, lo)
+    out[:, 1::2] = np.where(hi >= 8, hi - 16, hi)
+    return out.astype(np.int8)
+
+
+def gemm_w4a8(a: np.ndarray, b_packed: np.ndarray, K: int) -> np.ndarray:
+    """C = A . B^T for int8 A [M, K] and int4 B (packed [N, K/2]); int64."""
+    return gemm_int8(a, unpack_int4_rows(b_packed, K))
+
+
 def gemm_f64(a: np.ndarray, b: np.ndarray) -> np.ndarray:
     """C = A . B^T for already-decoded fp64 A [M,K], B [N,K]."""
     a = np.ascontiguousarray(a, dtype=np.float64)
@@ -229,6 +249,8 @@ def gemm_operands(ops, rows: Optional[np.ndarray] = None, cols: Optional[np.ndar
         sb = None if sb is None else sb[cols]
     if ops.dtype == "int8":
         return gemm_int8(a, b)
+    if ops.dtype == "w4a8":
+        return gemm_w4a8(a, b, ops.K)
     if ops.dtype == "bf16":
         return gemm_bf16(a, b)
     if ops.dtype == "fp16":
@@ -371,12 +393,12 @@ TILE_BYTES = 128
 
 
 def elem_bits(dtype: str) -> int:
-    return {"bf16": 16, "fp16": 16, "e4m3": 8, "int8": 8, "e2m1": 4}[dtype]
+    return {"bf16": 16, "fp16": 16, "e4m3": 8, "int8": 8, "e2m1": 4, "w4a8": 4}[dtype]
 
 
 def band_rows(dtype: str) -> int:
-    """Rows per packed tile: 8 for INT8, 128 for the tcgen05 element types."""
-    return 8 if dtype == "int8" else TILE_ROWS
+    """Rows per packed tile: 8 for INT8 and W4A8, 128 for the tcgen05 element types."""
+    return 8 if dtype in ("int8", "w4a8") else TILE_ROWS
 
 
 def packed_offset(n: np.ndarray, kb: np.ndarray, Kb: int, rows: int = TILE_ROWS) -> np.ndarray:
@@ -444,8 +466,33 @@ def byte_bias(dtype: str) -> int:
     return 0x80 if dtype == "int8" else 0
 
 
+# W4A8's int4 B: each 32-bit little-endian word of a row holds K values
+# k0..k7 as offset-binary nibbles u = b + 8, k0..k7 at bits 0, 16, 4, 20, 8,
+# 24, 12, 28, so that (word >> 4j) & 0x000F000F is the pair (k2j, k2j+1) as
+# two fp16 bit patterns.
+W4_NIBBLE_BITS = (0, 16, 4, 20, 8, 24, 12, 28)
+
+
+def interleave_int4_words(b_packed: np.ndarray) -> np.ndarray:
+    """int4 B bytes [N, K/2] (two's complement, even k low) -> the packed
+    word order above, as bytes [N, K/2]."""
+    p = np.ascontiguousarray(b_packed, dtype=np.uint8)
+    N, Kb = p.shape
+    nib = np.empty((N, Kb * 2), dtype=np.uint32)
+    nib[:, 0::2] = p & 0xF
+    nib[:, 1::2] = p >> 4
+    u = nib ^ 0x8                                         # offset binary: b + 8
+    u = u.reshape(N, Kb // 4, 8)
+    words = np.zeros((N, Kb // 4), dtype=np.uint32)
+    for k, bit in enumerate(W4_NIBBLE_BITS):
+        words |= u[:, :, k] << np.uint32(bit)
+    return words.astype("<u4").view(np.uint8).reshape(N, Kb)
+
+
 def pack_b(b: np.ndarray, dtype: str, scales: Optional[np.ndarray] = None) -> np.ndarray:
     """Whole packed buffer for B (data region, then the scale region for E2M1)."""
+    if dtype == "w4a8":
+        return pack_b_bytes(interleave_int4_words(b), band_rows(dtype))
     raw = np.ascontiguousarray(b).view(np.uint8).reshape(b.shape[0], -1) ^ np.uint8(byte_bias(dtype))
     data = pack_b_bytes(raw, band_rows(dtype))
     if dtype == "e2m1":

@@ -593,3 +593,58 @@ def test_planted_truncating_e4m3_is_caught(monkeypatch):
     monkeypatch.setattr(oracle, "encode_e4m3", trunc)
     with pytest.raises(AssertionError):
         test_encode_e4m3_vs_torch_cast()
+
+
+# ---------------------------------------------------------------- W4A8 (int4 weights, int8 activations)
+
+def test_unpack_int4_definition():
+    b = np.arange(256, dtype=np.uint8)[None, :]
+    v = oracle.unpack_int4_rows(b, 512)[0]
+    lo, hi = v[0::2], v[1::2]
+    for byte in range(256):
+        n0, n1 = byte & 0xF, byte >> 4
+        assert lo[byte] == (n0 - 16 if n0 >= 8 else n0) and hi[byte] == (n1 - 16 if n1 >= 8 else n1)
+
+
+@pytest.mark.parametrize("M,N,K", [(3, 4, 16), (5, 3, 64)])
+def test_w4a8_vs_brute_force(M, N, K):
+    ops = inputs.make_operands("w4a8", M, N, K, seed=13)
+    a = ops.a.astype(np.int64)
+    b = oracle.unpack_int4_rows(ops.b, K).astype(np.int64)
+    assert b.min() >= -8 and b.max() <= 7
+    got = oracle.gemm_operands(ops)
+    for m in range(M):
+        for n in range(N):
+            assert got[m, n] == sum(int(a[m, k]) * int(b[n, k]) for k in range(K))
+
+
+def test_w4a8_identity_and_extremes():
+    K = 64
+    eye = np.eye(K, dtype=np.int8)
+    b = inputs.int4_rows(24, K, inputs._gen(5))
+    assert np.array_equal(oracle.gemm_w4a8(eye, b, K), oracle.unpack_int4_rows(b, K).T.astype(np.int64))
+    a = np.full((2, 4096), -128, np.int8)
+    bb = np.full((3, 2048), 0x88, np.uint8)           # every nibble -8
+    assert np.all(oracle.gemm_w4a8(a, bb, 4096) == 4096 * 1024)
+
+
+def test_w4a8_pack_word_order():
+    # one row, K = 256 (128 bytes): values k = 0..7 in the first word are -8, -7, ..., -1
+    vals = np.array([-8, -7, -6, -5, -4, -3, -2, -1] + [0] * 248, np.int16)
+    nib = (vals & 0xF).astype(np.uint8)
+    b = (nib[0::2] | (nib[1::2] << 4))[None, :].repeat(8, axis=0)   # an 8-row band
+    p = oracle.pack_b(b, "w4a8")
+    word = int(p[:4].view("<u4")[0])
+    u = [v + 8 for v in range(-8, 0)]                   # offset binary 0..7
+    for k, bit in enumerate(oracle.W4_NIBBLE_BITS):
+        assert (word >> bit) & 0xF == u[k]
+    for j in range(4):                                   # (word >> 4j) & 0x000F000F is the pair (k2j, k2j+1)
+        pair = (word >> (4 * j)) & 0x000F000F
+        assert pair & 0xFFFF == u[2 * j] and pair >> 16 == u[2 * j + 1]
+    # a bijection of the bytes of B (as nibble multisets per word), with the 8-row band layout
+    rng = np.random.default_rng(4)
+    bb = rng.integers(0, 256, size=(16, 256), dtype=np.uint8)
+    pk = oracle.pack_b(bb, "w4a8")
+    assert pk.size == bb.size
+    il = oracle.interleave_int4_words(bb)
+    assert np.array_equal(pk, oracle.pack_b_bytes(il, 8))
