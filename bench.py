@@ -71,6 +71,8 @@ def algorithmic_bytes(dtype: str, M: int, N: int, K: int) -> int:
     INT8 workload's C is int32 and it has no scales."""
     if dtype == "int8":
         return M * K + N * K + M * N * 4
+    if dtype == "w4a8":
+        return M * K + N * K // 2 + M * N * 4
     if dtype == "e4m3":
         return M * K + N * K + M * N * 2 + (M + N) * 4
     if dtype in ("bf16", "fp16"):
@@ -83,7 +85,7 @@ def algorithmic_bytes(dtype: str, M: int, N: int, K: int) -> int:
 def bound_of(dtype: str, M: int) -> str:
     # the guide's rule of thumb (section 8.3): M <= 512 memory-bound; the
     # int8 small-batch workload is the weight-streaming case
-    return "hbm" if dtype == "int8" else "tensor"
+    return "hbm" if dtype in ("int8", "w4a8") else "tensor"
 
 
 class ClockSampler:
@@ -230,10 +232,11 @@ class Problem:
         self.A = [A] + [A.clone() for _ in range(copies - 1)]
         self.sa = self.host_sa.to(device) if self.host_sa is not None else None
         self.sb = sb if self.dtype == "e4m3" else None
-        cdt = torch.int32 if self.dtype == "int8" else (torch.float16 if self.dtype == "fp16" else torch.bfloat16)
+        cdt = torch.int32 if self.dtype in ("int8", "w4a8") else (
+            torch.float16 if self.dtype == "fp16" else torch.bfloat16)
         self.C = [torch.empty((self.M, self.N), dtype=cdt, device=device) for _ in range(min(copies, 4))]
-        self.c_dtype = {"int8": "int32", "fp16": "fp16"}.get(self.dtype, "bf16")
-        self.mode = {"int8": "none", "bf16": "none", "fp16": "none", "e4m3": "rowcol_f32",
+        self.c_dtype = {"int8": "int32", "w4a8": "int32", "fp16": "fp16"}.get(self.dtype, "bf16")
+        self.mode = {"int8": "none", "w4a8": "none", "bf16": "none", "fp16": "none", "e4m3": "rowcol_f32",
                      "e2m1": "block32_ue8m0"}[self.dtype]
         self.flops = 2 * self.M * self.N * self.K
         self.bytes = algorithmic_bytes(self.dtype, self.M, self.N, self.K)
@@ -497,7 +500,7 @@ def run_ours(args):
         # the fused bias + GELU epilogue on each float workload, against the plain product
         epi = {}
         for name in inputs.WORKLOADS:
-            if name.startswith("int8"):
+            if name.startswith(("int8", "w4a8")):
                 continue
             try:
                 p3 = Problem(name, device)

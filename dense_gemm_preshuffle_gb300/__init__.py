@@ -28,7 +28,7 @@ _LIB_PATH = os.path.join(_HERE, "_lib", "libgemm_preshuffle.so")
 _HEADER = os.path.join(os.path.dirname(_HERE), "include", "gemm_preshuffle.h")
 
 GP_OK = 0
-DTYPES = {"bf16": 0, "e4m3": 1, "int8": 2, "e2m1": 3, "int32": 4, "fp16": 5, "fp32": 6}
+DTYPES = {"bf16": 0, "e4m3": 1, "int8": 2, "e2m1": 3, "int32": 4, "fp16": 5, "fp32": 6, "w4a8": 7}
 SCALE_MODES = {"none": 0, "rowcol_f32": 1, "block32_ue8m0": 2}
 GP_RUN_DEFAULT = 0
 GP_RUN_B_CONSTANT = 1
@@ -189,7 +189,7 @@ def preshuffle_b(B, dtype, B_scales=None, stream=None):
     """Pack a device tensor B [N, K] (E2M1: [N, K/2] bytes) into a new uint8 tensor."""
     import torch
     N = B.shape[0]
-    K = B.shape[1] * (2 if _dt(dtype) == DTYPES["e2m1"] else 1)
+    K = B.shape[1] * (2 if _dt(dtype) in (DTYPES["e2m1"], DTYPES["w4a8"]) else 1)
     out = torch.empty(gemm_packed_b_bytes(dtype, N, K), dtype=torch.uint8, device=B.device)
     gemm_preshuffle_b(B, B_scales, dtype, N, K, out, stream)
     return out
@@ -211,7 +211,7 @@ def matmul(A, B_packed, dtype, N: int, K: int, scale_a=None, scale_b=None, out=N
     if out_dtype is None:
         out_dtype = "fp16" if d == DTYPES["fp16"] else "bf16"
     fdt = torch.float16 if out_dtype == "fp16" else torch.bfloat16
-    if d == DTYPES["int8"]:
+    if d in (DTYPES["int8"], DTYPES["w4a8"]):
         c_dtype, mode, tdt = "int32", "none", torch.int32
     elif d == DTYPES["e2m1"]:
         c_dtype, mode, tdt = out_dtype, "block32_ue8m0", fdt

@@ -74,11 +74,14 @@ int elem_bits(int dtype) {
     case GP_E4M3: return 8;
     case GP_INT8: return 8;
     case GP_E2M1: return 4;
+    case GP_W4A8: return 4;  // the bits of B; A is int8
     default: return 0;
   }
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int pack_layout(int dtype) { return dtype == GP_INT8 ? PACK_INT8 : dtype == GP_W4A8 ? PACK_W4 : PACK_TC; }
 
 // Shape rules shared by the packer and the GEMM (N, K part).
 int check_nk(int dtype, int64_t N, int64_t K, int64_t* kbytes) {
@@ -176,7 +179,7 @@ int gemm_preshuffle_b(const void* B, const void* B_scales, int dtype, int64_t N,
   DeviceInfo* d = nullptr;
   if ((rc = device_info(&d)) != GP_OK) return rc;
   return pack_b_launch(static_cast<const uint8_t*>(B), static_cast<const uint8_t*>(B_scales), N, kb, K / 32,
-                       dtype == GP_INT8, static_cast<uint8_t*>(B_packed), static_cast<cudaStream_t>(stream));
+                       pack_layout(dtype), static_cast<uint8_t*>(B_packed), static_cast<cudaStream_t>(stream));
 }
 
 int gemm_unpack_b(const void* B_packed, int dtype, int64_t N, int64_t K, void* B_out, void* B_scales_out,
@@ -190,7 +193,7 @@ int gemm_unpack_b(const void* B_packed, int dtype, int64_t N, int64_t K, void* B
   if (!aligned16(B_out) || !aligned16(B_packed)) return GP_ERR_ALIGNMENT;
   DeviceInfo* d = nullptr;
   if ((rc = device_info(&d)) != GP_OK) return rc;
-  return unpack_b_launch(static_cast<const uint8_t*>(B_packed), N, kb, K / 32, dtype == GP_INT8,
+  return unpack_b_launch(static_cast<const uint8_t*>(B_packed), N, kb, K / 32, pack_layout(dtype),
                          static_cast<uint8_t*>(B_out),
                          dtype == GP_E2M1 ? static_cast<uint8_t*>(B_scales_out) : nullptr,
                          static_cast<cudaStream_t>(stream));
@@ -217,7 +220,8 @@ int gemm_run_ex(const void* A, const void* B_packed, int dtype, int64_t M, int64
                         (dtype == GP_E4M3 && scale_mode == GP_SCALE_ROWCOL_F32 && float_out) ||
                         (dtype == GP_E4M3 && scale_mode == GP_SCALE_NONE && float_out) ||
                         (dtype == GP_E2M1 && scale_mode == GP_SCALE_BLOCK32_UE8M0 && float_out) ||
-                        (dtype == GP_INT8 && scale_mode == GP_SCALE_NONE && c_dtype == GP_INT32);
+                        (dtype == GP_INT8 && scale_mode == GP_SCALE_NONE && c_dtype == GP_INT32) ||
+                        (dtype == GP_W4A8 && scale_mode == GP_SCALE_NONE && c_dtype == GP_INT32);
   if (elem_bits(dtype) == 0 || scale_mode < GP_SCALE_NONE || scale_mode > GP_SCALE_BLOCK32_UE8M0 ||
       (!float_out && c_dtype != GP_INT32))
     return GP_ERR_INVALID_ARG;
@@ -227,7 +231,8 @@ int gemm_run_ex(const void* A, const void* B_packed, int dtype, int64_t M, int64
   int rc = check_nk(dtype, N, K, &kb);
   if (rc != GP_OK) return rc;
   if (M < 0 || M >= (int64_t(1) << 31)) return GP_ERR_SHAPE;
-  if (dtype == GP_INT8 && K > 131072) return GP_ERR_SHAPE;  // exact result must fit int32
+  if (dtype == GP_INT8 && K > 131072) return GP_ERR_SHAPE;      // exact result must fit int32
+  if (dtype == GP_W4A8 && K > 2097152) return GP_ERR_SHAPE;     // 128 * 8 * K < 2^31
   const size_t c_elem = c_dtype == GP_INT32 ? 4 : 2;
   if (M == 0 || N == 0) return GP_OK;  // empty output
   // ---- pointers
@@ -258,7 +263,8 @@ int gemm_run_ex(const void* A, const void* B_packed, int dtype, int64_t M, int64
     return cudaGetLastError() == cudaSuccess ? GP_OK : GP_ERR_CUDA;
   }
 
-  if (dtype == GP_INT8) {
+  if (dtype == GP_INT8 || dtype == GP_W4A8) {
+    const bool w4 = dtype == GP_W4A8;
     I8Params p{};
     p.Bp = static_cast<const uint8_t*>(B_packed);
     p.C = static_cast<int32_t*>(C);
@@ -267,15 +273,17 @@ int gemm_run_ex(const void* A, const void* B_packed, int dtype, int64_t M, int64
     p.M = (int)M;
     p.N = (int)N;
     p.K = (int)K;
-    p.ktiles = (int)(kb / 128);
+    p.ktiles = (int)(K / 128);  // 128-element K tiles of A (int8: K bytes a row)
     p.strip = i8_strip_rows((int)N, d->num_sms);
     p.b_constant = b_constant;
+    p.w4 = w4 ? 1 : 0;
+    const int64_t b_tiles = kb / 128;  // 128-byte tiles of a packed B row (256 K values for int4)
     // A as [K tiles][M rows][128 B] (3-D view, 128-byte swizzle): one copy
     // brings 8 K tiles of 16 rows.
     CUtensorMap tmA, tmB;
     {
       cuuint64_t dims[3] = {128, (cuuint64_t)M, (cuuint64_t)p.ktiles};
-      cuuint64_t strides[2] = {(cuuint64_t)kb, 128};
+      cuuint64_t strides[2] = {(cuuint64_t)K, 128};
       cuuint32_t box[3] = {128, 16, 8};
       cuuint32_t estr[3] = {1, 1, 1};
       if (g_encode(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(A), dims, strides, box, estr,
@@ -283,12 +291,13 @@ int gemm_run_ex(const void* A, const void* B_packed, int dtype, int64_t M, int64
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return GP_ERR_CUDA;
     }
-    // packed B as [8-row bands][K tiles][8 rows][128 B] (4-D view, already
-    // swizzled): one copy brings 8 K tiles of a CTA's whole strip of bands.
+    // packed B as [8-row bands][B tiles][8 rows][128 B] (4-D view, already
+    // swizzled): one copy brings a stage's 1024 K values (8 tiles, or 4 of
+    // int4) of a CTA's whole strip of bands.
     {
-      cuuint64_t dims[4] = {128, 8, (cuuint64_t)p.ktiles, (cuuint64_t)(N / 8)};
-      cuuint64_t strides[3] = {128, 1024, (cuuint64_t)p.ktiles * 1024};
-      cuuint32_t box[4] = {128, 8, 8, (cuuint32_t)(p.strip / 8)};
+      cuuint64_t dims[4] = {128, 8, (cuuint64_t)b_tiles, (cuuint64_t)(N / 8)};
+      cuuint64_t strides[3] = {128, 1024, (cuuint64_t)b_tiles * 1024};
+      cuuint32_t box[4] = {128, 8, w4 ? 4u : 8u, (cuuint32_t)(p.strip / 8)};
       cuuint32_t estr[4] = {1, 1, 1, 1};
       if (g_encode(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(B_packed), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

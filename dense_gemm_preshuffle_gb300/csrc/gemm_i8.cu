@@ -95,13 +95,15 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// NB8: eight-row units per strip.
-template <int NB8>
+// NB8: eight-row units per strip.  W4: B is W4A8's int4 (a packed 128-byte
+// B tile then spans two 128-element K tiles of A).
+template <int NB8, bool W4>
 __global__ void __launch_bounds__(I8_THREADS, i8_ctas_per_sm(NB8))
     i8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, I8Params p) {
   constexpr int SN = NB8 * 8;                    // rows of B per CTA
+  constexpr int BT = W4 ? I8_KT / 2 : I8_KT;     // packed B tiles (128 B per row) per stage
   constexpr int A_BYTES = I8_KT * 16 * 128;      // [kt][16 rows][128 B], 128-byte swizzle
-  constexpr int B_BYTES = I8_KT * SN * 128;      // [unit][kt][8 rows][128 B], packed swizzle
+  constexpr int B_BYTES = BT * SN * 128;         // [unit][B tile][8 rows][128 B], packed swizzle
   constexpr int STAGE = A_BYTES + B_BYTES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -140,14 +142,14 @@ __global__ void __launch_bounds__(I8_THREADS, i8_ctas_per_sm(NB8))
     prefetch_tensormap(&tmA);
     prefetch_tensormap(&tmB);
   }
-  // B: NB8 units x I8_KT K tiles of 8 rows; units past N read as zeros
+  // B: NB8 units x BT packed tiles of 8 rows; units past N read as zeros
   auto load_b = [&](int q) {
     const int s = q % I8_STAGES;
     mbar_arrive_expect_tx(&full[s], B_BYTES);
     asm volatile(
         "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];" ::
             "r"(smem_u32(base + s * STAGE + A_BYTES)),
-        "l"(reinterpret_cast<uint64_t>(&tmB)), "r"(0), "r"(0), "r"(q * I8_KT), "r"(u0), "r"(smem_u32(&full[s]))
+        "l"(reinterpret_cast<uint64_t>(&tmB)), "r"(0), "r"(0), "r"(q * BT), "r"(u0), "r"(smem_u32(&full[s]))
         : "memory");
   };
   // A: I8_KT K tiles x 16 rows x 128 B (rows >= M and K tiles >= ktiles read as zeros)
@@ -168,7 +170,7 @@ __global__ void __launch_bounds__(I8_THREADS, i8_ctas_per_sm(NB8))
     for (int q = early; q < nstages; ++q)
       asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
                        reinterpret_cast<uint64_t>(&tmB)),
-                   "r"(0), "r"(0), "r"(q * I8_KT), "r"(u0)
+                   "r"(0), "r"(0), "r"(q * BT), "r"(u0)
                    : "memory");
   }
   if (threadIdx.x == 32) {
@@ -234,43 +236,88 @@ __global__ void __launch_bounds__(I8_THREADS, i8_ctas_per_sm(NB8))
     if (!wait_bounded(&full[s], ph, abort_flag, p.status, ST_TIMEOUT_CONSUMER, limit)) break;
     const bool live = q * I8_KT + warp < p.ktiles;
     const uint8_t* sa = base + s * STAGE + warp * (16 * 128);
-    const uint8_t* sb = base + s * STAGE + A_BYTES + (warp * 8 + g) * 128;  // + unit * (I8_KT * 8 * 128)
     float f[NB8][4];
 #pragma unroll
     for (int nb = 0; nb < NB8; ++nb) f[nb][0] = f[nb][1] = f[nb][2] = f[nb][3] = 0.f;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int slot = ((2 * t + h) ^ g) << 4;
-      const uint4 ag = *reinterpret_cast<const uint4*>(sa + g * 128 + slot);
-      const uint4 ag8 = *reinterpret_cast<const uint4*>(sa + (g + 8) * 128 + slot);
+    if constexpr (W4) {
+      // K tile `warp` of A is half of packed B tile warp / 2: lane t's 32 K
+      // values are one 16-byte chunk, 4 * (warp % 2) + t, of each B row.
+      const uint8_t* sb = base + s * STAGE + A_BYTES + ((warp >> 1) * 8 + g) * 128 +
+                          (((4 * (warp & 1) + t) ^ g) << 4);  // + unit * (BT * 8 * 128)
       uint4 bw[NB8];
 #pragma unroll
-      for (int nb = 0; nb < NB8; ++nb)
-        bw[nb] = *reinterpret_cast<const uint4*>(sb + nb * (I8_KT * 8 * 128) + slot);
-      if (h == 1) {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);  // this warp's reads of the stage are done
-      }
-      if (live) {
-        const uint32_t aw[4] = {ag.x, ag.y, ag.z, ag.w};
-        const uint32_t a8w[4] = {ag8.x, ag8.y, ag8.z, ag8.w};
-        uint32_t alo[4], ahi[4], a8lo[4], a8hi[4];
+      for (int nb = 0; nb < NB8; ++nb) bw[nb] = *reinterpret_cast<const uint4*>(sb + nb * (BT * 8 * 128));
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          i8x4_to_f16x2(aw[j], alo[j], ahi[j]);
-          i8x4_to_f16x2(a8w[j], a8lo[j], a8hi[j]);
-          rs_lo = __dp4a((int)aw[j], 0x01010101, rs_lo);
-          rs_hi = __dp4a((int)a8w[j], 0x01010101, rs_hi);
+      for (int h = 0; h < 2; ++h) {
+        const int slot = ((2 * t + h) ^ g) << 4;
+        const uint4 ag = *reinterpret_cast<const uint4*>(sa + g * 128 + slot);
+        const uint4 ag8 = *reinterpret_cast<const uint4*>(sa + (g + 8) * 128 + slot);
+        if (h == 1) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[s]);  // this warp's reads of the stage are done
         }
+        if (live) {
+          const uint32_t aw[4] = {ag.x, ag.y, ag.z, ag.w};
+          const uint32_t a8w[4] = {ag8.x, ag8.y, ag8.z, ag8.w};
+          uint32_t alo[4], ahi[4], a8lo[4], a8hi[4];
 #pragma unroll
-        for (int nb = 0; nb < NB8; ++nb) {
-          if (nb < nu) {  // uniform: units past N are skipped
-            const uint32_t w[4] = {bw[nb].x, bw[nb].y, bw[nb].z, bw[nb].w};
+          for (int j = 0; j < 4; ++j) {
+            i8x4_to_f16x2(aw[j], alo[j], ahi[j]);
+            i8x4_to_f16x2(a8w[j], a8lo[j], a8hi[j]);
+            rs_lo = __dp4a((int)aw[j], 0x01010101, rs_lo);
+            rs_hi = __dp4a((int)a8w[j], 0x01010101, rs_hi);
+          }
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              uint32_t blo, bhi;
-              u8x4_to_f16x2_sub(w[j], blo, bhi);
-              mma_16816(f[nb], alo[j], a8lo[j], ahi[j], a8hi[j], blo, bhi);
+          for (int nb = 0; nb < NB8; ++nb) {
+            if (nb < nu) {  // uniform: units past N are skipped
+              const uint32_t w2[2] = {h == 0 ? bw[nb].x : bw[nb].z, h == 0 ? bw[nb].y : bw[nb].w};
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                // A word j holds K values 4j..4j+3 of this half: B word j / 2,
+                // nibble pairs (0,1),(2,3) or (4,5),(6,7) as fp16 subnormals
+                const uint32_t w = w2[j >> 1] >> ((j & 1) * 8);
+                mma_16816(f[nb], alo[j], a8lo[j], ahi[j], a8hi[j], w & 0x000F000Fu, (w >> 4) & 0x000F000Fu);
+              }
+            }
+          }
+        }
+      }
+    } else {
+      const uint8_t* sb = base + s * STAGE + A_BYTES + (warp * 8 + g) * 128;  // + unit * (I8_KT * 8 * 128)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int slot = ((2 * t + h) ^ g) << 4;
+        const uint4 ag = *reinterpret_cast<const uint4*>(sa + g * 128 + slot);
+        const uint4 ag8 = *reinterpret_cast<const uint4*>(sa + (g + 8) * 128 + slot);
+        uint4 bw[NB8];
+#pragma unroll
+        for (int nb = 0; nb < NB8; ++nb)
+          bw[nb] = *reinterpret_cast<const uint4*>(sb + nb * (I8_KT * 8 * 128) + slot);
+        if (h == 1) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[s]);  // this warp's reads of the stage are done
+        }
+        if (live) {
+          const uint32_t aw[4] = {ag.x, ag.y, ag.z, ag.w};
+          const uint32_t a8w[4] = {ag8.x, ag8.y, ag8.z, ag8.w};
+          uint32_t alo[4], ahi[4], a8lo[4], a8hi[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            i8x4_to_f16x2(aw[j], alo[j], ahi[j]);
+            i8x4_to_f16x2(a8w[j], a8lo[j], a8hi[j]);
+            rs_lo = __dp4a((int)aw[j], 0x01010101, rs_lo);
+            rs_hi = __dp4a((int)a8w[j], 0x01010101, rs_hi);
+          }
+#pragma unroll
+          for (int nb = 0; nb < NB8; ++nb) {
+            if (nb < nu) {  // uniform: units past N are skipped
+              const uint32_t w[4] = {bw[nb].x, bw[nb].y, bw[nb].z, bw[nb].w};
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                uint32_t blo, bhi;
+                u8x4_to_f16x2_sub(w[j], blo, bhi);
+                mma_16816(f[nb], alo[j], a8lo[j], ahi[j], a8hi[j], blo, bhi);
+              }
             }
           }
         }
@@ -295,11 +342,12 @@ __global__ void __launch_bounds__(I8_THREADS, i8_ctas_per_sm(NB8))
 #pragma unroll
   for (int nb = 0; nb < NB8; ++nb) {
     const int col = nb * 8 + 2 * t;
-    // sum a*b = sum a*(b + 128) - 128 * sum a
-    red[(warp * 16 + g) * SN + col] = acc[nb][0] - 128 * rs_lo;
-    red[(warp * 16 + g) * SN + col + 1] = acc[nb][1] - 128 * rs_lo;
-    red[(warp * 16 + g + 8) * SN + col] = acc[nb][2] - 128 * rs_hi;
-    red[(warp * 16 + g + 8) * SN + col + 1] = acc[nb][3] - 128 * rs_hi;
+    // sum a*b = sum a*(b + bias) - bias * sum a (bias 128 for int8 B, 8 for int4)
+    constexpr int OFF = W4 ? 8 : 128;
+    red[(warp * 16 + g) * SN + col] = acc[nb][0] - OFF * rs_lo;
+    red[(warp * 16 + g) * SN + col + 1] = acc[nb][1] - OFF * rs_lo;
+    red[(warp * 16 + g + 8) * SN + col] = acc[nb][2] - OFF * rs_hi;
+    red[(warp * 16 + g + 8) * SN + col + 1] = acc[nb][3] - OFF * rs_hi;
   }
   named_bar_sync(1, I8_CW * 32);
   const int cols = nu * 8;
@@ -323,14 +371,14 @@ static int env_int(const char* name, int dflt) {
   return v > 0 ? v : dflt;
 }
 
-template <int NB8>
+template <int NB8, bool W4>
 static int launch_i8(const CUtensorMap& tmA, const CUtensorMap& tmB, I8Params p, dim3 grid, cudaStream_t stream) {
-  constexpr int STAGE = I8_KT * (16 + NB8 * 8) * 128;
+  constexpr int STAGE = I8_KT * 16 * 128 + (W4 ? I8_KT / 2 : I8_KT) * NB8 * 8 * 128;
   constexpr int RED = I8_CW * 16 * NB8 * 8 * 4;
   constexpr int RING = I8_STAGES * STAGE;
   constexpr int SMEM = (RING > RED ? RING : RED) + 2 * I8_STAGES * 8 + 16 + 1024;
   static_assert(SMEM * i8_ctas_per_sm(NB8) <= 228 * 1024, "shared memory budget");
-  auto kern = i8_gemm_kernel<NB8>;
+  auto kern = i8_gemm_kernel<NB8, W4>;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -373,11 +421,19 @@ int i8_strip_rows(int N, int num_sms) {
 int i8_gemm_launch(const CUtensorMap& tmA, const CUtensorMap& tmB, I8Params p, int num_sms, cudaStream_t stream) {
   const int strip = p.strip;
   dim3 grid((unsigned)((p.N + strip - 1) / strip), (unsigned)((p.M + 15) / 16));
+  if (p.w4) {
+    switch (strip) {
+      case 16: return launch_i8<2, true>(tmA, tmB, p, grid, stream);
+      case 32: return launch_i8<4, true>(tmA, tmB, p, grid, stream);
+      case 48: return launch_i8<6, true>(tmA, tmB, p, grid, stream);
+      default: return launch_i8<8, true>(tmA, tmB, p, grid, stream);
+    }
+  }
   switch (strip) {
-    case 16: return launch_i8<2>(tmA, tmB, p, grid, stream);
-    case 32: return launch_i8<4>(tmA, tmB, p, grid, stream);
-    case 48: return launch_i8<6>(tmA, tmB, p, grid, stream);
-    default: return launch_i8<8>(tmA, tmB, p, grid, stream);
+    case 16: return launch_i8<2, false>(tmA, tmB, p, grid, stream);
+    case 32: return launch_i8<4, false>(tmA, tmB, p, grid, stream);
+    case 48: return launch_i8<6, false>(tmA, tmB, p, grid, stream);
+    default: return launch_i8<8, false>(tmA, tmB, p, grid, stream);
   }
 }
 

@@ -36,6 +36,7 @@ struct I8Params {
   int strip;              // rows of B per CTA (multiple of 16), the B box height
   int stages;
   int b_constant;         // 1: B may be read before the previous kernel on the stream completes
+  int w4;                 // 1: B is int4 (W4A8), packed as PACK_W4
 };
 
 void tc_tile_choice(int64_t M, int64_t N, int num_sms, int* bm, int* bn);
@@ -48,13 +49,16 @@ int mxf4_gemm_launch(const CUtensorMap& tmA, const CUtensorMap& tmC, TcParams p,
 int i8_strip_rows(int N, int num_sms);
 int i8_gemm_launch(const CUtensorMap& tmA, const CUtensorMap& tmB, I8Params p, int num_sms, cudaStream_t stream);
 
-// int8: 8-row bands and offset-binary bytes; otherwise 128-row bands, bytes as given
 int quant_launch(const void* X, bool x_bf16, int64_t M, int64_t K, bool to_e2m1, void* Q, void* S,
                  cudaStream_t stream);
 
-int pack_b_launch(const uint8_t* B, const uint8_t* Bsf, int64_t N, int64_t kbytes, int64_t nblk, bool int8,
+// Packed-B layouts: 128-row bands, bytes as given (tcgen05 types); 8-row
+// bands in offset binary (INT8); 8-row bands, interleaved offset-binary
+// nibbles (W4A8's int4 B).
+enum PackLayout : int { PACK_TC = 0, PACK_INT8 = 1, PACK_W4 = 2 };
+int pack_b_launch(const uint8_t* B, const uint8_t* Bsf, int64_t N, int64_t kbytes, int64_t nblk, int layout,
                   uint8_t* out, cudaStream_t stream);
-int unpack_b_launch(const uint8_t* packed, int64_t N, int64_t kbytes, int64_t nblk, bool int8, uint8_t* B,
+int unpack_b_launch(const uint8_t* packed, int64_t N, int64_t kbytes, int64_t nblk, int layout, uint8_t* B,
                     uint8_t* Bsf, cudaStream_t stream);
 
 }  // namespace gp

@@ -10,7 +10,9 @@
 //     Tile (tn, tk) is the R*128-byte block tn*(Kb/128) + tk, so the K tiles
 //     of one band are contiguous.
 //   - INT8 bytes are stored in offset binary (b XOR 0x80 = b + 128 as an
-//     unsigned byte), the form the INT8 kernel hands to the MMA.
+//     unsigned byte), the form the INT8 kernel hands to the MMA.  W4A8's
+//     int4 B uses the same 8-row bands, with the nibbles of each 32-bit
+//     word in offset binary and interleaved (w4_interleave).
 //   - Row r of a tile lives at r*128.  Its 16-byte chunk c is stored at slot
 //     c ^ (r % 8).  This is the 128-byte-swizzled K-major image that tcgen05
 //     descriptors and TMA use, so one bulk copy lands a tile in shared memory
@@ -39,35 +41,62 @@ __device__ __forceinline__ int64_t packed_scale_offset(int64_t n, int64_t j, int
   return group * 512 + (r & 31) * 16 + (r >> 5) * 4 + (jj & 3);
 }
 
+// W4A8's int4 B: a 32-bit word of a row holds k0..k7 (two's complement
+// nibbles at bits 4k).  Packed, each becomes u = b + 8 and k0..k7 move to
+// bits 0, 16, 4, 20, 8, 24, 12, 28: (word >> 4j) & 0x000F000F is then the
+// pair (k2j, k2j+1) as two fp16 bit patterns.
+__device__ __forceinline__ uint32_t w4_interleave(uint32_t w) {
+  uint32_t out = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    out |= ((w >> (8 * j)) & 0xFu) << (4 * j);             // k = 2j
+    out |= ((w >> (8 * j + 4)) & 0xFu) << (16 + 4 * j);    // k = 2j + 1
+  }
+  return out ^ 0x88888888u;
+}
+
+__device__ __forceinline__ uint32_t w4_deinterleave(uint32_t w) {
+  w ^= 0x88888888u;
+  uint32_t out = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    out |= ((w >> (4 * j)) & 0xFu) << (8 * j);
+    out |= ((w >> (16 + 4 * j)) & 0xFu) << (8 * j + 4);
+  }
+  return out;
+}
+
 // One thread per 16-byte chunk of B.
 __global__ void pack_data_kernel(const uint4* __restrict__ B, int64_t N, int64_t kbytes, int rshift, uint32_t bias,
-                                 uint8_t* __restrict__ out) {
+                                 bool w4, uint8_t* __restrict__ out) {
   const int64_t chunks_per_row = kbytes >> 4;
   const int64_t total = N * chunks_per_row;
   const int64_t ktiles = kbytes >> 7;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t n = i / chunks_per_row, cc = i - n * chunks_per_row;
     uint4 v = B[i];
-    v.x ^= bias;
-    v.y ^= bias;
-    v.z ^= bias;
-    v.w ^= bias;
+    if (w4) {
+      v.x = w4_interleave(v.x), v.y = w4_interleave(v.y), v.z = w4_interleave(v.z), v.w = w4_interleave(v.w);
+    } else {
+      v.x ^= bias, v.y ^= bias, v.z ^= bias, v.w ^= bias;
+    }
     *reinterpret_cast<uint4*>(out + packed_chunk_offset(n, cc, ktiles, rshift)) = v;
   }
 }
 
 __global__ void unpack_data_kernel(const uint8_t* __restrict__ in, int64_t N, int64_t kbytes, int rshift,
-                                   uint32_t bias, uint4* __restrict__ B) {
+                                   uint32_t bias, bool w4, uint4* __restrict__ B) {
   const int64_t chunks_per_row = kbytes >> 4;
   const int64_t total = N * chunks_per_row;
   const int64_t ktiles = kbytes >> 7;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t n = i / chunks_per_row, cc = i - n * chunks_per_row;
     uint4 v = *reinterpret_cast<const uint4*>(in + packed_chunk_offset(n, cc, ktiles, rshift));
-    v.x ^= bias;
-    v.y ^= bias;
-    v.z ^= bias;
-    v.w ^= bias;
+    if (w4) {
+      v.x = w4_deinterleave(v.x), v.y = w4_deinterleave(v.y), v.z = w4_deinterleave(v.z), v.w = w4_deinterleave(v.w);
+    } else {
+      v.x ^= bias, v.y ^= bias, v.z ^= bias, v.w ^= bias;
+    }
     B[i] = v;
   }
 }
@@ -95,24 +124,24 @@ static int grid_for(int64_t total, int threads) {
   return (int)g;
 }
 
-int pack_b_launch(const uint8_t* B, const uint8_t* Bsf, int64_t N, int64_t kbytes, int64_t nblk, bool int8,
+int pack_b_launch(const uint8_t* B, const uint8_t* Bsf, int64_t N, int64_t kbytes, int64_t nblk, int layout,
                   uint8_t* out, cudaStream_t stream) {
   const int64_t chunks = N * (kbytes >> 4);
-  const int rshift = int8 ? 3 : 7;
-  const uint32_t bias = int8 ? 0x80808080u : 0u;
+  const int rshift = layout == PACK_TC ? 7 : 3;
+  const uint32_t bias = layout == PACK_INT8 ? 0x80808080u : 0u;
   pack_data_kernel<<<grid_for(chunks, 256), 256, 0, stream>>>(reinterpret_cast<const uint4*>(B), N, kbytes, rshift,
-                                                              bias, out);
+                                                              bias, layout == PACK_W4, out);
   if (Bsf != nullptr)
     pack_scale_kernel<<<grid_for(N * nblk, 256), 256, 0, stream>>>(Bsf, N, nblk, out + N * kbytes);
   return cudaGetLastError() == cudaSuccess ? GP_OK : GP_ERR_CUDA;
 }
 
-int unpack_b_launch(const uint8_t* packed, int64_t N, int64_t kbytes, int64_t nblk, bool int8, uint8_t* B,
+int unpack_b_launch(const uint8_t* packed, int64_t N, int64_t kbytes, int64_t nblk, int layout, uint8_t* B,
                     uint8_t* Bsf, cudaStream_t stream) {
   const int64_t chunks = N * (kbytes >> 4);
-  const int rshift = int8 ? 3 : 7;
-  const uint32_t bias = int8 ? 0x80808080u : 0u;
-  unpack_data_kernel<<<grid_for(chunks, 256), 256, 0, stream>>>(packed, N, kbytes, rshift, bias,
+  const int rshift = layout == PACK_TC ? 7 : 3;
+  const uint32_t bias = layout == PACK_INT8 ? 0x80808080u : 0u;
+  unpack_data_kernel<<<grid_for(chunks, 256), 256, 0, stream>>>(packed, N, kbytes, rshift, bias, layout == PACK_W4,
                                                                 reinterpret_cast<uint4*>(B));
   if (Bsf != nullptr)
     unpack_scale_kernel<<<grid_for(N * nblk, 256), 256, 0, stream>>>(packed + N * kbytes, N, nblk, Bsf);

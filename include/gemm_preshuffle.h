@@ -57,7 +57,10 @@ typedef enum gp_dtype {
   GP_E2M1 = 3,
   GP_INT32 = 4,
   GP_FP16 = 5,                /* IEEE binary16 */
-  GP_FP32 = 6                 /* IEEE binary32 (quantiser input only) */
+  GP_FP32 = 6,                /* IEEE binary32 (quantiser input only) */
+  GP_W4A8 = 7                 /* int4 B (two's complement nibbles, two per byte, even k
+                                 low) with int8 A; "GEMM Optimization Guide" section 8.2
+                                 counts N*K//2 bytes for such a B */
 } gp_dtype;
 
 /* How operand scales enter the product. */
@@ -77,8 +80,9 @@ typedef enum gp_scale_mode {
  * scales for E2M1, with no padding.
  *
  * Shape rules: N % 128 == 0 and K*element_bits/8 % 128 == 0.  For the
- * element types that means K % 128 (E4M3, INT8), K % 64 (BF16, FP16) and K % 256
- * (E2M1).  Returns GP_ERR_SHAPE otherwise.  Host-only call.
+ * element types that means K % 128 (E4M3, INT8), K % 64 (BF16, FP16) and
+ * K % 256 (E2M1, and W4A8, whose packed B holds the int4 weights).
+ * Returns GP_ERR_SHAPE otherwise.  Host-only call.
  */
 int gemm_packed_b_bytes(int dtype, int64_t N, int64_t K, size_t* bytes_out);
 
@@ -91,11 +95,14 @@ int gemm_packed_b_bytes(int dtype, int64_t N, int64_t K, size_t* bytes_out);
  *
  * Layout of the packed buffer (a bijection of B's bytes):
  *   - B's bytes are cut into tiles of R rows x 128 bytes, with R = 128 for
- *     BF16, E4M3 and E2M1 and R = 8 for INT8.  The tile of (row band tn,
+ *     BF16, E4M3 and E2M1 and R = 8 for INT8 and W4A8.  The tile of (row band tn,
  *     byte column tk) is the R*128-byte block with index tn*(Kb/128)+tk,
  *     where Kb = row bytes.
  *   - INT8 bytes are stored in offset binary: b XOR 0x80, i.e. b + 128 as
- *     an unsigned byte.
+ *     an unsigned byte.  W4A8's int4 B also uses 8-row bands; each 32-bit
+ *     word of a row (8 K values, two's complement nibbles at bits 4k) is
+ *     stored with every nibble in offset binary (b + 8) and k0..k7 at bits
+ *     0, 16, 4, 20, 8, 24, 12, 28.
  *   - Inside a tile, row r sits at r*128.  Its 16-byte chunk c is stored at
  *     chunk slot c ^ (r % 8).  That is the 128-byte-swizzled K-major image
  *     that tcgen05 and TMA use, so one bulk copy moves a 128-row tile into
@@ -138,12 +145,14 @@ int gemm_unpack_b(const void* B_packed, int dtype, int64_t N, int64_t K, void* B
  *   (GP_E4M3, GP_SCALE_NONE,          FOUT)
  *   (GP_E2M1, GP_SCALE_BLOCK32_UE8M0, FOUT)      block scales applied inside the MMA
  *   (GP_INT8, GP_SCALE_NONE,          GP_INT32)  exact integer result
+ *   (GP_W4A8, GP_SCALE_NONE,          GP_INT32)  exact integer result; A is int8 [M, K],
+ *                                                B int4 [N, K/2] bytes (packed as W4A8)
  * Other combinations return GP_ERR_UNSUPPORTED.
  *
  * Shape rules: M >= 1 (any value), N and K as for gemm_packed_b_bytes, and
  * M, N, K < 2^31.  E2M1 also needs N % 256 == 0 (its tiles are 256 wide).
  * For INT8 the exact result must fit int32, which holds for every input
- * when K <= 131072.
+ * when K <= 131072 (W4A8: K <= 2097152).
  * Float outputs are rounded to nearest-even from the fp32 value (an fp16
  * output saturates to infinity beyond 65504, as IEEE rounding does).
  * The call launches one kernel and allocates no memory.  K == 0 writes

@@ -61,7 +61,7 @@ def check(ops, C, rows=None):
     ref = oracle.gemm_operands(ops, rows=rows)
     if rows is not None:
         c = c[rows]
-    if ops.dtype == "int8":
+    if ops.dtype in ("int8", "w4a8"):
         assert np.array_equal(c, ref), f"{int((c != ref).sum())} mismatching int32 outputs"
     else:
         err = oracle.max_rel_err(c, ref)
@@ -72,7 +72,8 @@ def check(ops, C, rows=None):
 # ---------------------------------------------------------------- packing
 
 @pytest.mark.parametrize("dtype,N,K", [("e4m3", 256, 512), ("int8", 384, 1024), ("bf16", 128, 192),
-                                       ("e2m1", 256, 1024), ("int8", 7168, 4096), ("fp16", 256, 320)])
+                                       ("e2m1", 256, 1024), ("int8", 7168, 4096), ("fp16", 256, 320),
+                                       ("w4a8", 384, 1024), ("w4a8", 7168, 4096)])
 def test_pack_matches_oracle_layout_and_roundtrips(dtype, N, K):
     ops = inputs.make_operands(dtype, 1, N, K, seed=123)
     _, B, _, sb = dev(ops)
@@ -98,6 +99,8 @@ SMALL = [
     ("int8", 16, 7168, 4096),
     ("e2m1", 1, 256, 256), ("e2m1", 200, 512, 512), ("e2m1", 129, 256, 1024), ("e2m1", 300, 768, 2048),
     ("fp16", 1, 128, 64), ("fp16", 257, 384, 512), ("fp16", 64, 256, 4096), ("fp16", 700, 640, 320),
+    ("w4a8", 1, 128, 256), ("w4a8", 37, 256, 512), ("w4a8", 16, 384, 256), ("w4a8", 100, 1152, 1280),
+    ("w4a8", 16, 7168, 4096),
 ]
 
 
@@ -143,7 +146,8 @@ def sample_rows(M, n=32, seed=0):
     return np.array(sorted(r))
 
 
-@pytest.mark.parametrize("name", ["fp8_128x256x512", "int8_16x7168x4096", "bf16_512x4096x4096"])
+@pytest.mark.parametrize("name", ["fp8_128x256x512", "int8_16x7168x4096", "bf16_512x4096x4096",
+                                  "w4a8_16x7168x4096"])
 def test_workload_full_compare(name):
     ops = inputs.workload_operands(name)
     check(ops, gpu_gemm(ops))
@@ -193,6 +197,23 @@ def test_int8_extremes_bit_exact():
     rng = np.random.default_rng(0)
     a[3:] = rng.choice(np.array([-128, 127, 0, 1, -1], np.int8), size=(M - 3, K))
     ops = inputs.Operands("int8", M, N, K, a, b)
+    check(ops, gpu_gemm(ops))
+
+
+def test_w4a8_extremes_bit_exact():
+    M, N, K = 16, 256, 4096
+    a = np.full((M, K), -128, np.int8)
+    b = np.full((N, K), -8, np.int8)
+    a[1] = 127
+    b[1] = 7
+    a[2, ::2] = 127                       # alternating signs: large cancellation
+    b[2, 1::2] = -7
+    rng = np.random.default_rng(1)
+    a[3:] = rng.choice(np.array([-128, 127, 0, 1, -1], np.int8), size=(M - 3, K))
+    b[3:] = rng.choice(np.array([-8, 7, 0, 1, -1], np.int8), size=(N - 3, K))
+    nib = (b.astype(np.int16) & 0xF).astype(np.uint8)
+    bp = nib[:, 0::2] | (nib[:, 1::2] << 4)
+    ops = inputs.Operands("w4a8", M, N, K, a, bp)
     check(ops, gpu_gemm(ops))
 
 
@@ -253,6 +274,7 @@ def test_repeatable_bitwise():
 
 @pytest.mark.parametrize("dtype,M,N,K", [
     ("int8", 16, 7168, 4096), ("int8", 37, 256, 384), ("int8", 16, 384, 128),
+    ("w4a8", 16, 7168, 4096), ("w4a8", 37, 256, 512),
     ("e4m3", 300, 512, 1024), ("e4m3", 17, 384, 256), ("bf16", 257, 384, 512),
     ("e2m1", 200, 512, 512), ("e2m1", 129, 256, 256),
     ("bf16", 400, 4096, 8192),   # split-K cluster path
