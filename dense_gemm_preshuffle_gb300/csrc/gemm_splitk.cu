@@ -18,7 +18,8 @@
 //     stages each 4 KiB block in its local buffer, with a row-XOR swizzle of
 //     the 16-byte chunks, so the owner's reads are free of bank conflicts.
 //     One cp.async.bulk shared::cta -> shared::cluster copy moves the block
-//     into the owner's ring (many small remote stores measured ~10x slower).
+//     into the owner's ring.  Remote stores from registers measured slower:
+//     st.shared::cluster ~10x, st.async ~1.3x the whole product's time.
 //     The copy completes its bytes on the owner's receive barrier, which
 //     the owner armed with the total it expects.
 //   - Owner epilogue: the owner adds its own partial and the SPLIT-1
@@ -58,11 +59,6 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
   return r;
-}
-
-__device__ __forceinline__ void st_cluster_v4(uint32_t caddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(caddr), "r"(a), "r"(b), "r"(c), "r"(d)
-               : "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t caddr) {
@@ -355,6 +351,10 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
+  // No CTA leaves while a peer may still write into its ring (after a
+  // bounded wait gave up, copies may still be in flight); every thread gets
+  // here, since all waits above are bounded.
+  cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc<512>(tmem_base);
@@ -396,13 +396,17 @@ int splitk_choice(int64_t M, int64_t N, int64_t ktiles, int num_sms) {
   // few microseconds per tile (measured ~5 us for 192 KiB per SM), so it
   // pays off only against a long main loop (at 16 steps per CTA the 128 x 128
   // tile path was faster: 21 us vs 23.5 us at 512 x 4096 x 4096 bf16).
-  // GP_SPLITK=0 disables the path.
+  // GP_SPLITK=0 disables the path; GP_SPLITK=2 or 4 forces that split
+  // where it is valid (for sweeps).
   static const int mode = [] {
     const char* e = std::getenv("GP_SPLITK");
     return e == nullptr ? -1 : std::atoi(e);
   }();
   if (mode == 0 || N % SK_BN != 0) return 1;
   const int64_t tiles = ((M + SK_BM - 1) / SK_BM) * (N / SK_BN);
+  if (mode == 2 || mode == 4) {  // forced split (sweeps), where it is valid
+    return (tiles * mode <= num_sms && ktiles % mode == 0 && ktiles / mode >= 4) ? mode : 1;
+  }
   for (int split : {4, 2}) {
     if (tiles * split <= num_sms && tiles * split * 2 > num_sms && ktiles % split == 0 && ktiles / split >= 32)
       return split;
