@@ -32,6 +32,7 @@ DTYPES = {"bf16": 0, "e4m3": 1, "int8": 2, "e2m1": 3, "int32": 4, "fp16": 5, "fp
 SCALE_MODES = {"none": 0, "rowcol_f32": 1, "block32_ue8m0": 2}
 GP_RUN_DEFAULT = 0
 GP_RUN_B_CONSTANT = 1
+GP_RUN_INDEPENDENT = 2
 EPILOGUES = {"none": 0, "bias": 1, "bias_relu": 2, "bias_silu": 3, "bias_gelu": 4}
 
 _lib = None
@@ -196,7 +197,8 @@ def preshuffle_b(B, dtype, B_scales=None, stream=None):
 
 
 def matmul(A, B_packed, dtype, N: int, K: int, scale_a=None, scale_b=None, out=None, stream=None,
-           b_constant: bool = False, epilogue: str = "none", bias=None, out_dtype: Optional[str] = None):
+           b_constant: bool = False, epilogue: str = "none", bias=None, out_dtype: Optional[str] = None,
+           independent: bool = False):
     """C = A . B^T with B packed; returns [M, N] in out_dtype ("bf16" or
     "fp16"; default fp16 for fp16 operands, bf16 for the other float types),
     int32 for int8.
@@ -204,7 +206,9 @@ def matmul(A, B_packed, dtype, N: int, K: int, scale_a=None, scale_b=None, out=N
     epilogue: "none", "bias", "bias_relu", "bias_silu" or "bias_gelu", with
     bias an fp32 [N] device tensor for all but "none".
     b_constant=True passes GP_RUN_B_CONSTANT: B_packed must not be written
-    by any GPU work still in flight (pack once, then synchronise)."""
+    by any GPU work still in flight (pack once, then synchronise).
+    independent=True passes GP_RUN_INDEPENDENT: no GPU work still in flight
+    writes any operand of the call or touches `out`."""
     import torch
     d = _dt(dtype)
     M = A.shape[0]
@@ -222,5 +226,6 @@ def matmul(A, B_packed, dtype, N: int, K: int, scale_a=None, scale_b=None, out=N
     if out is None:
         out = torch.empty((M, N), dtype=tdt, device=A.device)
     gemm_run_ex(A, B_packed, d, M, N, K, mode, scale_a, scale_b, epilogue, bias, out, c_dtype,
-                GP_RUN_B_CONSTANT if b_constant else GP_RUN_DEFAULT, stream)
+                (GP_RUN_B_CONSTANT if b_constant else GP_RUN_DEFAULT) | (GP_RUN_INDEPENDENT if independent else 0),
+                stream)
     return out

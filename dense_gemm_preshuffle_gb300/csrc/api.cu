@@ -208,8 +208,9 @@ int gemm_run(const void* A, const void* B_packed, int dtype, int64_t M, int64_t 
 int gemm_run_ex(const void* A, const void* B_packed, int dtype, int64_t M, int64_t N, int64_t K, int scale_mode,
                 const void* scale_a, const void* scale_b, int epilogue, const void* bias, void* C, int c_dtype,
                 unsigned flags, void* stream) {
-  if ((flags & ~(unsigned)GP_RUN_B_CONSTANT) != 0) return GP_ERR_INVALID_ARG;
-  const int b_constant = (flags & GP_RUN_B_CONSTANT) ? 1 : 0;
+  if ((flags & ~(unsigned)(GP_RUN_B_CONSTANT | GP_RUN_INDEPENDENT)) != 0) return GP_ERR_INVALID_ARG;
+  const int independent = (flags & GP_RUN_INDEPENDENT) ? 1 : 0;
+  const int b_constant = (flags & GP_RUN_B_CONSTANT) || independent ? 1 : 0;
   if (epilogue < GP_EPI_NONE || epilogue > GP_EPI_BIAS_GELU) return GP_ERR_INVALID_ARG;
   if ((epilogue == GP_EPI_NONE) != (bias == nullptr)) return GP_ERR_INVALID_ARG;
   const bool float_out = c_dtype == GP_BF16 || c_dtype == GP_FP16;
@@ -276,6 +277,7 @@ int gemm_run_ex(const void* A, const void* B_packed, int dtype, int64_t M, int64
     p.ktiles = (int)(K / 128);  // 128-element K tiles of A (int8: K bytes a row)
     p.strip = i8_strip_rows((int)N, d->num_sms);
     p.b_constant = b_constant;
+    p.independent = independent;
     p.w4 = w4 ? 1 : 0;
     const int64_t b_tiles = kb / 128;  // 128-byte tiles of a packed B row (256 K values for int4)
     // A as [K tiles][M rows][128 B] (3-D view, 128-byte swizzle): one copy

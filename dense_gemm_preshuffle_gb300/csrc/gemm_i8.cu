@@ -128,6 +128,7 @@ __global__ void __launch_bounds__(I8_THREADS, i8_ctas_per_sm(NB8))
     const uint32_t need = (uint32_t)(reinterpret_cast<const volatile uint8_t*>(abort_flag + 1) - smem_raw);
     if (nu < 1 || mg * 16 >= p.M || p.ktiles < 1 || need > dyn || (int)blockDim.x != I8_THREADS) {
       if (threadIdx.x == 0) atomicOr(p.status, ST_BAD_LAUNCH);
+      pdl_wait();  // complete after the previous kernel all the same
       return;
     }
   }
@@ -164,6 +165,9 @@ __global__ void __launch_bounds__(I8_THREADS, i8_ctas_per_sm(NB8))
   };
   // With constant weights the ring's first stages of B are requested before
   // the wait on the previous kernel; the rest of the strip is warmed in L2.
+  // An independent call (which implies constant weights) does not wait
+  // here at all: its whole body runs alongside the previous kernel, and it
+  // waits for that kernel at exit.
   const int early = p.b_constant ? min(nstages, I8_STAGES) : 0;
   if (threadIdx.x == I8_PRODUCER * 32) {
     // A prefetch is only a cache hint: safe while the previous kernel runs.
@@ -186,7 +190,7 @@ __global__ void __launch_bounds__(I8_THREADS, i8_ctas_per_sm(NB8))
   __syncthreads();
   if (threadIdx.x == I8_PRODUCER * 32)
     for (int q = 0; q < early; ++q) load_b(q);
-  pdl_wait();  // A may be produced, and C read, by the previous kernel
+  if (!p.independent) pdl_wait();  // A may be produced, and C read, by the previous kernel
 
   if (warp == I8_PRODUCER) {
     // ------------------------------------------------------------ producers
@@ -360,6 +364,9 @@ __global__ void __launch_bounds__(I8_THREADS, i8_ctas_per_sm(NB8))
     const int gm = mg * 16 + m;
     if (gm < p.M) p.C[(size_t)gm * p.N + n0 + n] = sum;
   }
+  // An independent call completes only after the kernel before it, so a
+  // later kernel's wait on this one covers everything earlier on the stream.
+  if (p.independent) pdl_wait();
 }
 
 // Tuning override, read once per process: GP_I8_STRIP (rows of B per CTA:

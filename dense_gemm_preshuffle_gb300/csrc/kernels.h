@@ -36,6 +36,7 @@ struct I8Params {
   int strip;              // rows of B per CTA (multiple of 16), the B box height
   int stages;
   int b_constant;         // 1: B may be read before the previous kernel on the stream completes
+  int independent;        // 1: nothing in flight touches the operands; wait for the previous kernel only at exit
   int w4;                 // 1: B is int4 (W4A8), packed as PACK_W4
 };
 

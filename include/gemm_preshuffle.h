@@ -186,7 +186,19 @@ typedef enum gp_run_flags {
    * finished, which hides its pipeline start behind that kernel's tail.  A,
    * the scales and C are still touched only after the preceding kernel
    * completes.  Breaking the condition gives undefined results. */
-  GP_RUN_B_CONSTANT = 1
+  GP_RUN_B_CONSTANT = 1,
+  /* The call is independent of the GPU work before it on `stream`: nothing
+   * that may still be running when the call is made writes A, B_packed,
+   * the scales or bias, or reads or writes C (for instance a run of GEMMs on
+   * weights of their own, into outputs of their own, whose activations were
+   * produced before the run).  The weight-streaming INT8/W4A8 kernel then
+   * runs its whole body alongside the preceding kernel and waits for that
+   * kernel only before it exits, so its completion still follows the
+   * completion of everything before it and work queued after the call sees
+   * every earlier result.  The tcgen05 kernels take this flag as
+   * GP_RUN_B_CONSTANT.  Implies GP_RUN_B_CONSTANT; breaking the condition
+   * gives undefined results. */
+  GP_RUN_INDEPENDENT = 2
 } gp_run_flags;
 
 /*
@@ -199,10 +211,10 @@ typedef enum gp_run_flags {
  * bias     : device, fp32 [N], 16-byte aligned; required for every epilogue
  *            but GP_EPI_NONE, and NULL with it (else GP_ERR_INVALID_ARG).
  * flags    : a bitwise OR of gp_run_flags.  Unknown bits return
- *            GP_ERR_INVALID_ARG before any launch.  GP_RUN_B_CONSTANT is a
- *            scheduling option of this library: the method itself only
- *            assumes that the packed weights are produced once, offline
- *            ("GEMM Optimization Guide" section 12).
+ *            GP_ERR_INVALID_ARG before any launch.  GP_RUN_B_CONSTANT and
+ *            GP_RUN_INDEPENDENT are scheduling options of this library: the
+ *            method itself only assumes that the packed weights are
+ *            produced once, offline ("GEMM Optimization Guide" section 12).
  * The other arguments are as for gemm_run.  With K == 0 the product is
  * zero, so every row of C is act(bias[n]) (a broadcast kernel).
  */

@@ -95,12 +95,16 @@ def test_empty_problem_is_a_noop(lib):
 
 def test_run_ex_rejects_unknown_flags(lib):
     rc = lib.gemm_run_ex(FAKE, FAKE, gp.DTYPES["e4m3"], 16, 256, 512, 0, None, None, 0, None, FAKE,
-                         gp.DTYPES["bf16"], 2, None)
+                         gp.DTYPES["bf16"], 4, None)
     assert rc == 1
     # the known flag passes validation; a shape error is still reported first-class
     rc = lib.gemm_run_ex(FAKE, FAKE, gp.DTYPES["e4m3"], 16, 100, 512, 0, None, None, 0, None, FAKE,
                          gp.DTYPES["bf16"], gp.GP_RUN_B_CONSTANT, None)
     assert rc == 3
+    for f in (gp.GP_RUN_INDEPENDENT, gp.GP_RUN_B_CONSTANT | gp.GP_RUN_INDEPENDENT):
+        rc = lib.gemm_run_ex(FAKE, FAKE, gp.DTYPES["int8"], 16, 100, 512, 0, None, None, 0, None, FAKE,
+                             gp.DTYPES["int32"], f, None)
+        assert rc == 3
 
 
 @pytest.mark.parametrize("epi,bias,dtype,c_dtype,code", [

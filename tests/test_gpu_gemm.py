@@ -328,6 +328,73 @@ def test_b_constant_reads_a_only_after_previous_kernel(M, N1, K1, N2):
     check(ops1, C1, rows=sample_rows(M, 16, seed=6))
 
 
+# ---------------------------------------------------------------- independent-call scheduling flag
+
+@pytest.mark.parametrize("dtype,M,N,K", [
+    ("int8", 16, 7168, 4096), ("int8", 37, 256, 384), ("int8", 16, 384, 128),
+    ("w4a8", 16, 7168, 4096), ("w4a8", 37, 256, 512),
+    ("e4m3", 300, 512, 1024), ("bf16", 257, 384, 512),   # tcgen05 kernels: taken as B constant
+], ids=lambda v: str(v))
+def test_independent_run_matches_default(dtype, M, N, K):
+    """A run of GP_RUN_INDEPENDENT calls on weights and outputs of their own
+    overlaps the calls; every output is bit-identical to the plain call."""
+    ops = inputs.make_operands(dtype, M, N, K, seed=4100 + M + N + K)
+    A, B, sa, sb = dev(ops)
+    Bp = gp.preshuffle_b(B, dtype)
+    copies = [Bp] + [Bp.clone() for _ in range(3)]
+    torch.cuda.synchronize()
+    ref = gp.matmul(A, Bp, dtype, N, K, scale_a=sa, scale_b=sb)
+    torch.cuda.synchronize()
+    for trial in range(2):
+        outs = [gp.matmul(A, copies[i % 4], dtype, N, K, scale_a=sa, scale_b=sb, independent=True)
+                for i in range(12)]
+        torch.cuda.synchronize()
+        assert gp.gemm_last_device_status() == 0
+        for C in outs:
+            if C.dtype == torch.int32:
+                assert torch.equal(C, ref)
+            else:
+                assert torch.equal(C.view(torch.int16), ref.view(torch.int16))
+    rows = None if M * N <= 1 << 21 else sample_rows(M, 24, seed=7)
+    check(ops, outs[-1], rows=rows)
+
+
+def test_independent_run_keeps_stream_order():
+    """A long plain INT8 call writes C_a; three short independent calls
+    follow; then a plain call reads C_a (its bytes as int8 activations).
+    The independent calls wait for their predecessor before exiting, so the
+    last call's wait on them also covers C_a."""
+    Ma, Na, Ka = 16, 7168, 65536
+    opsa = inputs.make_operands("int8", Ma, Na, Ka, seed=91)
+    Aa, Ba, _, _ = dev(opsa)
+    Bpa = gp.preshuffle_b(Ba, "int8")
+    opsb = inputs.make_operands("int8", 16, 384, 256, seed=92)
+    Ab, Bb, _, _ = dev(opsb)
+    Bpb = gp.preshuffle_b(Bb, "int8")
+    Kc, Nc = 4 * Na, 256
+    opsc = inputs.make_operands("int8", Ma, Nc, Kc, seed=93)
+    _, Bc, _, _ = dev(opsc)
+    Bpc = gp.preshuffle_b(Bc, "int8")
+    torch.cuda.synchronize()
+    ref_b = gp.matmul(Ab, Bpb, "int8", 384, 256)
+    for trial in range(3):
+        Ca = torch.full((Ma, Na), 0x7F7F7F7F, dtype=torch.int32, device="cuda")
+        gp.matmul(Aa, Bpa, "int8", Na, Ka, out=Ca, b_constant=True)
+        outs_b = [gp.matmul(Ab, Bpb, "int8", 384, 256, independent=True) for _ in range(3)]
+        Cc = gp.matmul(Ca.view(torch.int8), Bpc, "int8", Nc, Kc, b_constant=True)
+        torch.cuda.synchronize()
+        assert gp.gemm_last_device_status() == 0
+        again = gp.matmul(Ca.view(torch.int8), Bpc, "int8", Nc, Kc)
+        torch.cuda.synchronize()
+        assert torch.equal(Cc, again)
+        for C in outs_b:
+            assert torch.equal(C, ref_b)
+    # C_a itself, on a few columns, against the oracle
+    cols = np.arange(0, Na, 997)
+    want = (opsa.a.astype(np.int64) @ opsa.b[cols].astype(np.int64).T)
+    assert np.array_equal(Ca.cpu().numpy()[:, cols].astype(np.int64), want)
+
+
 # ---------------------------------------------------------------- fused epilogues
 
 EPI_SHAPES = [("bf16", 257, 384, 512), ("e4m3", 300, 512, 1024), ("e2m1", 200, 512, 512), ("e4m3", 17, 256, 256),
