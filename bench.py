@@ -30,6 +30,10 @@ it once per weight, not per product.
     beside the plain product's time.
   - "quantize": the activation quantiser (gemm_quantize_a) on the FP8 and
     MXFP4 workloads' A shapes, against the HBM roofline.
+  - "trials" (in the line and each "others" entry): 7 trials of 80
+    back-to-back steps; median, p10 and p90 of the time per step.
+  - "independent_stream": the INT8 and W4A8 workloads as runs of calls with
+    GP_RUN_INDEPENDENT (each on its own weights and output).
 """
 from __future__ import annotations
 
@@ -288,6 +292,37 @@ def time_device(prob: Problem, steps: int, warmup: int, pg, device, graph_len: i
     return e0.elapsed_time(e1) / 1e3
 
 
+def time_trials(prob, warmup: int, device, R: int = 80, n: int = 7):
+    """n trials of R back-to-back steps (one CUDA-graph replay each): the
+    median, p10 and p90 of the per-step device time, in microseconds."""
+    import torch
+    stream = torch.cuda.current_stream(device)
+    for i in range(max(3, warmup)):
+        prob.step(i)
+    torch.cuda.synchronize(device)
+    graph = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream(device)
+    s.wait_stream(stream)
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            for i in range(R):
+                prob.step(i)
+    stream.wait_stream(s)
+    graph.replay()
+    torch.cuda.synchronize(device)
+    per = []
+    for _ in range(n):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        graph.replay()
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        per.append(e0.elapsed_time(e1) * 1e3 / R)
+    q = np.percentile(np.array(per), [10, 50, 90])
+    return {"R": R, "n": n, "median_us": round(float(q[1]), 3), "p10_us": round(float(q[0]), 3),
+            "p90_us": round(float(q[2]), 3)}
+
+
 class QuantProblem:
     """gemm_quantize_a on an activation matrix [M, K] (rotating copies past L2)."""
 
@@ -444,6 +479,7 @@ def run_ours(args):
     else:
         e2e_sec, h2d, d2h = time_e2e(prob, e2e_steps, args.warmup, device)
         e2e_sec = max_over_ranks(pg, e2e_sec, device)
+    trials = time_trials(prob, args.warmup, device)
     clocks.stop()
 
     per = sec / args.steps
@@ -473,6 +509,7 @@ def run_ours(args):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_sec / e2e_steps * 1e3, 5), "steps": e2e_steps},
         "roofline": roofline(prob, per, peaks, peak_kind, traffic_from_profiles(prob.name)),
+        "trials": trials,
         "clocks": clock_summary,
         "pack_b": {"us": round(prob.pack_us, 2), "bytes": prob.packed_bytes,
                    "GB/s": round(2 * prob.packed_bytes / (prob.pack_us * 1e-6) / 1e9, 1)},
@@ -494,7 +531,8 @@ def run_ours(args):
                 others[name] = {"us_per_step": round(s2 / steps2 * 1e6, 3),
                                 "TFLOP/s": round(p2.flops * steps2 / s2 / 1e12, 2),
                                 "GB/s": round(p2.bytes * steps2 / s2 / 1e9, 1), "roofline": r,
-                                "steps": steps2, "pack_b_us": round(p2.pack_us, 2)}
+                                "steps": steps2, "pack_b_us": round(p2.pack_us, 2),
+                                "trials": time_trials(p2, args.warmup, device)}
                 del p2
                 torch.cuda.empty_cache()
             except Exception as e:  # a workload whose kernel is not built yet

@@ -262,6 +262,60 @@ def gemm_operands(ops, rows: Optional[np.ndarray] = None, cols: Optional[np.ndar
     raise ValueError(ops.dtype)
 
 
+def gemm_abs_operands(ops, rows: Optional[np.ndarray] = None, cols: Optional[np.ndarray] = None) -> np.ndarray:
+    """S[m,n] = sum_k |dq(A)[m,k]| |dq(B)[n,k]|, the magnitude that the
+    accumulation runs through: the denominator of the error diagnostic
+    max |C - C_ref| / S, in which bf16 output rounding contributes at most
+    2^-9 and an fp32 accumulation at most about K 2^-24 (the dequantised
+    operands are the same as in ``gemm_operands``; scales are positive)."""
+    a, b, sa, sb = ops.a, ops.b, ops.scale_a, ops.scale_b
+    if rows is not None:
+        a = a[rows]
+        sa = None if sa is None else sa[rows]
+    if cols is not None:
+        b = b[cols]
+        sb = None if sb is None else sb[cols]
+    if ops.dtype == "int8":
+        return gemm_f64(np.abs(a.astype(np.float64)), np.abs(b.astype(np.float64)))
+    if ops.dtype == "w4a8":
+        return gemm_f64(np.abs(a.astype(np.float64)), np.abs(unpack_int4_rows(b, ops.K).astype(np.float64)))
+    if ops.dtype == "bf16":
+        return gemm_f64(np.abs(decode_bf16(a)), np.abs(decode_bf16(b)))
+    if ops.dtype == "fp16":
+        return gemm_f64(np.abs(decode_fp16(a)), np.abs(decode_fp16(b)))
+    if ops.dtype == "e4m3":
+        acc = gemm_f64(np.abs(decode_e4m3(a)), np.abs(decode_e4m3(b)))
+        if sa is not None:
+            acc = acc * np.abs(np.asarray(sa, np.float64))[:, None]
+        if sb is not None:
+            acc = acc * np.abs(np.asarray(sb, np.float64))[None, :]
+        return acc
+    if ops.dtype == "e2m1":
+        K = ops.K
+        av = np.ascontiguousarray(np.abs(decode_e2m1(unpack_e2m1_rows(a, K))))
+        bv = np.ascontiguousarray(np.abs(decode_e2m1(unpack_e2m1_rows(b, K))))
+        M, N = av.shape[0], bv.shape[0]
+        c = np.empty((M, N), dtype=np.float64)
+        _load().oracle_gemm_block_f64(_p(av), _p(bv), _p(np.ascontiguousarray(decode_ue8m0(sa))),
+                                      _p(np.ascontiguousarray(decode_ue8m0(sb))), M, N, K, 32, _p(c))
+        return c
+    raise ValueError(ops.dtype)
+
+
+def max_err_over_abs(c: np.ndarray, c_ref: np.ndarray, s: np.ndarray) -> float:
+    """max |C - C_ref| / S with S from ``gemm_abs_operands`` (entries with
+    S = 0 must match exactly and count as 0)."""
+    c = np.asarray(c, np.float64)
+    r = np.asarray(c_ref, np.float64)
+    s = np.asarray(s, np.float64)
+    if c.size == 0:
+        return 0.0
+    d = np.abs(c - r)
+    if np.any((s == 0) & (d != 0)):
+        return float("inf")
+    return float(np.max(np.where(s > 0, d / np.where(s > 0, s, 1.0), 0.0)))
+
+
 # ----------------------------------------------------------------------------
 # Output rounding model and the parity metric
 # ----------------------------------------------------------------------------

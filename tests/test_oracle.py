@@ -648,3 +648,63 @@ def test_w4a8_pack_word_order():
     assert pk.size == bb.size
     il = oracle.interleave_int4_words(bb)
     assert np.array_equal(pk, oracle.pack_b_bytes(il, 8))
+
+
+# ---------------------------------------------------------------- error diagnostic denominator
+
+def _abs_sum_pins(dtype):
+    K = 256 if dtype == "e2m1" else 192
+    ops = inputs.make_operands(dtype, 9, 10, K, seed=71)
+    c = oracle.gemm_operands(ops).astype(np.float64)
+    s = oracle.gemm_abs_operands(ops)
+    assert np.all(s >= np.abs(c) - 1e-12 * s)
+    if dtype in ("int8", "w4a8"):
+        a = np.abs(ops.a.astype(np.int16)).clip(0, 127).astype(np.int8)
+        if dtype == "int8":
+            b = np.abs(ops.b.astype(np.int16)).clip(0, 127).astype(np.int8)
+        else:   # int4 nibbles 0..7 (non-negative), two per byte
+            b = (ops.b & 0x77).astype(np.uint8)
+        pos = inputs.Operands(dtype, 9, 10, K, a, b, None, None)
+    elif dtype in ("bf16", "fp16"):
+        pos = inputs.Operands(dtype, 9, 10, K, ops.a & 0x7FFF, ops.b & 0x7FFF, None, None)
+    elif dtype == "e4m3":
+        pos = inputs.Operands(dtype, 9, 10, K, ops.a & 0x7F, ops.b & 0x7F, ops.scale_a, ops.scale_b)
+    else:   # E2M1: clear the sign bit of both nibbles
+        pos = inputs.Operands(dtype, 9, 10, K, ops.a & 0x77, ops.b & 0x77, ops.scale_a, ops.scale_b)
+    assert np.array_equal(oracle.gemm_abs_operands(pos), oracle.gemm_operands(pos).astype(np.float64))
+
+
+@pytest.mark.parametrize("dtype", ["int8", "w4a8", "bf16", "fp16", "e4m3", "e2m1"])
+def test_abs_sum_bounds_and_equality_for_nonnegative_operands(dtype):
+    """S = sum |a||b| is at least |C| everywhere; with every operand value
+    non-negative it equals C (the same product with no cancellation)."""
+    _abs_sum_pins(dtype)
+
+
+def test_abs_sum_of_sign_matrices_is_k():
+    # A, B with entries +-1: every |a||b| is 1, so S = K while C varies
+    K = 128
+    rng = np.random.default_rng(9)
+    a = rng.choice(np.array([-1, 1], np.int8), size=(6, K))
+    b = rng.choice(np.array([-1, 1], np.int8), size=(7, K))
+    ops = inputs.Operands("int8", 6, 7, K, a, b, None, None)
+    assert np.all(oracle.gemm_abs_operands(ops) == K)
+    c = oracle.gemm_operands(ops)
+    assert oracle.max_err_over_abs(c + 1, c, np.full((6, 7), K)) == 1.0 / K
+
+
+@pytest.mark.parametrize("dtype", ["e4m3", "e2m1"])
+def test_planted_abs_sum_dropped_scale_is_caught(monkeypatch, dtype):
+    # an S that leaves out the scales of B must fail one of the pins
+    real = oracle.gemm_abs_operands
+
+    def dropped(ops, rows=None, cols=None):
+        if ops.dtype == "e4m3":
+            ops = inputs.Operands(ops.dtype, ops.M, ops.N, ops.K, ops.a, ops.b, ops.scale_a, None)
+        else:
+            ops = inputs.Operands(ops.dtype, ops.M, ops.N, ops.K, ops.a, ops.b, ops.scale_a,
+                                  np.full_like(ops.scale_b, 127))
+        return real(ops, rows, cols)
+    monkeypatch.setattr(oracle, "gemm_abs_operands", dropped)
+    with pytest.raises(AssertionError):
+        _abs_sum_pins(dtype)
