@@ -321,9 +321,23 @@ int gemm_run_ex(const void* A, const void* B_packed, int dtype, int64_t M, int64
       tc_tile_choice(M, N, d->num_sms, &bm, &bn);
   }
   CUtensorMap tmA, tmC;
-  if ((rc = encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, (uint64_t)kb, (uint64_t)M, (uint64_t)kb, 128,
-                      (uint32_t)bm, CU_TENSOR_MAP_SWIZZLE_128B)) != GP_OK)
-    return rc;
+  const int kstep = (dtype != GP_E2M1 && split == 1) ? tc_kstep(bm, bn) : 1;
+  if (kstep == 1) {
+    if ((rc = encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, (uint64_t)kb, (uint64_t)M, (uint64_t)kb, 128,
+                        (uint32_t)bm, CU_TENSOR_MAP_SWIZZLE_128B)) != GP_OK)
+      return rc;
+  } else {
+    // A as [K tiles][M rows][128 B] (3-D view, 128-byte swizzle): one copy
+    // brings `kstep` K tiles of a bm-row band.
+    cuuint64_t dims[3] = {128, (cuuint64_t)M, (cuuint64_t)(kb / 128)};
+    cuuint64_t strides[2] = {(cuuint64_t)kb, 128};
+    cuuint32_t box[3] = {128, (cuuint32_t)bm, (cuuint32_t)kstep};
+    cuuint32_t estr[3] = {1, 1, 1};
+    if (g_encode(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(A), dims, strides, box, estr,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return GP_ERR_CUDA;
+  }
   if ((rc = encode_2d(&tmC, c_dtype == GP_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, C, (uint64_t)N, (uint64_t)M, (uint64_t)N * 2, 64, 32,
                       CU_TENSOR_MAP_SWIZZLE_128B)) != GP_OK)
     return rc;

@@ -27,9 +27,11 @@
 //     A stage is therefore full after one producer arrival plus its
 //     transaction bytes and one arrival from warp 6.
 //   - TMEM: one 256-column fp32 accumulator, plus one scale slot per ring
-//     stage (A: 2 atoms x 4 columns; B: 2 atoms x 8 columns).  tcgen05.cp
-//     and tcgen05.mma issued by the same thread execute in order, so a
-//     stage's scale copy always lands before its MMAs read it.
+//     stage (A: 2 atoms x 4 columns; B: 2 atoms x 8 columns).  Warp 7
+//     copies a stage's scales into its slot (tcgen05.cp) as soon as the
+//     stage lands and commits them to the stage's "scales ready" barrier,
+//     which the MMA thread waits on; its own MMAs are then not held behind
+//     the copies.
 #include "kernels.h"
 #include "epilogue.cuh"
 #include "ptx.cuh"
@@ -38,7 +40,7 @@ namespace gp {
 
 namespace {
 
-constexpr int F4_THREADS = 224;  // producer, MMA, 4 epilogue warps, A-scale warp
+constexpr int F4_THREADS = 256;  // producer, MMA, 4 epilogue warps, A-scale warp, scale-copy warp
 constexpr int F4_BN = 256;
 constexpr int F4_STAGES = 4;
 constexpr int F4_SF_LOOKAHEAD = 2;  // stages the A-scale warp keeps in flight
@@ -104,7 +106,9 @@ __global__ void __launch_bounds__(F4_THREADS, 1)
   uint64_t* accf = empty + F4_STAGES;
   uint64_t* acce = accf + 1;
   uint64_t* drain = acce + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* sfr = drain + 1;             // [stage] scales of the stage are in TMEM
+  uint64_t* sfdrain = sfr + F4_STAGES;   // the scale-copy warp's copies have completed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sfdrain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -120,6 +124,8 @@ __global__ void __launch_bounds__(F4_THREADS, 1)
     mbar_init(accf, 1);
     mbar_init(acce, 4);
     mbar_init(drain, 1);
+    for (int s = 0; s < F4_STAGES; ++s) mbar_init(&sfr[s], 1);
+    mbar_init(sfdrain, 1);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tensormap(&tmA);
@@ -257,18 +263,14 @@ __global__ void __launch_bounds__(F4_THREADS, 1)
             ok = false;
             break;
           }
+          // the stage's scales are in TMEM (copied by warp 7)
+          if (!wait_bounded(&sfr[s], ph, abort_flag, p.status, ST_TIMEOUT_MMA, limit)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
           const uint32_t sfa_t = tmem_base + Cfg::SF_COL0 + s * (Cfg::SFA_COLS + Cfg::SFB_COLS);
           const uint32_t sfb_t = sfa_t + Cfg::SFA_COLS;
-          const uint32_t sfa_s = smem_u32(s_sfa + s * Cfg::SFA_BYTES);
-          const uint32_t sfb_s = smem_u32(s_sfb + s * Cfg::SFB_BYTES);
-#pragma unroll
-          for (int at = 0; at < 2; ++at) {
-            tmem_cp_32x128b_warpx4(sfa_t + at * 4, smem_desc_sf(sfa_s + at * 512));
-#pragma unroll
-            for (int j = 0; j < F4_BN / 128; ++j)
-              tmem_cp_32x128b_warpx4(sfb_t + at * (F4_BN / 32) + j * 4, smem_desc_sf(sfb_s + j * 1024 + at * 512));
-          }
           const uint32_t a0 = smem_u32(s_a + s * Cfg::A_BYTES);
           const uint32_t b0 = smem_u32(s_b + s * Cfg::B_BYTES);
 #pragma unroll
@@ -290,6 +292,49 @@ __global__ void __launch_bounds__(F4_THREADS, 1)
       umma_commit(drain);
       volatile int never = 0;
       wait_bounded(drain, 0, &never, p.status, ST_TIMEOUT_DRAIN, limit);
+    }
+  } else if (warp == 7) {
+    // ------------------------------------------------------------ scale-copy warp
+    // One lane copies each stage's scales from shared memory into that
+    // stage's TMEM slot as soon as the stage lands, and commits the copies
+    // to sfr[s].  The MMA thread then finds them in place: copies issued
+    // from its own thread, right before the MMAs that read them, held the
+    // tensor pipe (measured: 11% of the MXFP4 product).  A slot is free
+    // again when its stage is refilled, since the producer refills a stage
+    // only after the MMAs that read its slot have completed.
+    if (lane == 0) {
+      int s = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+        for (int kt = 0; kt < p.ktiles; ++kt) {
+          if (!wait_bounded(&full[s], ph, abort_flag, p.status, ST_TIMEOUT_MMA, limit)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sfa_t = tmem_base + Cfg::SF_COL0 + s * (Cfg::SFA_COLS + Cfg::SFB_COLS);
+          const uint32_t sfb_t = sfa_t + Cfg::SFA_COLS;
+          const uint32_t sfa_s = smem_u32(s_sfa + s * Cfg::SFA_BYTES);
+          const uint32_t sfb_s = smem_u32(s_sfb + s * Cfg::SFB_BYTES);
+#pragma unroll
+          for (int at = 0; at < 2; ++at) {
+            tmem_cp_32x128b_warpx4(sfa_t + at * 4, smem_desc_sf(sfa_s + at * 512));
+#pragma unroll
+            for (int j = 0; j < F4_BN / 128; ++j)
+              tmem_cp_32x128b_warpx4(sfb_t + at * (F4_BN / 32) + j * 4, smem_desc_sf(sfb_s + j * 1024 + at * 512));
+          }
+          umma_commit(&sfr[s]);
+          if (++s == F4_STAGES) {
+            s = 0;
+            ph ^= 1;
+          }
+        }
+      }
+      // every copy issued has completed before TMEM is released
+      umma_commit(sfdrain);
+      volatile int never = 0;
+      wait_bounded(sfdrain, 0, &never, p.status, ST_TIMEOUT_DRAIN, limit);
     }
   } else if (warp >= 2 && warp <= 5) {
     // ------------------------------------------------------------ epilogue

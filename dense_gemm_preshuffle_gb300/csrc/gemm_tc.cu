@@ -10,13 +10,17 @@
 // This kernel is the Blackwell form of those steps.
 //   - One persistent CTA per SM walks BM x BN output tiles in a grouped
 //     order, so that concurrent CTAs share A rows and B columns in L2.
-//   - Warp 0 is the producer.  Each K step its lane 1 issues one 2-D TMA
-//     load for the BM x 128-byte A tile (128-byte swizzle, rows >= M
-//     zero-filled) and its lane 0 issues BN/128 plain bulk copies of 16 KiB
-//     packed-B tiles, which already hold the swizzled image.  One thread's
-//     copies complete one after another, so two issuers let A and B travel
-//     in parallel.  Data lands in an S-stage shared-memory ring with
-//     full/empty mbarriers.
+//   - Warp 0 is the producer.  Each ring stage holds KSTEP K steps.  Its
+//     lane 1 issues one TMA load for the BM x 128-byte A tile of each (a 2-D
+//     box, or one 3-D box of KSTEP K tiles; 128-byte swizzle, rows >= M and
+//     K tiles past the end zero-filled).  Its lane 0 issues one plain bulk
+//     copy per 128-row band of packed B, covering the stage's KSTEP
+//     consecutive 16 KiB tiles, which already hold the swizzled image.  One
+//     thread's copies complete one after another, so two issuers let A and
+//     B travel in parallel; and each copy costs a fixed time whatever its
+//     size, so 128 x 128 tiles take two K steps a stage (32 KiB copies,
+//     7% faster at FP8 8192^3 than 16 KiB ones).  Data lands in an S-stage
+//     shared-memory ring with full/empty mbarriers.
 //   - Warp 1, one lane, issues tcgen05.mma.  Each 128-row half of the tile
 //     has its own fp32 accumulator in tensor memory, and both halves
 //     multiply the same B tile.
@@ -56,11 +60,12 @@ namespace gp {
 constexpr int TC_EPI_WARPS = 8;  // warps 2..9: two per TMEM lane quarter, alternate 64-column chunks
 constexpr int TC_THREADS = 32 * (2 + TC_EPI_WARPS);
 
-template <int BM, int BN, int STAGES>
+template <int BM, int BN, int STAGES, int KSTEP>
 struct TcCfg {
   static constexpr int MH = BM / 128;  // 128-row halves (one MMA each)
-  static constexpr int A_BYTES = BM * 128;
-  static constexpr int B_BYTES = BN * 128;
+  static constexpr int BANDS = BN / 128;  // 128-row bands of packed B
+  static constexpr int A_BYTES = KSTEP * BM * 128;  // [K tile][BM rows][128 B]
+  static constexpr int B_BYTES = KSTEP * BN * 128;  // [band][K tile][128 rows][128 B]
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int EPI_BYTES = TC_EPI_WARPS * 32 * 128;  // one 32 x 64 bf16 staging tile per warp
   static constexpr int ACC_COLS = MH * BN;  // one accumulator buffer
@@ -84,10 +89,10 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int
   nb = r / gm;
 }
 
-template <int KIND, int BM, int BN, int STAGES>
+template <int KIND, int BM, int BN, int STAGES, int KSTEP>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmC, TcParams p) {
-  using Cfg = TcCfg<BM, BN, STAGES>;
+  using Cfg = TcCfg<BM, BN, STAGES, KSTEP>;
   constexpr int NBUF = Cfg::NBUF;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -105,6 +110,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint64_t limit = p.wait_limit_ns;
+  const int kstages = (p.ktiles + KSTEP - 1) / KSTEP;  // ring stages per tile (KSTEP K tiles each)
+  // K tiles in stage ks (the last stage of a tile may hold fewer)
+  auto stage_ktiles = [&](int ks) { return min(KSTEP, p.ktiles - ks * KSTEP); };
+  // A of stage ks: one 2-D box (one K tile) or one 3-D box of KSTEP K tiles
+  // (K tiles past the end read as zeros; the box is always complete)
+  auto load_a = [&](int st, int mb, int ks) {
+    if constexpr (KSTEP == 1)
+      tma_load_2d(s_a + st * Cfg::A_BYTES, &tmA, ks * 128, mb * BM, &full[st]);
+    else
+      tma_load_3d(s_a + st * Cfg::A_BYTES, &tmA, 0, mb * BM, ks * KSTEP, &full[st]);
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -127,27 +143,32 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     // previous kernel may still run (a prefetch never changes later loads).
     int mb, nb;
     tile_coords(blockIdx.x, p.tiles_m, p.tiles_n, mb, nb);
-    const int kpre = p.ktiles < STAGES ? p.ktiles : STAGES;
-    for (int kt = 0; kt < kpre; ++kt) {
-      prefetch_l2_tile_2d(&tmA, kt * 128, mb * BM);
-      for (int j = 0; j < BN / 128; ++j)
-        prefetch_l2_bulk(p.Bp + ((size_t)(nb * (BN / 128) + j) * p.ktiles + kt) * 16384, 16384);
+    const int kpre = kstages < STAGES ? kstages : STAGES;
+    for (int ks = 0; ks < kpre; ++ks) {
+      if constexpr (KSTEP == 1)
+        prefetch_l2_tile_2d(&tmA, ks * 128, mb * BM);
+      else
+        prefetch_l2_tile_3d(&tmA, 0, mb * BM, ks * KSTEP);
+      for (int j = 0; j < Cfg::BANDS; ++j)
+        prefetch_l2_bulk(p.Bp + ((size_t)(nb * Cfg::BANDS + j) * p.ktiles + ks * KSTEP) * 16384,
+                         (uint32_t)stage_ktiles(ks) * 16384);
     }
   }
   // With constant weights the producer requests B for the first stages of
   // its first tile before the wait on the previous kernel; A follows after.
-  const int early = (p.b_constant && (int)blockIdx.x < p.num_tiles) ? min(p.ktiles, STAGES) : 0;
+  const int early = (p.b_constant && (int)blockIdx.x < p.num_tiles) ? min(kstages, STAGES) : 0;
   if (threadIdx.x == 0 && early > 0) {  // the producer thread, which initialised the barriers
     int mb, nb;
     tile_coords(blockIdx.x, p.tiles_m, p.tiles_n, mb, nb);
     const uint8_t* bsrc = p.Bp + (size_t)nb * (BN / 128) * p.ktiles * 16384;
     const uint64_t pol_b = policy_evict_first();
-    for (int kt = 0; kt < early; ++kt) {
-      if (p.debug_skip_load == 1 + kt) continue;
-      mbar_arrive_expect_tx(&full[kt], Cfg::B_BYTES);
-      for (int j = 0; j < BN / 128; ++j)
-        bulk_load_hint(s_b + kt * Cfg::B_BYTES + j * 16384, bsrc + ((size_t)j * p.ktiles + kt) * 16384, 16384,
-                       &full[kt], pol_b);
+    for (int ks = 0; ks < early; ++ks) {
+      if (p.debug_skip_load == 1 + ks) continue;
+      const uint32_t nk = (uint32_t)stage_ktiles(ks);
+      mbar_arrive_expect_tx(&full[ks], Cfg::BANDS * nk * 16384);
+      for (int j = 0; j < Cfg::BANDS; ++j)
+        bulk_load_hint(s_b + ks * Cfg::B_BYTES + j * KSTEP * 16384, bsrc + ((size_t)j * p.ktiles + ks * KSTEP) * 16384,
+                       nk * 16384, &full[ks], pol_b);
     }
   }
   pdl_launch_dependents();
@@ -171,8 +192,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
         int mb, nb;
         tile_coords(t, p.tiles_m, p.tiles_n, mb, nb);
-        const uint8_t* bsrc = p.Bp + (size_t)nb * (BN / 128) * p.ktiles * 16384;
-        for (int kt = 0; kt < p.ktiles; ++kt) {
+        const uint8_t* bsrc = p.Bp + (size_t)nb * Cfg::BANDS * p.ktiles * 16384;
+        for (int ks = 0; ks < kstages; ++ks) {
           // B's first `early` stages are free and already requested
           const bool b_done = is_b && (int)issued < early;
           if (!b_done && !wait_bounded(&empty[s], ph ^ 1, abort_flag, p.status, ST_TIMEOUT_PRODUCER, limit)) {
@@ -184,12 +205,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             // without its arrivals, so the consumer's bounded wait times out.
           } else if (!is_b) {
             mbar_arrive_expect_tx(&full[s], Cfg::A_BYTES);
-            tma_load_2d(s_a + s * Cfg::A_BYTES, &tmA, kt * 128, mb * BM, &full[s]);
+            load_a(s, mb, ks);
           } else if (!b_done) {
-            mbar_arrive_expect_tx(&full[s], Cfg::B_BYTES);
-            for (int j = 0; j < BN / 128; ++j)
-              bulk_load_hint(s_b + s * Cfg::B_BYTES + j * 16384, bsrc + ((size_t)j * p.ktiles + kt) * 16384, 16384,
-                             &full[s], pol_b);
+            const uint32_t nk = (uint32_t)stage_ktiles(ks);
+            mbar_arrive_expect_tx(&full[s], Cfg::BANDS * nk * 16384);
+            for (int j = 0; j < Cfg::BANDS; ++j)
+              bulk_load_hint(s_b + s * Cfg::B_BYTES + j * KSTEP * 16384,
+                             bsrc + ((size_t)j * p.ktiles + ks * KSTEP) * 16384, nk * 16384, &full[s], pol_b);
           }
           ++issued;
           if (++s == STAGES) {
@@ -216,7 +238,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t fmt = (KIND == 0) ? 1u /*bf16*/ : 0u /*fp16 (kind::f16) or e4m3 (kind::f8f6f4)*/;
-      constexpr uint32_t idesc = idesc_dense(fmt, fmt, 128, BN);
+      // With one K tile per stage the bands of B sit back to back and one
+      // MMA covers all BN columns; with KSTEP > 1 each band is its own
+      // 128-column MMA.
+      constexpr uint32_t idesc = idesc_dense(fmt, fmt, 128, KSTEP == 1 ? BN : 128);
       int s = 0;
       uint32_t ph = 0;
       int local = 0;
@@ -230,7 +255,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
         tc_fence_after();
         const uint32_t d = tmem_base + (uint32_t)(buf * Cfg::ACC_COLS);
-        for (int kt = 0; kt < p.ktiles; ++kt) {
+        for (int ks = 0; ks < kstages; ++ks) {
           if (!wait_bounded(&full[s], ph, abort_flag, p.status, ST_TIMEOUT_MMA, limit)) {
             ok = false;
             break;
@@ -238,13 +263,27 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           tc_fence_after();
           const uint32_t a0 = smem_u32(s_a + s * Cfg::A_BYTES);
           const uint32_t b0 = smem_u32(s_b + s * Cfg::B_BYTES);
+          const int nk = stage_ktiles(ks);
+          for (int kk = 0; kk < nk; ++kk) {
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint64_t bdesc = smem_desc_sw128(b0 + 32 * k);
+            for (int k = 0; k < 4; ++k) {
+              const uint32_t acc = (ks | kk | k) != 0 ? 1u : 0u;
+              if constexpr (KSTEP == 1) {
+                const uint64_t bdesc = smem_desc_sw128(b0 + 32 * k);
 #pragma unroll
-            for (int mh = 0; mh < Cfg::MH; ++mh)
-              umma<KIND>(d + (uint32_t)(mh * BN), smem_desc_sw128(a0 + mh * 16384 + 32 * k), bdesc, idesc,
-                         (kt | k) != 0 ? 1u : 0u);
+                for (int mh = 0; mh < Cfg::MH; ++mh)
+                  umma<KIND>(d + (uint32_t)(mh * BN), smem_desc_sw128(a0 + mh * 16384 + 32 * k), bdesc, idesc, acc);
+              } else {
+#pragma unroll
+                for (int j = 0; j < Cfg::BANDS; ++j) {
+                  const uint64_t bdesc = smem_desc_sw128(b0 + (j * KSTEP + kk) * 16384 + 32 * k);
+#pragma unroll
+                  for (int mh = 0; mh < Cfg::MH; ++mh)
+                    umma<KIND>(d + (uint32_t)(mh * BN + j * 128),
+                               smem_desc_sw128(a0 + kk * (BM * 128) + mh * 16384 + 32 * k), bdesc, idesc, acc);
+                }
+              }
+            }
           }
           umma_commit(&empty[s]);
           if (++s == STAGES) {
@@ -331,11 +370,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
 // ---------------------------------------------------------------- host side
 
-template <int KIND, int BM, int BN, int STAGES>
+template <int KIND, int BM, int BN, int STAGES, int KSTEP>
 static int launch_tc(const CUtensorMap& tmA, const CUtensorMap& tmC, const TcParams& p, int grid,
                      cudaStream_t stream) {
-  using Cfg = TcCfg<BM, BN, STAGES>;
-  auto kern = tc_gemm_kernel<KIND, BM, BN, STAGES>;
+  using Cfg = TcCfg<BM, BN, STAGES, KSTEP>;
+  auto kern = tc_gemm_kernel<KIND, BM, BN, STAGES, KSTEP>;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -361,7 +400,7 @@ static int launch_tc(const CUtensorMap& tmA, const CUtensorMap& tmC, const TcPar
 void tc_tile_choice(int64_t M, int64_t N, int num_sms, int* bm, int* bn) {
   // The tile shape with the least estimated time: waves (ceil(tiles / SMs))
   // x tile area / the shape's relative throughput, measured on GB300 with
-  // full waves (FP8 8192^3): 256 x 256 1.0, 128 x 256 0.90, 128 x 128 0.645
+  // full waves (FP8 8192^3): 256 x 256 1.0, 128 x 256 0.90, 128 x 128 0.66
   // (smaller tiles bring fewer flops per operand byte, and each SM takes in
   // operands at ~110 GB/s).  Ties go to the larger tile.  GP_TC_TILE
   // (256x256, 128x256 or 128x128) overrides, for sweeps, where N allows.
@@ -389,7 +428,7 @@ void tc_tile_choice(int64_t M, int64_t N, int num_sms, int* bm, int* bn) {
     int bm, bn;
     double rate;
   };
-  const Shape shapes[3] = {{256, 256, 1.0}, {128, 256, 0.90}, {128, 128, 0.645}};
+  const Shape shapes[3] = {{256, 256, 1.0}, {128, 256, 0.90}, {128, 128, 0.66}};
   double best = 0.0;
   for (const Shape& t : shapes) {
     if (N % t.bn != 0) continue;
@@ -403,6 +442,8 @@ void tc_tile_choice(int64_t M, int64_t N, int num_sms, int* bm, int* bn) {
   }
 }
 
+int tc_kstep(int bm, int bn) { return (bm == 128 && bn == 128) ? 2 : 1; }
+
 int tc_gemm_launch(int kind, int bm, int bn, const CUtensorMap& tmA, const CUtensorMap& tmC, TcParams p, int num_sms,
                    cudaStream_t stream) {
   p.tiles_m = (p.M + bm - 1) / bm;
@@ -412,21 +453,21 @@ int tc_gemm_launch(int kind, int bm, int bn, const CUtensorMap& tmA, const CUten
   if (bm == 256) {
     if (bn != 256) return GP_ERR_UNSUPPORTED;
     switch (kind) {
-      case 0: return launch_tc<0, 256, 256, 3>(tmA, tmC, p, grid, stream);
-      case 1: return launch_tc<1, 256, 256, 3>(tmA, tmC, p, grid, stream);
-      default: return launch_tc<2, 256, 256, 3>(tmA, tmC, p, grid, stream);
+      case 0: return launch_tc<0, 256, 256, 3, 1>(tmA, tmC, p, grid, stream);
+      case 1: return launch_tc<1, 256, 256, 3, 1>(tmA, tmC, p, grid, stream);
+      default: return launch_tc<2, 256, 256, 3, 1>(tmA, tmC, p, grid, stream);
     }
   }
   switch (kind) {
     case 0:
-      return bn == 256 ? launch_tc<0, 128, 256, 4>(tmA, tmC, p, grid, stream)
-                       : launch_tc<0, 128, 128, 6>(tmA, tmC, p, grid, stream);
+      return bn == 256 ? launch_tc<0, 128, 256, 4, 1>(tmA, tmC, p, grid, stream)
+                       : launch_tc<0, 128, 128, 3, 2>(tmA, tmC, p, grid, stream);
     case 1:
-      return bn == 256 ? launch_tc<1, 128, 256, 4>(tmA, tmC, p, grid, stream)
-                       : launch_tc<1, 128, 128, 6>(tmA, tmC, p, grid, stream);
+      return bn == 256 ? launch_tc<1, 128, 256, 4, 1>(tmA, tmC, p, grid, stream)
+                       : launch_tc<1, 128, 128, 3, 2>(tmA, tmC, p, grid, stream);
     default:
-      return bn == 256 ? launch_tc<2, 128, 256, 4>(tmA, tmC, p, grid, stream)
-                       : launch_tc<2, 128, 128, 6>(tmA, tmC, p, grid, stream);
+      return bn == 256 ? launch_tc<2, 128, 256, 4, 1>(tmA, tmC, p, grid, stream)
+                       : launch_tc<2, 128, 128, 3, 2>(tmA, tmC, p, grid, stream);
   }
 }
 

@@ -41,6 +41,10 @@ struct I8Params {
 };
 
 void tc_tile_choice(int64_t M, int64_t N, int num_sms, int* bm, int* bn);
+// K tiles per ring stage of the tile kernel: 2 for 128 x 128 tiles (A then
+// travels as one 3-D TMA box [2][128 rows][128 B] and B as one 32 KiB
+// copy), 1 for the others (a 2-D A box).
+int tc_kstep(int bm, int bn);
 int tc_gemm_launch(int kind, int bm, int bn, const CUtensorMap& tmA, const CUtensorMap& tmC, TcParams p, int num_sms,
                    cudaStream_t stream);
 int splitk_choice(int64_t M, int64_t N, int64_t ktiles, int num_sms);
