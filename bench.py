@@ -20,7 +20,9 @@ it once per weight, not per product.
 - JSON line keys:
   - "e2e": the same metric through the public call, with pinned host
     buffers.  A and its scales are copied host->device and C device->host
-    every step.
+    every step; successive steps alternate over four streams, so the copies
+    of one step overlap the GEMM of another, and the steps are replayed
+    from a CUDA graph (copies included), as a serving loop would.
   - "roofline": the GEMM kernel against the measured HBM or tensor peak.
   - "cpu_baseline": the oracle, timed on this host's cores on a bounded
     sample.
@@ -373,34 +375,80 @@ def time_quantizers(args, pg, device, peaks, peak_kind):
     return res
 
 
+# streams the end-to-end steps alternate over (BENCH_E2E_STREAMS overrides)
+E2E_STREAMS = int(os.environ.get("BENCH_E2E_STREAMS", "4"))
+
+
 def time_e2e(prob: Problem, steps: int, warmup: int, device):
     """Through the public call with pinned host buffers: H2D of A (+ its
-    scales), gemm_run, D2H of C, every step.  Returns (seconds, h2d, d2h)."""
+    scales), gemm_run_ex, D2H of C, every step.  Successive steps alternate
+    over E2E_STREAMS streams, so one step's copies overlap another's GEMM
+    (each device and host buffer is only ever used by steps of one stream,
+    so stream order alone keeps the buffers consistent).  Returns (seconds,
+    h2d bytes, d2h bytes) per step."""
     import torch
+    S = E2E_STREAMS
     ha = prob.host_a.pin_memory()
     hsa = prob.host_sa.pin_memory() if prob.host_sa is not None else None
-    hc = torch.empty(prob.C[0].shape, dtype=prob.C[0].dtype).pin_memory()
-    stream = torch.cuda.current_stream(device)
+    hc = [torch.empty(prob.C[0].shape, dtype=prob.C[0].dtype).pin_memory() for _ in range(S)]
+    # per-stream device scales (the row scales are an input of every step)
+    sa = [prob.sa.clone() if prob.sa is not None else None for _ in range(S)]
+    nA = max(S, (prob.copies // S) * S)
+    nC = max(S, (len(prob.C) // S) * S)
+    A = [prob.A[k % len(prob.A)] if k < len(prob.A) else prob.A[0].clone() for k in range(nA)]
+    C = [prob.C[k] if k < len(prob.C) else torch.empty_like(prob.C[0]) for k in range(nC)]
+    main = torch.cuda.current_stream(device)
+    streams = [torch.cuda.Stream(device) for _ in range(S)]
 
     def one(i):
-        j = i % prob.copies
-        prob.A[j].copy_(ha, non_blocking=True)
-        if hsa is not None:
-            prob.sa.copy_(hsa, non_blocking=True)
-        prob.gp.gemm_run_ex(prob.A[j], prob.Bp[j], prob.dtype, prob.M, prob.N, prob.K, prob.mode, prob.sa,
-                            prob.sb, prob.epilogue, prob.bias, prob.C[0], prob.c_dtype, prob.flags)
-        hc.copy_(prob.C[0], non_blocking=True)
+        s = i % S
+        st = streams[s]
+        with torch.cuda.stream(st):
+            a = A[i % nA]            # i % nA has the parity of i: only stream s uses it
+            c = C[i % nC]
+            a.copy_(ha, non_blocking=True)
+            if hsa is not None:
+                sa[s].copy_(hsa, non_blocking=True)
+            prob.gp.gemm_run_ex(a, prob.Bp[i % prob.copies], prob.dtype, prob.M, prob.N, prob.K, prob.mode, sa[s],
+                                prob.sb, prob.epilogue, prob.bias, c, prob.c_dtype, prob.flags, st)
+            hc[s].copy_(c, non_blocking=True)
+
+    for st in streams:
+        st.wait_stream(main)
     for i in range(max(3, warmup)):
         one(i)
     torch.cuda.synchronize(device)
+    # Serving replays captured steps (the copies are graph memcpy nodes):
+    # a graph of G steps forks onto the streams and joins back.
+    G = max(S, min(100, steps) // S * S)
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(device)
+    cap.wait_stream(main)
+    with torch.cuda.graph(graph, stream=cap):
+        for st in streams:
+            st.wait_stream(cap)
+        for i in range(G):
+            one(i)
+        for st in streams:
+            cap.wait_stream(st)
+    main.wait_stream(cap)
+    graph.replay()  # untimed warm replay
+    torch.cuda.synchronize(device)
+    full, rest = divmod(steps, G)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for i in range(steps):
+    e0.record(main)
+    for _ in range(full):
+        graph.replay()
+    for st in streams:
+        st.wait_stream(main)
+    for i in range(rest):
         one(i)
-    e1.record(stream)
+    for st in streams:
+        main.wait_stream(st)
+    e1.record(main)
     torch.cuda.synchronize(device)
     h2d = ha.numel() * ha.element_size() + (hsa.numel() * hsa.element_size() if hsa is not None else 0)
-    d2h = hc.numel() * hc.element_size()
+    d2h = hc[0].numel() * hc[0].element_size()
     return e0.elapsed_time(e1) / 1e3, h2d, d2h
 
 
@@ -507,7 +555,8 @@ def run_ours(args):
         "e2e": {"value": None if args.no_e2e else round(world * prob.flops * e2e_steps / e2e_sec / 1e12, 3),
                 "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": round(e2e_sec / e2e_steps * 1e3, 5), "steps": e2e_steps},
+                "ms_per_step": round(e2e_sec / e2e_steps * 1e3, 5), "steps": e2e_steps,
+                "streams": E2E_STREAMS, "timing": "CUDA-graph replay of H2D copy + gemm_run_ex + D2H copy per step"},
         "roofline": roofline(prob, per, peaks, peak_kind, traffic_from_profiles(prob.name)),
         "trials": trials,
         "clocks": clock_summary,
