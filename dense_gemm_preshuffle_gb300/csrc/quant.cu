@@ -6,9 +6,9 @@
 //     q = E4M3FN(x / s), round to nearest even, saturating at +-448.  Both
 //     divisions are IEEE fp32 (this file is built without fast math, so
 //     neither division nor denormal flushing can move a code).  One CTA per
-//     row: a first pass reduces amax, a second pass writes the codes.  Rows
-//     of up to 8192 elements stay in registers between the passes (32
-//     values a thread); longer rows are read again, from L2.
+//     fp32 row, or per two bf16 rows: a first pass reduces amax, a second
+//     pass writes the codes.  Rows of up to 8192 elements stay in registers
+//     between the passes; longer rows are read again, from L2.
 //   - MXFP4, per 32-element block along K: e = the smallest integer with
 //     amax <= 6 * 2^e.  With amax = f * 2^x (f in [0.5, 1)) that is x - 3
 //     when f <= 0.75, else x - 2.  Then q = E2M1(x * 2^-e), round to
@@ -44,26 +44,30 @@ __device__ __forceinline__ void load4<__nv_bfloat16>(const __nv_bfloat16* p, flo
   v[2] = __uint_as_float(u.y << 16), v[3] = __uint_as_float(u.y & 0xFFFF0000u);
 }
 
-// One 16-byte load: 4 fp32 or 8 bf16 values (EV of them).
+// One 16-byte vector: 4 fp32 or 8 bf16 values (EV of them), kept raw in
+// registers and widened to fp32 (exactly) where used.
 template <typename XT>
 struct Vec16;
 
 template <>
 struct Vec16<float> {
   static constexpr int EV = 4;
-  __device__ __forceinline__ static void load(const float* p, float (&v)[4]) { load4<float>(p, v); }
+  __device__ __forceinline__ static void decode(const uint4& u, float (&v)[4]) {
+    v[0] = __uint_as_float(u.x), v[1] = __uint_as_float(u.y), v[2] = __uint_as_float(u.z), v[3] = __uint_as_float(u.w);
+  }
 };
 
 template <>
 struct Vec16<__nv_bfloat16> {
   static constexpr int EV = 8;
-  __device__ __forceinline__ static void load(const __nv_bfloat16* p, float (&v)[8]) {
-    const uint4 u = *reinterpret_cast<const uint4*>(p);
+  __device__ __forceinline__ static void decode(const uint4& u, float (&v)[8]) {
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) v[2 * j] = __uint_as_float(w[j] << 16), v[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
   }
 };
+
+__device__ __forceinline__ uint4 ld_vec16(const void* p) { return *reinterpret_cast<const uint4*>(p); }
 
 // Two fp32 values -> two E4M3 codes: lo in bits 0-7, hi in bits 8-15.
 __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
@@ -100,57 +104,112 @@ __device__ __forceinline__ float quotient_for_e4m3(float x, float s, float inv) 
   return __fdiv_rn(x, s);
 }
 
-__device__ __forceinline__ float block_amax(float amax, float* red) {
+// Max over the NW warps of a CTA of each of R values (red: R x NW floats).
+template <int R, int NW>
+__device__ __forceinline__ void block_amax(float (&amax)[R], float* red) {
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  for (int r = 0; r < R; ++r) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax[r] = fmaxf(amax[r], __shfl_xor_sync(0xffffffffu, amax[r], o));
+    if ((threadIdx.x & 31) == 0) red[r * NW + (threadIdx.x >> 5)] = amax[r];
+  }
   __syncthreads();
-  amax = red[0];
 #pragma unroll
-  for (int w = 1; w < 8; ++w) amax = fmaxf(amax, red[w]);
-  __syncthreads();  // red is reused by the next row
-  return amax;
+  for (int r = 0; r < R; ++r) {
+    float m = red[r * NW];
+#pragma unroll
+    for (int w = 1; w < NW; ++w) m = fmaxf(m, red[r * NW + w]);
+    amax[r] = m;
+  }
+  __syncthreads();  // red is reused by the next rows
 }
 
-// Rows of up to 256 * VPT * EV elements: each thread keeps its VPT 16-byte
+// fp32 rows of up to 256 * 8 * 4 elements: each thread keeps its 8 float4
 // vectors in registers between the amax pass and the quantising pass, so
-// the row is read from memory once.
-template <typename XT, int VPT>
-__global__ void __launch_bounds__(256, 4) quant_e4m3_rows_reg_kernel(const XT* __restrict__ X, int64_t M, int64_t K,
-                                                                  uint8_t* __restrict__ Q, float* __restrict__ S) {
-  constexpr int EV = Vec16<XT>::EV;
+// the row is read from memory once.  One CTA per row, four per SM.
+__global__ void __launch_bounds__(256, 4) quant_e4m3_rows_f32_kernel(const float* __restrict__ X, int64_t M,
+                                                                  int64_t K, uint8_t* __restrict__ Q,
+                                                                  float* __restrict__ S) {
+  constexpr int VPT = 8;
   __shared__ float red[8];
   for (int64_t row = blockIdx.x; row < M; row += gridDim.x) {
-    const XT* x = X + row * K;
-    float v[VPT][EV];
-    float amax = 0.0f;
+    const float* x = X + row * K;
+    float v[VPT][4];
+    float amax[1] = {0.0f};
 #pragma unroll
     for (int j = 0; j < VPT; ++j) {
-      const int64_t i = ((int64_t)j * blockDim.x + threadIdx.x) * EV;
+      const int64_t i = ((int64_t)j * blockDim.x + threadIdx.x) * 4;
       if (i < K) {
-        Vec16<XT>::load(x + i, v[j]);
+        load4<float>(x + i, v[j]);
 #pragma unroll
-        for (int e = 0; e < EV; ++e) amax = fmaxf(amax, fabsf(v[j][e]));
+        for (int e = 0; e < 4; ++e) amax[0] = fmaxf(amax[0], fabsf(v[j][e]));
       }
     }
-    amax = block_amax(amax, red);
-    const float s = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+    block_amax<1, 8>(amax, red);
+    const float s = amax[0] > 0.0f ? __fdiv_rn(amax[0], 448.0f) : 1.0f;
     const float inv = __frcp_rn(s);
     if (threadIdx.x == 0) S[row] = s;
 #pragma unroll
     for (int j = 0; j < VPT; ++j) {
-      const int64_t i = ((int64_t)j * blockDim.x + threadIdx.x) * EV;
-      if (i < K) {
-        uint32_t w[EV / 4];
+      const int64_t i = ((int64_t)j * blockDim.x + threadIdx.x) * 4;
+      if (i < K)
+        *reinterpret_cast<uint32_t*>(Q + row * K + i) =
+            e4m3x2(quotient_for_e4m3(v[j][0], s, inv), quotient_for_e4m3(v[j][1], s, inv)) |
+            (e4m3x2(quotient_for_e4m3(v[j][2], s, inv), quotient_for_e4m3(v[j][3], s, inv)) << 16);
+    }
+  }
+}
+
+// bf16 rows of up to THREADS * VPT * 8 elements, kept as raw 16-byte
+// vectors (half the registers of fp32 values) and widened where used.  The
+// bytes in flight per SM are the resident CTAs' rows, so the fewer
+// registers buy more CTAs per SM (MINB).  Two rows a CTA at four CTAs per
+// SM were slower than one row at six (bf16 8192 x 8192: 55 vs 46 us).
+template <int THREADS, int VPT, int MINB>
+__global__ void __launch_bounds__(THREADS, MINB) quant_e4m3_rows_bf16_kernel(const __nv_bfloat16* __restrict__ X,
+                                                                          int64_t M, int64_t K,
+                                                                          uint8_t* __restrict__ Q,
+                                                                          float* __restrict__ S) {
+  using V = Vec16<__nv_bfloat16>;
+  constexpr int EV = V::EV;
+  constexpr int NW = THREADS / 32;
+  __shared__ float red[NW];
+  for (int64_t row = blockIdx.x; row < M; row += gridDim.x) {
+    const __nv_bfloat16* x = X + row * K;
+    uint4 raw[VPT];
+    float amax[1] = {0.0f};
 #pragma unroll
-        for (int k = 0; k < EV / 4; ++k)
-          w[k] = e4m3x2(quotient_for_e4m3(v[j][4 * k], s, inv), quotient_for_e4m3(v[j][4 * k + 1], s, inv)) |
-                 (e4m3x2(quotient_for_e4m3(v[j][4 * k + 2], s, inv), quotient_for_e4m3(v[j][4 * k + 3], s, inv))
-                  << 16);
-        if constexpr (EV == 4)
-          *reinterpret_cast<uint32_t*>(Q + row * K + i) = w[0];
-        else
-          *reinterpret_cast<uint2*>(Q + row * K + i) = make_uint2(w[0], w[1]);
+    for (int j = 0; j < VPT; ++j) {
+      const int i = (j * THREADS + (int)threadIdx.x) * EV;  // K <= THREADS * VPT * EV here
+      if (i < K) raw[j] = ld_vec16(x + i);
+    }
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+      const int i = (j * THREADS + (int)threadIdx.x) * EV;
+      if (i < K) {
+        float v[EV];
+        V::decode(raw[j], v);
+#pragma unroll
+        for (int e = 0; e < EV; ++e) amax[0] = fmaxf(amax[0], fabsf(v[e]));
+      }
+    }
+    block_amax<1, NW>(amax, red);
+    const float s = amax[0] > 0.0f ? __fdiv_rn(amax[0], 448.0f) : 1.0f;
+    const float inv = __frcp_rn(s);
+    if (threadIdx.x == 0) S[row] = s;
+    uint8_t* q = Q + row * K;
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+      const int i = (j * THREADS + (int)threadIdx.x) * EV;
+      if (i < K) {
+        float v[EV];
+        V::decode(raw[j], v);
+        uint32_t w[2];
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+          w[k] = e4m3x2(quotient_for_e4m3(v[4 * k], s, inv), quotient_for_e4m3(v[4 * k + 1], s, inv)) |
+                 (e4m3x2(quotient_for_e4m3(v[4 * k + 2], s, inv), quotient_for_e4m3(v[4 * k + 3], s, inv)) << 16);
+        *reinterpret_cast<uint2*>(q + i) = make_uint2(w[0], w[1]);
       }
     }
   }
@@ -169,7 +228,9 @@ __global__ void __launch_bounds__(256) quant_e4m3_rows_kernel(const XT* __restri
       load4<XT>(x + i, v);
       amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3]))));
     }
-    amax = block_amax(amax, red);
+    float am[1] = {amax};
+    block_amax<1, 8>(am, red);
+    amax = am[0];
     const float s = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
     if (threadIdx.x == 0) S[row] = s;
     for (int64_t i = threadIdx.x * 4; i < K; i += 4 * blockDim.x) {
@@ -183,44 +244,50 @@ __global__ void __launch_bounds__(256) quant_e4m3_rows_kernel(const XT* __restri
 }
 
 // grid.x covers the 8-element groups of a row (256 per CTA); grid.y strides
-// over groups of MX_ROWS rows, whose loads a thread issues together (more
+// over groups of ROWS rows, whose loads a thread issues together (more
 // bytes in flight).  All index arithmetic is division-free.
-constexpr int MX_ROWS = 4;
+template <typename XT>
+struct MxRows {
+  static constexpr int value = 4;  // 8 rows of bf16 halve the grid and were slower (measured)
+};
 
 template <typename XT>
 __global__ void __launch_bounds__(256) quant_mxfp4_kernel(const XT* __restrict__ X, int64_t M, int K,
                                                           uint8_t* __restrict__ Q, uint8_t* __restrict__ E) {
+  constexpr int MX_ROWS = MxRows<XT>::value;
+  constexpr int NV = 8 / Vec16<XT>::EV;  // 16-byte vectors per 8-element group
   const int per_row = K / 8;  // 8-element groups per row; 4 groups per 32-element block
   const int c8 = blockIdx.x * blockDim.x + threadIdx.x;
   // A 4-lane group is entirely inside or outside the row (per_row % 4 == 0),
   // and every lane takes part in the shuffles.
   const bool active = c8 < per_row;
   for (int64_t row0 = (int64_t)blockIdx.y * MX_ROWS; row0 < M; row0 += (int64_t)gridDim.y * MX_ROWS) {
-    float v[MX_ROWS][8];
+    uint4 raw[MX_ROWS][NV];
 #pragma unroll
     for (int r = 0; r < MX_ROWS; ++r) {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) v[r][j] = 0.0f;
       const int64_t row = row0 + r;
+#pragma unroll
+      for (int q = 0; q < NV; ++q) raw[r][q] = make_uint4(0u, 0u, 0u, 0u);
       if (active && row < M) {
         const XT* x = X + row * (int64_t)K + (int64_t)c8 * 8;
-        if constexpr (Vec16<XT>::EV == 8) {
-          Vec16<XT>::load(x, v[r]);
-        } else {
-          float a[4], b[4];
-          load4<XT>(x, a);
-          load4<XT>(x + 4, b);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) v[r][j] = a[j], v[r][4 + j] = b[j];
-        }
+        for (int q = 0; q < NV; ++q) raw[r][q] = ld_vec16(x + q * Vec16<XT>::EV);
       }
     }
 #pragma unroll
     for (int r = 0; r < MX_ROWS; ++r) {
       const int64_t row = row0 + r;
+      float v[8];
+#pragma unroll
+      for (int q = 0; q < NV; ++q) {
+        float t[Vec16<XT>::EV];
+        Vec16<XT>::decode(raw[r][q], t);
+#pragma unroll
+        for (int e = 0; e < Vec16<XT>::EV; ++e) v[q * Vec16<XT>::EV + e] = t[e];
+      }
       float amax = 0.0f;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[r][j]));
+      for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[j]));
       amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
       amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
       int e = 0;
@@ -234,7 +301,7 @@ __global__ void __launch_bounds__(256) quant_mxfp4_kernel(const XT* __restrict__
       const float scale = __int_as_float((uint32_t)(127 - e) << 23);
       uint32_t packed = 0;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) packed |= e2m1x2(v[r][2 * j] * scale, v[r][2 * j + 1] * scale) << (8 * j);
+      for (int j = 0; j < 4; ++j) packed |= e2m1x2(v[2 * j] * scale, v[2 * j + 1] * scale) << (8 * j);
       if (active && row < M) {
         *reinterpret_cast<uint32_t*>(Q + row * (int64_t)(K / 2) + (int64_t)c8 * 4) = packed;
         if ((c8 & 3) == 0) E[row * (int64_t)(K / 32) + c8 / 4] = (uint8_t)(e + 127);
@@ -242,6 +309,10 @@ __global__ void __launch_bounds__(256) quant_mxfp4_kernel(const XT* __restrict__
     }
   }
 }
+
+// bf16 rows of up to 8192: 256 threads x 4 vectors, six CTAs per SM (the
+// best of 256 x 4 at 5-7 CTAs and 128 x 8 at 8-12, measured at 8192 x 8192)
+constexpr int QB_THREADS = 256, QB_VPT = 4, QB_MINB = 6;
 
 int grid_rows(int64_t M) { return (int)(M < 65535 * 4 ? M : 65535 * 4); }
 
@@ -251,13 +322,12 @@ int quant_launch(const void* X, bool x_bf16, int64_t M, int64_t K, bool to_e2m1,
                  cudaStream_t stream) {
   if (!to_e2m1) {
     const int grid = grid_rows(M);
-    if (x_bf16 && K <= 256 * 4 * 8) {
-      quant_e4m3_rows_reg_kernel<__nv_bfloat16, 4><<<grid, 256, 0, stream>>>(
+    if (x_bf16 && K <= QB_THREADS * QB_VPT * 8) {
+      quant_e4m3_rows_bf16_kernel<QB_THREADS, QB_VPT, QB_MINB><<<grid, QB_THREADS, 0, stream>>>(
           static_cast<const __nv_bfloat16*>(X), M, K, static_cast<uint8_t*>(Q), static_cast<float*>(S));
     } else if (!x_bf16 && K <= 256 * 8 * 4) {
-      quant_e4m3_rows_reg_kernel<float, 8><<<grid, 256, 0, stream>>>(static_cast<const float*>(X), M, K,
-                                                                      static_cast<uint8_t*>(Q),
-                                                                      static_cast<float*>(S));
+      quant_e4m3_rows_f32_kernel<<<grid, 256, 0, stream>>>(static_cast<const float*>(X), M, K,
+                                                           static_cast<uint8_t*>(Q), static_cast<float*>(S));
     } else if (x_bf16)
       quant_e4m3_rows_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(X), M, K,
                                                                        static_cast<uint8_t*>(Q),
@@ -266,7 +336,8 @@ int quant_launch(const void* X, bool x_bf16, int64_t M, int64_t K, bool to_e2m1,
       quant_e4m3_rows_kernel<float><<<grid, 256, 0, stream>>>(static_cast<const float*>(X), M, K,
                                                                static_cast<uint8_t*>(Q), static_cast<float*>(S));
   } else {
-    const int64_t groups = (M + MX_ROWS - 1) / MX_ROWS;
+    const int rows = x_bf16 ? MxRows<__nv_bfloat16>::value : MxRows<float>::value;
+    const int64_t groups = (M + rows - 1) / rows;
     const dim3 grid((unsigned)((K / 8 + 255) / 256), (unsigned)(groups < 65535 ? groups : 65535));
     if (x_bf16)
       quant_mxfp4_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(X), M, (int)K,
