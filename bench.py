@@ -464,10 +464,16 @@ def roofline(prob: Problem, sec_per_step: float, peaks: dict, peak_kind: str, tr
     base = float(peaks["bf16_tflops"])
     peak = base * ratio
     achieved = prob.flops / sec_per_step / 1e12
-    return {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak, 1), "unit": "TFLOP/s",
-            "frac": round(achieved / peak, 4), "traffic": traffic,
-            "peak_source": f"bf16_tflops burst ({peak_kind}) x {ratio:g} nominal {prob.dtype}/bf16 ratio",
-            "algorithmic_flops_per_launch": prob.flops}
+    out = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak, 1), "unit": "TFLOP/s",
+           "frac": round(achieved / peak, 4), "traffic": traffic,
+           "peak_source": f"bf16_tflops burst ({peak_kind}) x {ratio:g} nominal {prob.dtype}/bf16 ratio",
+           "algorithmic_flops_per_launch": prob.flops}
+    if peaks.get("bf16_tflops_sustained"):
+        # beside it, the power-capped rate of a seconds-long cuBLAS loop
+        sus = float(peaks["bf16_tflops_sustained"]) * ratio
+        out["peak_sustained"] = round(sus, 1)
+        out["frac_of_sustained"] = round(achieved / sus, 4)
+    return out
 
 
 def traffic_from_profiles(name: str):
