@@ -28,7 +28,8 @@
 //     transaction bytes and one arrival from warp 6.
 //   - The epilogue reads a tile's whole accumulator into registers (rounded
 //     to packed bf16/fp16) before it stages and stores it, and frees the
-//     accumulator in between, so the next tile's MMAs overlap the stores.
+//     accumulator in between, so the next tile's MMAs overlap the stores
+//     (not with SiLU / GELU, whose cost before the release outweighs it).
 //   - TMEM: one 256-column fp32 accumulator, plus one scale slot per ring
 //     stage (A: 2 atoms x 4 columns; B: 2 atoms x 8 columns).  Warp 7
 //     copies a stage's scales into its slot (tcgen05.cp) as soon as the
@@ -342,6 +343,7 @@ __global__ void __launch_bounds__(F4_THREADS, 1)
   } else if (warp >= 2 && warp <= 5) {
     // ------------------------------------------------------------ epilogue
     const int quad = warp & 3;
+    const bool early_release = p.act == EPI_ACT_NONE || p.act == EPI_ACT_RELU;
     uint8_t* stg = s_epi + (warp - 2) * 4096;
     const uint32_t stg_row = smem_u32(stg) + lane * 128;
     int local = 0;
@@ -352,43 +354,81 @@ __global__ void __launch_bounds__(F4_THREADS, 1)
       tc_fence_after();
       const int row0 = mb * 128 + quad * 32;
       const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16);
-      // The whole row of the tile (256 outputs) is read from TMEM and
-      // rounded into 128 packed registers first, and the accumulator is
-      // released: the next tile's MMAs then run while this tile is staged
-      // and stored (the single accumulator otherwise holds them back).
-      uint32_t pk[F4_BN / 2];
+      if (early_release) {
+        // The whole row of the tile (256 outputs) is read from TMEM and
+        // rounded into 128 packed registers first, and the accumulator is
+        // released: the next tile's MMAs then run while this tile is staged
+        // and stored (the single accumulator otherwise holds them back).
+        uint32_t pk[F4_BN / 2];
 #pragma unroll
-      for (int c = 0; c < F4_BN / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(tbase + (uint32_t)(c * 32), r);
-        tmem_ld_wait();
-        float v[32];
+        for (int c = 0; c < F4_BN / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(tbase + (uint32_t)(c * 32), r);
+          tmem_ld_wait();
+          float v[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]);
-        uint32_t q16[16];
-        epi_row32(v, 1.0f, nullptr, p.bias != nullptr ? p.bias + nb * F4_BN + c * 32 : nullptr, p.act,
-                  p.out_f16 != 0, q16);
+          for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]);
+          uint32_t q16[16];
+          epi_row32(v, 1.0f, nullptr, p.bias != nullptr ? p.bias + nb * F4_BN + c * 32 : nullptr, p.act,
+                    p.out_f16 != 0, q16);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) pk[c * 16 + e] = q16[e];
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(acce);
-#pragma unroll
-      for (int c = 0; c < F4_BN / 64; ++c) {
-        const int n0 = nb * F4_BN + c * 64;
-        if (lane == 0) bulk_wait_group_read<0>();  // the previous store has read the staging tile
-        __syncwarp();
-#pragma unroll
-        for (int chunk = 0; chunk < 8; ++chunk)
-          st_shared_v4(stg_row + (uint32_t)(((chunk ^ (lane & 7)) * 16)), pk[c * 32 + 4 * chunk],
-                       pk[c * 32 + 4 * chunk + 1], pk[c * 32 + 4 * chunk + 2], pk[c * 32 + 4 * chunk + 3]);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0 && row0 < p.M) {
-          tma_store_2d(&tmC, n0, row0, stg);
-          bulk_commit_group();
+          for (int e = 0; e < 16; ++e) pk[c * 16 + e] = q16[e];
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acce);
+#pragma unroll
+        for (int c = 0; c < F4_BN / 64; ++c) {
+          const int n0 = nb * F4_BN + c * 64;
+          if (lane == 0) bulk_wait_group_read<0>();  // the previous store has read the staging tile
+          __syncwarp();
+#pragma unroll
+          for (int chunk = 0; chunk < 8; ++chunk)
+            st_shared_v4(stg_row + (uint32_t)(((chunk ^ (lane & 7)) * 16)), pk[c * 32 + 4 * chunk],
+                         pk[c * 32 + 4 * chunk + 1], pk[c * 32 + 4 * chunk + 2], pk[c * 32 + 4 * chunk + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && row0 < p.M) {
+            tma_store_2d(&tmC, n0, row0, stg);
+            bulk_commit_group();
+          }
+        }
+      } else {
+        // SiLU / GELU: computing them for the whole row before the release
+        // was slower than storing chunk by chunk and releasing at the end
+#pragma unroll 1
+        for (int c = 0; c < F4_BN / 64; ++c) {
+          const int n0 = nb * F4_BN + c * 64;
+          if (lane == 0) bulk_wait_group_read<0>();
+          __syncwarp();
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(tbase + (uint32_t)(c * 64 + h * 32), r);
+            tmem_ld_wait();
+            float v[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]);
+            uint32_t q16[16];
+            epi_row32(v, 1.0f, nullptr, p.bias != nullptr ? p.bias + n0 + h * 32 : nullptr, p.act, p.out_f16 != 0,
+                      q16);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int chunk = h * 4 + q;
+              st_shared_v4(stg_row + (uint32_t)(((chunk ^ (lane & 7)) * 16)), q16[4 * q], q16[4 * q + 1],
+                           q16[4 * q + 2], q16[4 * q + 3]);
+            }
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && row0 < p.M) {
+            tma_store_2d(&tmC, n0, row0, stg);
+            bulk_commit_group();
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acce);
       }
     }
     if (lane == 0) bulk_wait_group<0>();
