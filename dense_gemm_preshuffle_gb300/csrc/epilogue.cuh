@@ -46,7 +46,9 @@ __device__ __forceinline__ float epi_act(float x, int act) {
 
 // v: the row's 32 fp32 values; sb, bias: the same 32 columns (16-byte
 // aligned) or null; sa: the row scale (1 when absent); out_f16: round to
-// IEEE binary16 instead of bf16 (both RNE).
+// IEEE binary16 instead of bf16 (both RNE).  BIAS_SMEM: bias points into
+// shared memory (else global, read through the read-only path).
+template <bool BIAS_SMEM = false>
 __device__ __forceinline__ void epi_row32(float (&v)[32], float sa, const float* sb, const float* bias, int act,
                                           bool out_f16, uint32_t (&pk)[16]) {
   if (sb != nullptr) {
@@ -64,7 +66,7 @@ __device__ __forceinline__ void epi_row32(float (&v)[32], float sa, const float*
     const float4* b4 = reinterpret_cast<const float4*>(bias);
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
-      const float4 b = __ldg(b4 + q);
+      const float4 b = BIAS_SMEM ? b4[q] : __ldg(b4 + q);
       v[4 * q] += b.x;
       v[4 * q + 1] += b.y;
       v[4 * q + 2] += b.z;

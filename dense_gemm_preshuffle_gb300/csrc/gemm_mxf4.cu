@@ -62,8 +62,9 @@ struct F4Cfg {
   static constexpr int SF_COL0 = ACC_COLS;
   static constexpr int TMEM_COLS = 512;
   static_assert(ACC_COLS + F4_STAGES * (SFA_COLS + SFB_COLS) <= TMEM_COLS, "tensor memory budget");
+  static constexpr int BIAS_BYTES = 4 * F4_BN * 4;  // each epilogue warp's copy of a tile's bias
   static constexpr int SMEM =
-      F4_STAGES * (A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES) + EPI_BYTES + 256 + 1024;
+      F4_STAGES * (A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES) + EPI_BYTES + BIAS_BYTES + 256 + 1024;
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
@@ -105,7 +106,8 @@ __global__ void __launch_bounds__(F4_THREADS, 1)
   uint8_t* s_sfa = s_b + F4_STAGES * Cfg::B_BYTES;
   uint8_t* s_sfb = s_sfa + F4_STAGES * Cfg::SFA_BYTES;
   uint8_t* s_epi = s_sfb + F4_STAGES * Cfg::SFB_BYTES;
-  uint64_t* full = reinterpret_cast<uint64_t*>(s_epi + Cfg::EPI_BYTES);
+  float* s_bias = reinterpret_cast<float*>(s_epi + Cfg::EPI_BYTES);
+  uint64_t* full = reinterpret_cast<uint64_t*>(s_epi + Cfg::EPI_BYTES + Cfg::BIAS_BYTES);
   uint64_t* empty = full + F4_STAGES;
   uint64_t* accf = empty + F4_STAGES;
   uint64_t* acce = accf + 1;
@@ -350,6 +352,21 @@ __global__ void __launch_bounds__(F4_THREADS, 1)
     for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++local) {
       int mb, nb;
       f4_tile_coords(t, p.tiles_m, p.tiles_n, mb, nb);
+      // The tile's bias goes to this warp's shared-memory copy while the
+      // tile's main loop runs (every thread would otherwise fetch all 256
+      // values while the accumulator is held).  A copy per warp needs no
+      // barrier across warps: the warp's own reads of the previous tile are
+      // done (the __syncwarp below orders the overwrite after them).
+      const float* bias_t = nullptr;
+      if (p.bias != nullptr) {
+        float4* sbuf = reinterpret_cast<float4*>(s_bias + (warp - 2) * F4_BN);
+        const float4* src = reinterpret_cast<const float4*>(p.bias + nb * F4_BN);
+        __syncwarp();
+        sbuf[2 * lane] = __ldg(src + 2 * lane);
+        sbuf[2 * lane + 1] = __ldg(src + 2 * lane + 1);
+        __syncwarp();
+        bias_t = reinterpret_cast<const float*>(sbuf);
+      }
       if (!wait_bounded(accf, (uint32_t)(local & 1), abort_flag, p.status, ST_TIMEOUT_EPILOGUE, limit)) break;
       tc_fence_after();
       const int row0 = mb * 128 + quad * 32;
@@ -369,8 +386,8 @@ __global__ void __launch_bounds__(F4_THREADS, 1)
 #pragma unroll
           for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]);
           uint32_t q16[16];
-          epi_row32(v, 1.0f, nullptr, p.bias != nullptr ? p.bias + nb * F4_BN + c * 32 : nullptr, p.act,
-                    p.out_f16 != 0, q16);
+          epi_row32<true>(v, 1.0f, nullptr, bias_t != nullptr ? bias_t + c * 32 : nullptr, p.act, p.out_f16 != 0,
+                          q16);
 #pragma unroll
           for (int e = 0; e < 16; ++e) pk[c * 16 + e] = q16[e];
         }
@@ -410,8 +427,8 @@ __global__ void __launch_bounds__(F4_THREADS, 1)
 #pragma unroll
             for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]);
             uint32_t q16[16];
-            epi_row32(v, 1.0f, nullptr, p.bias != nullptr ? p.bias + n0 + h * 32 : nullptr, p.act, p.out_f16 != 0,
-                      q16);
+            epi_row32<true>(v, 1.0f, nullptr, bias_t != nullptr ? bias_t + c * 64 + h * 32 : nullptr, p.act,
+                            p.out_f16 != 0, q16);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               const int chunk = h * 4 + q;
