@@ -342,16 +342,22 @@ __global__ void __launch_bounds__(I8_THREADS, i8_ctas_per_sm(NB8))
 
   // ------------------------------------------------------------ reduction
   named_bar_sync(1, I8_CW * 32);  // every consumer is done with the ring (no copy in flight)
-  int32_t* red = reinterpret_cast<int32_t*>(base);  // [CW][16][SN]
+  // [CW][16][RS] partials.  A lane stores its two adjacent columns as one
+  // 8-byte word; with the row stride RS = 8 (mod 32) ints, the 16 lanes of
+  // each half-warp (rows g, 4 column pairs each) hit 16 distinct bank pairs
+  // (a stride of 32 put all 8 rows on the same banks: 8-way conflicts).
+  constexpr int RS = ((SN - 8 + 31) / 32) * 32 + 8;
+  static_assert(I8_CW * 16 * RS * 4 <= I8_STAGES * STAGE, "the reduction fits in the ring");
+  int32_t* red = reinterpret_cast<int32_t*>(base);
 #pragma unroll
   for (int nb = 0; nb < NB8; ++nb) {
     const int col = nb * 8 + 2 * t;
     // sum a*b = sum a*(b + bias) - bias * sum a (bias 128 for int8 B, 8 for int4)
     constexpr int OFF = W4 ? 8 : 128;
-    red[(warp * 16 + g) * SN + col] = acc[nb][0] - OFF * rs_lo;
-    red[(warp * 16 + g) * SN + col + 1] = acc[nb][1] - OFF * rs_lo;
-    red[(warp * 16 + g + 8) * SN + col] = acc[nb][2] - OFF * rs_hi;
-    red[(warp * 16 + g + 8) * SN + col + 1] = acc[nb][3] - OFF * rs_hi;
+    *reinterpret_cast<int2*>(red + (warp * 16 + g) * RS + col) =
+        make_int2(acc[nb][0] - OFF * rs_lo, acc[nb][1] - OFF * rs_lo);
+    *reinterpret_cast<int2*>(red + (warp * 16 + g + 8) * RS + col) =
+        make_int2(acc[nb][2] - OFF * rs_hi, acc[nb][3] - OFF * rs_hi);
   }
   named_bar_sync(1, I8_CW * 32);
   const int cols = nu * 8;
@@ -360,7 +366,7 @@ __global__ void __launch_bounds__(I8_THREADS, i8_ctas_per_sm(NB8))
     const int m = i / cols, n = i - m * cols;
     int sum = 0;
 #pragma unroll
-    for (int w = 0; w < I8_CW; ++w) sum += red[(w * 16 + m) * SN + n];
+    for (int w = 0; w < I8_CW; ++w) sum += red[(w * 16 + m) * RS + n];
     const int gm = mg * 16 + m;
     if (gm < p.M) p.C[(size_t)gm * p.N + n0 + n] = sum;
   }
