@@ -95,7 +95,7 @@ int gemm_packed_b_bytes(int dtype, int64_t N, int64_t K, size_t* bytes_out);
  *
  * Layout of the packed buffer (a bijection of B's bytes):
  *   - B's bytes are cut into tiles of R rows x 128 bytes, with R = 128 for
- *     BF16, E4M3 and E2M1 and R = 8 for INT8 and W4A8.  The tile of (row band tn,
+ *     BF16, FP16, E4M3 and E2M1 and R = 8 for INT8 and W4A8.  The tile of (row band tn,
  *     byte column tk) is the R*128-byte block with index tn*(Kb/128)+tk,
  *     where Kb = row bytes.
  *   - INT8 bytes are stored in offset binary: b XOR 0x80, i.e. b + 128 as
@@ -167,7 +167,7 @@ int gemm_run(const void* A, const void* B_packed, int dtype, int64_t M, int64_t 
  * "bias_silu" and "bias_gelu").  After the scales, v = acc * scale_a[m] *
  * scale_b[n] + bias[n] with bias fp32 [N], then the activation: ReLU
  * max(v, 0); SiLU v / (1 + e^-v); GELU 0.5 v (1 + erf(v / sqrt 2)) (the
- * exact form).  The result is rounded to bf16. */
+ * exact form).  The result is rounded to the float c_dtype (bf16 or fp16). */
 typedef enum gp_epilogue {
   GP_EPI_NONE = 0,
   GP_EPI_BIAS = 1,
