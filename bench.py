@@ -268,7 +268,9 @@ def time_device(prob: Problem, steps: int, warmup: int, pg, device, graph_len: i
     for i in range(max(3, warmup)):
         prob.step(i)
     torch.cuda.synchronize(device)
-    g_len = max(1, min(graph_len, steps))
+    # the graph covers every rotating copy (else a small workload's replays
+    # would cycle through only graph_len copies, which stay in L2)
+    g_len = max(1, min(steps, max(graph_len, prob.copies)))
     graph = torch.cuda.CUDAGraph()
     s = torch.cuda.Stream(device)
     s.wait_stream(stream)
@@ -296,8 +298,10 @@ def time_device(prob: Problem, steps: int, warmup: int, pg, device, graph_len: i
 
 def time_trials(prob, warmup: int, device, R: int = 80, n: int = 7):
     """n trials of R back-to-back steps (one CUDA-graph replay each): the
-    median, p10 and p90 of the per-step device time, in microseconds."""
+    median, p10 and p90 of the per-step device time, in microseconds.  R is
+    raised to the number of rotating copies, so a trial's inputs exceed L2."""
     import torch
+    R = max(R, prob.copies)
     stream = torch.cuda.current_stream(device)
     for i in range(max(3, warmup)):
         prob.step(i)
@@ -357,7 +361,7 @@ def time_quantizers(args, pg, device, peaks, peak_kind):
             name = f"{q}_{M}x{K}_from_{xd}"
             try:
                 p = QuantProblem(q, xd, M, K, device)
-                steps = max(20, min(args.steps, 400))
+                steps = max(20, min(args.steps, 400), p.copies)
                 sec = max_over_ranks(pg, time_device(p, steps, args.warmup, pg, device), device)
                 per = sec / steps
                 achieved = p.bytes / per / 1e9
@@ -579,7 +583,7 @@ def run_ours(args):
                 continue
             try:
                 p2 = Problem(name, device)
-                steps2 = max(20, min(args.steps, 400))
+                steps2 = max(20, min(args.steps, 400), p2.copies)  # every rotating copy at least once
                 s2 = time_device(p2, steps2, args.warmup, pg, device)
                 s2 = max_over_ranks(pg, s2, device)
                 r = roofline(p2, s2 / steps2, peaks, peak_kind, traffic_from_profiles(name))
@@ -620,7 +624,7 @@ def run_ours(args):
                 continue
             try:
                 p3 = Problem(name, device)
-                steps3 = max(20, min(args.steps, 400))
+                steps3 = max(20, min(args.steps, 400), p3.copies)
                 s_plain = time_device(p3, steps3, args.warmup, pg, device)
                 gen = torch.Generator().manual_seed(99)
                 p3.epilogue = "bias_gelu"

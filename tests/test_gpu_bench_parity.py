@@ -1,0 +1,86 @@
+"""Parity in the launch configuration the benchmark times.
+
+bench.py times back-to-back gemm_run_ex launches:
+- with GP_RUN_B_CONSTANT (and GP_RUN_INDEPENDENT for the weight-streaming
+  runs);
+- replayed from a CUDA graph;
+- over rotating copies of A and packed B.
+These tests drive that same code path (bench.Problem and bench.time_device)
+on every workload at its full size. They then check every output buffer it
+wrote against the oracle: every row of the small products, sampled rows of
+the large ones.
+"""
+import os
+import sys
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import dense_gemm_preshuffle_gb300 as gp
+from dense_gemm_preshuffle_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+import bench  # noqa: E402
+
+TOL = 8e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from dense_gemm_preshuffle_gb300 import build
+    build.build()
+    gp.load_library()
+
+
+def rows_to_check(M, seed):
+    if M <= 512:
+        return np.arange(M)
+    rng = np.random.default_rng(seed)
+    return np.unique(np.concatenate([rng.choice(M, 16, replace=False), [0, M - 1]]))
+
+
+def check_outputs(prob, ops, rows):
+    ref = oracle.gemm_operands(ops, rows=rows)
+    for C in prob.C:
+        if C.dtype == torch.int32:
+            c = C.cpu().numpy().astype(np.int64)[rows]
+            assert np.array_equal(c, ref), f"{int((c != ref).sum())} mismatching int32 outputs"
+        else:
+            c = C.float().cpu().numpy().astype(np.float64)[rows]
+            err = oracle.max_rel_err(c, ref)
+            assert err <= TOL, f"max rel err {err:.3e}"
+
+
+@pytest.mark.parametrize("name", list(inputs.ALL_WORKLOADS))
+def test_bench_launch_configuration_matches_oracle(name):
+    dev = torch.device("cuda", 0)
+    prob = bench.Problem(name, dev)
+    for C in prob.C:
+        C.zero_()
+    steps = 2 * len(prob.C) + 3  # every output buffer is written, some twice
+    bench.time_device(prob, steps, 3, None, dev)
+    torch.cuda.synchronize()
+    assert gp.gemm_last_device_status() == 0
+    ops = inputs.workload_operands(name)
+    check_outputs(prob, ops, rows_to_check(ops.M, seed=zlib.crc32(name.encode())))
+
+
+@pytest.mark.parametrize("name", ["int8_16x7168x4096", "w4a8_16x7168x4096"])
+def test_bench_independent_runs_match_oracle(name):
+    dev = torch.device("cuda", 0)
+    prob = bench.Problem(name, dev)
+    prob.flags = gp.GP_RUN_B_CONSTANT | gp.GP_RUN_INDEPENDENT
+    for C in prob.C:
+        C.zero_()
+    bench.time_device(prob, 2 * len(prob.C) + 3, 3, None, dev)
+    torch.cuda.synchronize()
+    assert gp.gemm_last_device_status() == 0
+    ops = inputs.workload_operands(name)
+    check_outputs(prob, ops, np.arange(ops.M))
