@@ -424,7 +424,7 @@ def time_e2e(prob: Problem, steps: int, warmup: int, device):
     torch.cuda.synchronize(device)
     # Serving replays captured steps (the copies are graph memcpy nodes):
     # a graph of G steps forks onto the streams and joins back.
-    G = max(S, min(100, steps) // S * S)
+    G = max(S, min(steps, max(100, prob.copies)) // S * S)  # every rotating copy, where steps allow
     graph = torch.cuda.CUDAGraph()
     cap = torch.cuda.Stream(device)
     cap.wait_stream(main)
