@@ -279,6 +279,7 @@ int gemm_run_ex(const void* A, const void* B_packed, int dtype, int64_t M, int64
     p.b_constant = b_constant;
     p.independent = independent;
     p.w4 = w4 ? 1 : 0;
+    p.debug_skip_load = g_debug_skip_load.exchange(0);
     const int64_t b_tiles = kb / 128;  // 128-byte tiles of a packed B row (256 K values for int4)
     // A as [K tiles][M rows][128 B] (3-D view, 128-byte swizzle): one copy
     // brings 8 K tiles of 16 rows.

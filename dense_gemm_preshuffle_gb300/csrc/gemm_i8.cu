@@ -189,7 +189,8 @@ __global__ void __launch_bounds__(I8_THREADS, i8_ctas_per_sm(NB8))
   pdl_launch_dependents();
   __syncthreads();
   if (threadIdx.x == I8_PRODUCER * 32)
-    for (int q = 0; q < early; ++q) load_b(q);
+    for (int q = 0; q < early; ++q)
+      if (p.debug_skip_load != 1 + q) load_b(q);  // fault injection: see the producer loop
   if (!p.independent) pdl_wait();  // A may be produced, and C read, by the previous kernel
 
   if (warp == I8_PRODUCER) {
@@ -205,16 +206,20 @@ __global__ void __launch_bounds__(I8_THREADS, i8_ctas_per_sm(NB8))
           ok = false;
           break;
         }
-        if (is_b)
-          load_b(q);
-        else
+        if (is_b) {
+          // Fault injection (host-selected): B's copy and arrival for this
+          // stage are left out, so the consumers' waits on it must time out.
+          if (p.debug_skip_load != 1 + q) load_b(q);
+        } else {
           load_a(q);
+        }
       }
       if (!ok || *abort_flag) {
         // wait (bounded) for this thread's copies still in flight
         const int issued = q;
         for (int i = 0; i < I8_STAGES && i < issued; ++i) {
           const int qq = issued - 1 - i;
+          if (is_b && p.debug_skip_load == 1 + qq) continue;  // nothing was issued for it
           volatile int never = 0;
           wait_bounded(&full[qq % I8_STAGES], (uint32_t)(qq / I8_STAGES) & 1, &never, p.status, ST_TIMEOUT_DRAIN,
                        limit);

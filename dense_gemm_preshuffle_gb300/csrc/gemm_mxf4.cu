@@ -156,6 +156,7 @@ __global__ void __launch_bounds__(F4_THREADS, 1)
     int mb, nb;
     f4_tile_coords(blockIdx.x, p.tiles_m, p.tiles_n, mb, nb);
     for (int kt = 0; kt < early; ++kt) {
+      if (p.debug_skip_load == 1 + kt) continue;  // fault injection: see the producer loop
       mbar_arrive_expect_tx(&full[kt], Cfg::STAGE_TX);
       load_b(kt, nb, kt);
     }
@@ -178,7 +179,10 @@ __global__ void __launch_bounds__(F4_THREADS, 1)
         int mb, nb;
         f4_tile_coords(t, p.tiles_m, p.tiles_n, mb, nb);
         for (int kt = 0; kt < p.ktiles; ++kt) {
-          if ((int)issued < early) {  // a free stage whose B is already requested
+          if (p.debug_skip_load == 1 + (int)issued) {
+            // Fault injection (host-selected): this stage gets neither copies
+            // nor the producer's arrival, so the waits on it must time out.
+          } else if ((int)issued < early) {  // a free stage whose B is already requested
             tma_load_2d(s_a + s * Cfg::A_BYTES, &tmA, kt * 128, mb * 128, &full[s]);
           } else {
             if (!wait_bounded(&empty[s], ph ^ 1, abort_flag, p.status, ST_TIMEOUT_PRODUCER, limit)) {
@@ -202,6 +206,7 @@ __global__ void __launch_bounds__(F4_THREADS, 1)
         const uint32_t n = issued < (uint32_t)F4_STAGES ? issued : (uint32_t)F4_STAGES;
         for (uint32_t i = 0; i < n; ++i) {
           const uint32_t q = issued - 1 - i;
+          if (p.debug_skip_load == 1 + (int)q) continue;  // nothing was issued for it
           volatile int never = 0;
           wait_bounded(&full[q % F4_STAGES], (q / F4_STAGES) & 1, &never, p.status, ST_TIMEOUT_DRAIN, limit);
         }

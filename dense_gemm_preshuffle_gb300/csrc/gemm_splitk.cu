@@ -160,6 +160,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
   const int early = p.b_constant ? min(ks, SK_STAGES) : 0;
   if (threadIdx.x == 0) {  // the producer thread, which initialised the barriers
     for (int i = 0; i < early; ++i) {
+      if (p.debug_skip_load == 1 + i) continue;  // fault injection: see the producer loop
       mbar_arrive_expect_tx(&full[i], SK_STAGE_BYTES);
       for (int j = 0; j < SK_BN / 128; ++j)
         bulk_load(s_b + i * SK_B_BYTES + j * 16384,
@@ -183,6 +184,12 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
         const int s = i % SK_STAGES;
         const uint32_t ph = (uint32_t)(i / SK_STAGES) & 1;
         const int kt = k0 + i;
+        if (p.debug_skip_load == 1 + i) {
+          // Fault injection (host-selected): this stage gets neither copies
+          // nor the producer's arrival, so the waits on it must time out.
+          ++issued;
+          continue;
+        }
         if (i < early) {  // a free stage whose B is already requested
           tma_load_2d(s_a + s * SK_A_BYTES, &tmA, kt * 128, mb * SK_BM, &full[s]);
           ++issued;
@@ -202,6 +209,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
         const uint32_t n = issued < (uint32_t)SK_STAGES ? issued : (uint32_t)SK_STAGES;
         for (uint32_t i = 0; i < n; ++i) {
           const uint32_t q = issued - 1 - i;
+          if (p.debug_skip_load == 1 + (int)q) continue;  // nothing was issued for it
           volatile int never = 0;
           wait_bounded(&full[q % SK_STAGES], (q / SK_STAGES) & 1, &never, p.status, ST_TIMEOUT_DRAIN, limit);
         }

@@ -38,6 +38,7 @@ struct I8Params {
   int b_constant;         // 1: B may be read before the previous kernel on the stream completes
   int independent;        // 1: nothing in flight touches the operands; wait for the previous kernel only at exit
   int w4;                 // 1: B is int4 (W4A8), packed as PACK_W4
+  int debug_skip_load;    // 0 = off; i > 0: the B producer skips its i-th stage load
 };
 
 void tc_tile_choice(int64_t M, int64_t N, int num_sms, int* bm, int* bn);

@@ -262,14 +262,15 @@ const char* gemm_status_string(int status);
 
 /*
  * Fault-injection hook for tests of the bounded waits; it has no
- * counterpart in the method.  The next tcgen05 GEMM launched by gemm_run
- * skips its producer's `index`-th shared-memory stage load (1-based).  The
- * MMA warp's wait for that stage then times out after the wait limit, which
+ * counterpart in the method.  The next GEMM launched by gemm_run (any of
+ * its kernels: tile, split-K, MXFP4, INT8/W4A8) skips its producer's
+ * `index`-th shared-memory stage load (1-based; for INT8/W4A8 the B load).
+ * The waits for that stage then time out after the wait limit, which
  * defaults to 2 s and is overridden by the environment variable
  * GP_WAIT_LIMIT_MS, read once per process.
  *
  * When the wait times out, the kernel drains its in-flight copies, frees
- * its tensor memory and exits.  The library's status word is set, and
+ * any tensor memory and exits.  The library's status word is set, and
  * gemm_last_device_status() reports GP_ERR_DEVICE_TIMEOUT.  The hook
  * disarms itself after one launch.  index = 0 disarms it.  Host-only.
  */
