@@ -232,8 +232,10 @@ int gemm_run_ex(const void* A, const void* B_packed, int dtype, int64_t M, int64
   int rc = check_nk(dtype, N, K, &kb);
   if (rc != GP_OK) return rc;
   if (M < 0 || M >= (int64_t(1) << 31)) return GP_ERR_SHAPE;
-  if (dtype == GP_INT8 && K > 131072) return GP_ERR_SHAPE;      // exact result must fit int32
-  if (dtype == GP_W4A8 && K > 2097152) return GP_ERR_SHAPE;     // 128 * 8 * K < 2^31
+  // the exact result must fit int32 for every input: K * 128 * 128 < 2^31
+  // (int8 x int8) and K * 128 * 8 < 2^31 (int8 x int4)
+  if (dtype == GP_INT8 && K >= 131072) return GP_ERR_SHAPE;
+  if (dtype == GP_W4A8 && K >= 2097152) return GP_ERR_SHAPE;
   const size_t c_elem = c_dtype == GP_INT32 ? 4 : 2;
   if (M == 0 || N == 0) return GP_OK;  // empty output
   // ---- pointers

@@ -152,7 +152,8 @@ int gemm_unpack_b(const void* B_packed, int dtype, int64_t N, int64_t K, void* B
  * Shape rules: M >= 1 (any value), N and K as for gemm_packed_b_bytes, and
  * M, N, K < 2^31.  E2M1 also needs N % 256 == 0 (its tiles are 256 wide).
  * For INT8 the exact result must fit int32, which holds for every input
- * when K <= 131072 (W4A8: K <= 2097152).
+ * when K < 131072, i.e. K <= 130944 (W4A8: K < 2097152, i.e. K <= 2096896):
+ * (-128) * (-128) * 131072 is already 2^31.
  * Float outputs are rounded to nearest-even from the fp32 value (an fp16
  * output saturates to infinity beyond 65504, as IEEE rounding does).
  * The call launches one kernel and allocates no memory.  K == 0 writes

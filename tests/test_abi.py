@@ -107,6 +107,16 @@ def test_run_ex_rejects_unknown_flags(lib):
         assert rc == 3
 
 
+@pytest.mark.parametrize("dtype,k_ok,k_bad", [("int8", 130944, 131072), ("w4a8", 2096896, 2097152)])
+def test_integer_k_limit_keeps_the_exact_result_in_int32(lib, dtype, k_ok, k_bad):
+    # at k_bad, (-128) * (-128) * K (int8) or (-128) * (-8) * K (int4) reaches
+    # 2^31; M = 0 makes a valid call a no-op (the shape rules still apply)
+    assert lib.gemm_run_ex(None, None, gp.DTYPES[dtype], 0, 256, k_bad, 0, None, None, 0, None, None,
+                           gp.DTYPES["int32"], 0, None) == 3
+    assert lib.gemm_run_ex(None, None, gp.DTYPES[dtype], 0, 256, k_ok, 0, None, None, 0, None, None,
+                           gp.DTYPES["int32"], 0, None) == 0
+
+
 @pytest.mark.parametrize("epi,bias,dtype,c_dtype,code", [
     (5, FAKE, "e4m3", "bf16", 1),        # unknown epilogue
     (-1, FAKE, "e4m3", "bf16", 1),
