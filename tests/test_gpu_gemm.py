@@ -220,6 +220,29 @@ def test_int8_extremes_bit_exact():
     check(ops, gpu_gemm(ops))
 
 
+@pytest.mark.parametrize("dtype,K", [("int8", 130944), ("w4a8", 2096896)])
+def test_integer_extremes_at_the_k_limit(dtype, K):
+    """The largest K the ABI accepts: all -128 (x -128 or x -8) sums to just
+    below 2^31, and the exact int32 result survives every partial sum."""
+    M, N = 16, 256
+    a = np.full((M, K), -128, np.int8)
+    rng = np.random.default_rng(1)
+    a[1] = 127
+    a[2:] = rng.choice(np.array([-128, 127, 0, -1], np.int8), size=(M - 2, K))
+    if dtype == "int8":
+        b = np.full((N, K), -128, np.int8)
+        b[1] = 127
+    else:
+        b = np.full((N, K // 2), 0x88, np.uint8)  # every nibble -8
+        b[1] = 0x77                                # every nibble 7
+    ops = inputs.Operands(dtype, M, N, K, a, b)
+    C = gpu_gemm(ops)
+    rows = np.arange(M)
+    ref = oracle.gemm_operands(ops, rows=rows)
+    assert ref[0, 0] == K * 128 * (128 if dtype == "int8" else 8) and ref[0, 0] < 2**31
+    check(ops, C)
+
+
 def test_w4a8_extremes_bit_exact():
     M, N, K = 16, 256, 4096
     a = np.full((M, K), -128, np.int8)
