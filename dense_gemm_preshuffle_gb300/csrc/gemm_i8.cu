@@ -116,7 +116,7 @@ __global__ void __launch_bounds__(I8_THREADS, i8_ctas_per_sm(NB8))
   const int units = p.N >> 3;
   const int u0 = blockIdx.x * NB8;
   const int nu = min(NB8, units - u0);  // units of this strip that exist (the last strip may be short)
-  const int mg = blockIdx.y;
+  const int mg = p.mg0 + (int)blockIdx.y;  // this CTA's group of 16 rows of A
   const int nstages = (p.ktiles + I8_KT - 1) / I8_KT;
   const uint64_t limit = p.wait_limit_ns;
   {
@@ -436,9 +436,29 @@ int i8_strip_rows(int N, int num_sms) {
   return one_per_sm > 64 ? 64 : one_per_sm;
 }
 
+static int i8_gemm_launch_groups(const CUtensorMap& tmA, const CUtensorMap& tmB, I8Params p, int ngroups,
+                                 cudaStream_t stream);
+
 int i8_gemm_launch(const CUtensorMap& tmA, const CUtensorMap& tmB, I8Params p, int num_sms, cudaStream_t stream) {
+  const int groups = (p.M + 15) / 16;  // groups of 16 rows of A
+  if (groups > 65535) {
+    // more row groups than one grid's y extent: one launch per 65535 groups
+    for (int g0 = 0; g0 < groups; g0 += 65535) {
+      I8Params q = p;
+      q.mg0 = g0;
+      const int rc = i8_gemm_launch_groups(tmA, tmB, q, min(65535, groups - g0), stream);
+      if (rc != GP_OK) return rc;
+    }
+    return GP_OK;
+  }
+  p.mg0 = 0;
+  return i8_gemm_launch_groups(tmA, tmB, p, groups, stream);
+}
+
+static int i8_gemm_launch_groups(const CUtensorMap& tmA, const CUtensorMap& tmB, I8Params p, int ngroups,
+                                 cudaStream_t stream) {
   const int strip = p.strip;
-  dim3 grid((unsigned)((p.N + strip - 1) / strip), (unsigned)((p.M + 15) / 16));
+  dim3 grid((unsigned)((p.N + strip - 1) / strip), (unsigned)ngroups);
   if (p.w4) {
     switch (strip) {
       case 16: return launch_i8<2, true>(tmA, tmB, p, grid, stream);

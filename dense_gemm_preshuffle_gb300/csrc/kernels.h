@@ -39,6 +39,7 @@ struct I8Params {
   int independent;        // 1: nothing in flight touches the operands; wait for the previous kernel only at exit
   int w4;                 // 1: B is int4 (W4A8), packed as PACK_W4
   int debug_skip_load;    // 0 = off; i > 0: the B producer skips its i-th stage load
+  int mg0;                // first group of 16 rows of A of this launch (grids hold <= 65535 groups)
 };
 
 void tc_tile_choice(int64_t M, int64_t N, int num_sms, int* bm, int* bn);

@@ -150,7 +150,8 @@ int gemm_unpack_b(const void* B_packed, int dtype, int64_t N, int64_t K, void* B
  * Other combinations return GP_ERR_UNSUPPORTED.
  *
  * Shape rules: M >= 1 (any value), N and K as for gemm_packed_b_bytes, and
- * M, N, K < 2^31.  E2M1 also needs N % 256 == 0 (its tiles are 256 wide).
+ * M, N, K < 2^31.  (The INT8/W4A8 kernel is built for small M; past 65535
+ * groups of 16 rows it is launched once per 65535 groups.)  E2M1 also needs N % 256 == 0 (its tiles are 256 wide).
  * For INT8 the exact result must fit int32, which holds for every input
  * when K < 131072, i.e. K <= 130944 (W4A8: K < 2097152, i.e. K <= 2096896):
  * (-128) * (-128) * 131072 is already 2^31.

@@ -243,6 +243,18 @@ def test_integer_extremes_at_the_k_limit(dtype, K):
     check(ops, C)
 
 
+def test_int8_more_row_groups_than_one_grid():
+    """M past 65535 groups of 16 rows: the launcher splits the row groups
+    over launches; rows on both sides of the split are checked."""
+    M, N, K = 16 * 65537, 128, 256
+    ops = inputs.make_operands("int8", M, N, K, seed=77)
+    C = gpu_gemm(ops)
+    split = 16 * 65535
+    rows = np.unique(np.concatenate([np.arange(16), np.arange(split - 16, split + 32), [M - 1],
+                                     np.random.default_rng(3).choice(M, 64, replace=False)]))
+    check(ops, C, rows=rows)
+
+
 def test_w4a8_extremes_bit_exact():
     M, N, K = 16, 256, 4096
     a = np.full((M, K), -128, np.int8)
