@@ -188,38 +188,38 @@ __global__ void __launch_bounds__(I8_THREADS, i8_ctas_per_sm(NB8))
   }
   pdl_launch_dependents();
   __syncthreads();
+  // Fault injection (host-selected): B is issued only up to, not including,
+  // stage debug_skip_load - 1, so the consumers' waits on that stage must
+  // time out. The bound is computed once, off the per-stage path.
+  const int b_end = p.debug_skip_load > 0 ? min(nstages, p.debug_skip_load - 1) : nstages;
   if (threadIdx.x == I8_PRODUCER * 32)
-    for (int q = 0; q < early; ++q)
-      if (p.debug_skip_load != 1 + q) load_b(q);  // fault injection: see the producer loop
+    for (int q = 0; q < min(early, b_end); ++q) load_b(q);
   if (!p.independent) pdl_wait();  // A may be produced, and C read, by the previous kernel
 
   if (warp == I8_PRODUCER) {
     // ------------------------------------------------------------ producers
     if (lane < 2) {
       const bool is_b = lane == 0;
-      int q = is_b ? early : 0;
+      int q = is_b ? min(early, b_end) : 0;
+      const int q_end = is_b ? b_end : nstages;
       bool ok = true;
-      for (; q < nstages; ++q) {
+      for (; q < q_end; ++q) {
         const int s = q % I8_STAGES;
         const uint32_t ph = (uint32_t)(q / I8_STAGES) & 1;
         if (!wait_bounded(&empty[s], ph ^ 1, abort_flag, p.status, ST_TIMEOUT_PRODUCER, limit)) {
           ok = false;
           break;
         }
-        if (is_b) {
-          // Fault injection (host-selected): B's copy and arrival for this
-          // stage are left out, so the consumers' waits on it must time out.
-          if (p.debug_skip_load != 1 + q) load_b(q);
-        } else {
+        if (is_b)
+          load_b(q);
+        else
           load_a(q);
-        }
       }
       if (!ok || *abort_flag) {
         // wait (bounded) for this thread's copies still in flight
         const int issued = q;
         for (int i = 0; i < I8_STAGES && i < issued; ++i) {
           const int qq = issued - 1 - i;
-          if (is_b && p.debug_skip_load == 1 + qq) continue;  // nothing was issued for it
           volatile int never = 0;
           wait_bounded(&full[qq % I8_STAGES], (uint32_t)(qq / I8_STAGES) & 1, &never, p.status, ST_TIMEOUT_DRAIN,
                        limit);

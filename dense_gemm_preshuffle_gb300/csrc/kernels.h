@@ -38,7 +38,7 @@ struct I8Params {
   int b_constant;         // 1: B may be read before the previous kernel on the stream completes
   int independent;        // 1: nothing in flight touches the operands; wait for the previous kernel only at exit
   int w4;                 // 1: B is int4 (W4A8), packed as PACK_W4
-  int debug_skip_load;    // 0 = off; i > 0: the B producer skips its i-th stage load
+  int debug_skip_load;    // 0 = off; i > 0: the B producer stops before its i-th stage load
   int mg0;                // first group of 16 rows of A of this launch (grids hold <= 65535 groups)
 };
 

@@ -266,7 +266,8 @@ const char* gemm_status_string(int status);
  * Fault-injection hook for tests of the bounded waits; it has no
  * counterpart in the method.  The next GEMM launched by gemm_run (any of
  * its kernels: tile, split-K, MXFP4, INT8/W4A8) skips its producer's
- * `index`-th shared-memory stage load (1-based; for INT8/W4A8 the B load).
+ * `index`-th shared-memory stage load (1-based).  For INT8/W4A8 the B
+ * load of that stage and of every later stage is skipped.
  * The waits for that stage then time out after the wait limit, which
  * defaults to 2 s and is overridden by the environment variable
  * GP_WAIT_LIMIT_MS, read once per process.
