@@ -401,8 +401,8 @@ int gemm_quantize_a(const void* X, int x_dtype, int64_t M, int64_t K, int q_dtyp
   DeviceInfo* d = nullptr;
   int rc = device_info(&d);
   if (rc != GP_OK) return rc;
-  return quant_launch(X, x_dtype == GP_BF16, M, K, q_dtype == GP_E2M1, A_out, scales_out,
-                      static_cast<cudaStream_t>(stream));
+  return quant_launch(X, x_dtype == GP_BF16, M, K, q_dtype == GP_E2M1, A_out, scales_out, d->num_sms, d->status,
+                      wait_limit_ns(), static_cast<cudaStream_t>(stream));
 }
 
 // Test hook: the next tcgen05 GEMM launch skips the producer's `index`-th

@@ -56,8 +56,8 @@ int mxf4_gemm_launch(const CUtensorMap& tmA, const CUtensorMap& tmC, TcParams p,
 int i8_strip_rows(int N, int num_sms);
 int i8_gemm_launch(const CUtensorMap& tmA, const CUtensorMap& tmB, I8Params p, int num_sms, cudaStream_t stream);
 
-int quant_launch(const void* X, bool x_bf16, int64_t M, int64_t K, bool to_e2m1, void* Q, void* S,
-                 cudaStream_t stream);
+int quant_launch(const void* X, bool x_bf16, int64_t M, int64_t K, bool to_e2m1, void* Q, void* S, int num_sms,
+                 uint32_t* status, uint64_t limit_ns, cudaStream_t stream);
 
 // Packed-B layouts: 128-row bands, bytes as given (tcgen05 types); 8-row
 // bands in offset binary (INT8); 8-row bands, interleaved offset-binary

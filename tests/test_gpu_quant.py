@@ -38,8 +38,9 @@ def special_rows(K):
 @pytest.mark.parametrize("q", ["e4m3", "e2m1"])
 @pytest.mark.parametrize("xd", ["fp32", "bf16"])
 @pytest.mark.parametrize("M,K", [(1, 32), (37, 256), (300, 1024), (16, 7168), (5, 8192),
-                                 (3, 16384), (2, 12288),   # rows past 8192: the kernel that reads a row twice
-                                 (300000, 32)])            # more rows than one grid: the striding loops
+                                 (3, 16384), (2, 12288),   # bf16 rows past 8192 (fp32 past 12288): read twice
+                                 (300000, 32),             # more rows than one grid: the striding loops
+                                 (4000, 2048), (1000, 12288)])  # fp32: several rows per CTA through the staged ring
 def test_quantize_bit_exact(q, xd, M, K):
     g = torch.Generator().manual_seed(M * 131 + K)
     x = torch.randn((M, K), generator=g, dtype=torch.float32) * torch.exp(torch.randn((M, 1), generator=g) * 3)
