@@ -227,7 +227,7 @@ int gemm_run_ex(const void* A, const void* B_packed, int dtype, int64_t M, int64
 /*
  * Synchronises `stream`, then reads and clears the library's device status
  * word on the current device.  The word is set when a bounded wait in a GEMM
- * kernel times out, or when a kernel's check of its own launch shape against
+ * or quantiser kernel times out, or when a kernel's check of its own launch shape against
  * its arguments fails (the kernel then returns before touching memory).
  * Returns GP_OK, GP_ERR_DEVICE_TIMEOUT, GP_ERR_DEVICE_CHECK or GP_ERR_CUDA.
  */
@@ -253,8 +253,10 @@ int gemm_last_device_status(void* stream);
  * infinite inputs are not supported.
  * Shape rules: K % 32 == 0; M, K < 2^31.  M == 0 or K == 0 is a no-op.
  * Pointers must be 16-byte aligned (GP_ERR_ALIGNMENT).  One kernel on
- * `stream`; nothing is allocated.  This step precedes the method's GEMM;
- * the pages do it on the host for their inputs.
+ * `stream`; nothing is allocated.  Its waits on its own row copies are
+ * bounded: a timeout sets the device status word (gemm_last_device_status).
+ * This step precedes the method's GEMM; the pages do it on the host for
+ * their inputs.
  */
 int gemm_quantize_a(const void* X, int x_dtype, int64_t M, int64_t K, int q_dtype, void* A_out,
                     void* scales_out, void* stream);
