@@ -14,11 +14,17 @@
  *   - `stream` is a cudaStream_t passed as void*.  NULL means the legacy
  *     default stream.
  *   - Calls are asynchronous with respect to the host and ordered on `stream`.
+ *     The GEMM and quantiser kernels are launched with programmatic
+ *     dependent launch: a kernel may become resident while the previous
+ *     kernel on the stream still runs, but it reads and writes the caller's
+ *     buffers only after that kernel has finished.  The two exceptions are
+ *     opt-in: GP_RUN_B_CONSTANT and GP_RUN_INDEPENDENT (gemm_run_ex).
  *   - Argument errors are detected on the host before anything is launched.
  *     The call then returns a nonzero gp_status and leaves all buffers
  *     untouched.
- *   - Device-side timeouts of the bounded waits inside the GEMM kernels set
- *     a sticky status word.  gemm_last_device_status() reads and clears it.
+ *   - Device-side timeouts of the bounded waits inside the GEMM and
+ *     quantiser kernels set a sticky status word.  gemm_last_device_status()
+ *     reads and clears it.
  *   - Matrices are row-major and densely packed (row pitch = K elements for
  *     A and B, N elements for C).
  *   - Every device pointer must be 16-byte aligned.

@@ -88,6 +88,51 @@ def test_quantize_then_gemm(q, M, N, K):
     assert oracle.max_rel_err(C.float().cpu().numpy().astype(np.float64), ref) <= 8e-3
 
 
+@pytest.mark.parametrize("q", ["e4m3", "e2m1"])
+def test_quantizer_waits_for_the_gemm_reading_its_buffer(q):
+    """Quantiser and GEMM launches overlap their neighbours on the stream
+    (programmatic dependent launch).  Here one A buffer is quantised into,
+    read by a GEMM, and quantised into again, three times back to back.
+    Each quantiser must wait until the GEMM before it has read A, so every
+    product matches its own input."""
+    M, N, K = 1024, 4096, 4096
+    g = torch.Generator().manual_seed(11)
+    xs = [torch.randn((M, K), generator=g) for _ in range(3)]
+    w = torch.randn((N, K), generator=g)
+    Xs = [x.cuda() for x in xs]
+    B, SB = gp.quantize(w.cuda(), q)
+    if q == "e4m3":
+        Bp = gp.preshuffle_b(B, "e4m3")
+        A = torch.empty((M, K), dtype=torch.uint8, device="cuda")
+        S = torch.empty((M,), dtype=torch.float32, device="cuda")
+    else:
+        Bp = gp.preshuffle_b(B, "e2m1", B_scales=SB)
+        A = torch.empty((M, K // 2), dtype=torch.uint8, device="cuda")
+        S = torch.empty((M, K // 32), dtype=torch.uint8, device="cuda")
+    torch.cuda.synchronize()
+    Cs = []
+    for X in Xs:
+        gp.gemm_quantize_a(X, "fp32", M, K, q, A, S, None)
+        Cs.append(gp.matmul(A, Bp, q, N, K, scale_a=S, scale_b=SB if q == "e4m3" else None))
+    torch.cuda.synchronize()
+    assert gp.gemm_last_device_status() == 0
+    rows = np.r_[0:48, M - 48:M]
+    if q == "e4m3":
+        qb, sb = oracle.quantize_e4m3_rows(w.numpy())
+    else:
+        pb, eb = oracle.quantize_mxfp4_rows(w.numpy())
+    for x, C in zip(xs, Cs):
+        xr = x.numpy()[rows]
+        if q == "e4m3":
+            qa, sa = oracle.quantize_e4m3_rows(xr)
+            ref = oracle.gemm_e4m3_rowcol(qa, qb, sa, sb)
+        else:
+            pa, ea = oracle.quantize_mxfp4_rows(xr)
+            ref = oracle.gemm_mxfp4(pa, pb, ea, eb, K)
+        c = C.float().cpu().numpy().astype(np.float64)[rows]
+        assert oracle.max_rel_err(c, ref) <= 8e-3
+
+
 def test_e4m3_near_midpoints_bit_exact():
     """Quotients within a few fp32 ulps of E4M3 rounding midpoints, where the
     kernel must fall back to the IEEE division to match fp32(x / s)."""
