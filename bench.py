@@ -216,19 +216,16 @@ class Problem:
         self.host_a, self.host_sa = t(ops.a), t(ops.scale_a)
         B = t(ops.b).to(device)
         sb = t(ops.scale_b).to(device) if ops.scale_b is not None else None
-        # time the offline pack (device events around the kernel only)
-        bp = torch.empty(gp.gemm_packed_b_bytes(self.dtype, self.N, self.K), dtype=torch.uint8, device=device)
+        # time the offline pack on the device (a CUDA graph of pack calls over
+        # copies of B that rotate past L2), then pack once for the GEMM
         bsf = sb if self.dtype == "e2m1" else None
-        for _ in range(3):
-            gp.gemm_preshuffle_b(B, bsf, self.dtype, self.N, self.K, bp)
+        pack = PackProblem(gp, self.dtype, self.N, self.K, B, bsf, device)
+        pack_steps = max(20, pack.copies)
+        self.pack_us = time_device(pack, pack_steps, 3, None, device) / pack_steps * 1e6
+        del pack
+        bp = torch.empty(gp.gemm_packed_b_bytes(self.dtype, self.N, self.K), dtype=torch.uint8, device=device)
+        gp.gemm_preshuffle_b(B, bsf, self.dtype, self.N, self.K, bp)
         torch.cuda.synchronize(device)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(5):
-            gp.gemm_preshuffle_b(B, bsf, self.dtype, self.N, self.K, bp)
-        e1.record()
-        torch.cuda.synchronize(device)
-        self.pack_us = e0.elapsed_time(e1) * 1e3 / 5
         self.packed_bytes = bp.numel()
         if copies is None:
             copies = max(1, math.ceil(2 * L2_BYTES / max(1, bp.numel())) + 1)
@@ -259,6 +256,24 @@ class Problem:
         self.gp.gemm_run_ex(self.A[j], self.Bp[j], self.dtype, self.M, self.N, self.K, self.mode,
                             self.sa, self.sb, self.epilogue, self.bias, self.C[j % len(self.C)], self.c_dtype,
                             self.flags, stream)
+
+
+class PackProblem:
+    """The offline pack of B as a timed step: copies of B (and of the packed
+    output) rotate past L2, so each pack reads and writes HBM."""
+
+    def __init__(self, gp, dtype, N, K, B, bsf, device):
+        import torch
+        self.gp, self.dtype, self.N, self.K, self.bsf = gp, dtype, N, K, bsf
+        out_bytes = gp.gemm_packed_b_bytes(dtype, N, K)
+        pair = B.numel() * B.element_size() + out_bytes
+        self.copies = max(1, math.ceil(2 * L2_BYTES / max(1, pair)) + 1)
+        self.B = [B] + [B.clone() for _ in range(self.copies - 1)]
+        self.out = [torch.empty(out_bytes, dtype=torch.uint8, device=device) for _ in range(self.copies)]
+
+    def step(self, i: int, stream=None):
+        j = i % self.copies
+        self.gp.gemm_preshuffle_b(self.B[j], self.bsf, self.dtype, self.N, self.K, self.out[j], stream)
 
 
 def time_device(prob: Problem, steps: int, warmup: int, pg, device, graph_len: int = 100):

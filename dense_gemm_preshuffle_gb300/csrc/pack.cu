@@ -66,38 +66,50 @@ __device__ __forceinline__ uint32_t w4_deinterleave(uint32_t w) {
   return out;
 }
 
-// One thread per 16-byte chunk of B.
-__global__ void pack_data_kernel(const uint4* __restrict__ B, int64_t N, int64_t kbytes, int rshift, uint32_t bias,
-                                 bool w4, uint8_t* __restrict__ out) {
-  const int64_t chunks_per_row = kbytes >> 4;
-  const int64_t total = N * chunks_per_row;
-  const int64_t ktiles = kbytes >> 7;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t n = i / chunks_per_row, cc = i - n * chunks_per_row;
-    uint4 v = B[i];
-    if (w4) {
-      v.x = w4_interleave(v.x), v.y = w4_interleave(v.y), v.z = w4_interleave(v.z), v.w = w4_interleave(v.w);
-    } else {
-      v.x ^= bias, v.y ^= bias, v.z ^= bias, v.w ^= bias;
-    }
-    *reinterpret_cast<uint4*>(out + packed_chunk_offset(n, cc, ktiles, rshift)) = v;
-  }
-}
+// One warp per row of B; its lanes take consecutive 16-byte chunks, so a
+// step reads 512 contiguous bytes of the row (pack) and writes whole
+// 128-byte row segments of four tiles (the slot permutation stays inside a
+// segment).  Each lane loads PACK_UNROLL chunks before it stores any, for
+// more bytes in flight.  UNPACK runs the same walk in reverse.
+constexpr int PACK_WARPS = 8, PACK_UNROLL = 4;
 
-__global__ void unpack_data_kernel(const uint8_t* __restrict__ in, int64_t N, int64_t kbytes, int rshift,
-                                   uint32_t bias, bool w4, uint4* __restrict__ B) {
-  const int64_t chunks_per_row = kbytes >> 4;
-  const int64_t total = N * chunks_per_row;
+template <bool UNPACK>
+__global__ void __launch_bounds__(32 * PACK_WARPS)
+    pack_rows_kernel(const uint8_t* __restrict__ src, int64_t N, int64_t kbytes, int rshift, uint32_t bias, bool w4,
+                     uint8_t* __restrict__ dst) {
+  const int lane = threadIdx.x & 31;
+  const int64_t cpr = kbytes >> 4;  // 16-byte chunks per row
   const int64_t ktiles = kbytes >> 7;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t n = i / chunks_per_row, cc = i - n * chunks_per_row;
-    uint4 v = *reinterpret_cast<const uint4*>(in + packed_chunk_offset(n, cc, ktiles, rshift));
-    if (w4) {
-      v.x = w4_deinterleave(v.x), v.y = w4_deinterleave(v.y), v.z = w4_deinterleave(v.z), v.w = w4_deinterleave(v.w);
-    } else {
-      v.x ^= bias, v.y ^= bias, v.z ^= bias, v.w ^= bias;
+  for (int64_t n = (int64_t)blockIdx.x * PACK_WARPS + (threadIdx.x >> 5); n < N; n += (int64_t)gridDim.x * PACK_WARPS) {
+    for (int64_t c0 = 0; c0 < cpr; c0 += 32 * PACK_UNROLL) {
+      uint4 v[PACK_UNROLL];
+#pragma unroll
+      for (int u = 0; u < PACK_UNROLL; ++u) {
+        const int64_t cc = c0 + u * 32 + lane;
+        if (cc < cpr) {
+          const int64_t off = UNPACK ? packed_chunk_offset(n, cc, ktiles, rshift) : (n * cpr + cc) * 16;
+          v[u] = *reinterpret_cast<const uint4*>(src + off);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < PACK_UNROLL; ++u) {
+        const int64_t cc = c0 + u * 32 + lane;
+        if (cc < cpr) {
+          uint4 x = v[u];
+          if (w4) {
+            if (UNPACK)
+              x.x = w4_deinterleave(x.x), x.y = w4_deinterleave(x.y), x.z = w4_deinterleave(x.z),
+              x.w = w4_deinterleave(x.w);
+            else
+              x.x = w4_interleave(x.x), x.y = w4_interleave(x.y), x.z = w4_interleave(x.z), x.w = w4_interleave(x.w);
+          } else {
+            x.x ^= bias, x.y ^= bias, x.z ^= bias, x.w ^= bias;
+          }
+          const int64_t off = UNPACK ? (n * cpr + cc) * 16 : packed_chunk_offset(n, cc, ktiles, rshift);
+          *reinterpret_cast<uint4*>(dst + off) = x;
+        }
+      }
     }
-    B[i] = v;
   }
 }
 
@@ -126,11 +138,10 @@ static int grid_for(int64_t total, int threads) {
 
 int pack_b_launch(const uint8_t* B, const uint8_t* Bsf, int64_t N, int64_t kbytes, int64_t nblk, int layout,
                   uint8_t* out, cudaStream_t stream) {
-  const int64_t chunks = N * (kbytes >> 4);
   const int rshift = layout == PACK_TC ? 7 : 3;
   const uint32_t bias = layout == PACK_INT8 ? 0x80808080u : 0u;
-  pack_data_kernel<<<grid_for(chunks, 256), 256, 0, stream>>>(reinterpret_cast<const uint4*>(B), N, kbytes, rshift,
-                                                              bias, layout == PACK_W4, out);
+  pack_rows_kernel<false><<<grid_for(N, PACK_WARPS), 32 * PACK_WARPS, 0, stream>>>(B, N, kbytes, rshift, bias,
+                                                                                  layout == PACK_W4, out);
   if (Bsf != nullptr)
     pack_scale_kernel<<<grid_for(N * nblk, 256), 256, 0, stream>>>(Bsf, N, nblk, out + N * kbytes);
   return cudaGetLastError() == cudaSuccess ? GP_OK : GP_ERR_CUDA;
@@ -138,11 +149,10 @@ int pack_b_launch(const uint8_t* B, const uint8_t* Bsf, int64_t N, int64_t kbyte
 
 int unpack_b_launch(const uint8_t* packed, int64_t N, int64_t kbytes, int64_t nblk, int layout, uint8_t* B,
                     uint8_t* Bsf, cudaStream_t stream) {
-  const int64_t chunks = N * (kbytes >> 4);
   const int rshift = layout == PACK_TC ? 7 : 3;
   const uint32_t bias = layout == PACK_INT8 ? 0x80808080u : 0u;
-  unpack_data_kernel<<<grid_for(chunks, 256), 256, 0, stream>>>(packed, N, kbytes, rshift, bias, layout == PACK_W4,
-                                                                reinterpret_cast<uint4*>(B));
+  pack_rows_kernel<true><<<grid_for(N, PACK_WARPS), 32 * PACK_WARPS, 0, stream>>>(packed, N, kbytes, rshift, bias,
+                                                                                 layout == PACK_W4, B);
   if (Bsf != nullptr)
     unpack_scale_kernel<<<grid_for(N * nblk, 256), 256, 0, stream>>>(packed + N * kbytes, N, nblk, Bsf);
   return cudaGetLastError() == cudaSuccess ? GP_OK : GP_ERR_CUDA;
