@@ -258,6 +258,14 @@ class Problem:
                             self.flags, stream)
 
 
+def gpu_record(device) -> dict:
+    """The GPU the numbers were taken on (name, SMs, L2, compute capability)."""
+    import torch
+    pr = torch.cuda.get_device_properties(device)
+    return {"name": pr.name, "sms": pr.multi_processor_count, "l2_bytes": getattr(pr, "L2_cache_size", None),
+            "cc": f"{pr.major}.{pr.minor}", "memory_bytes": pr.total_memory}
+
+
 class PackProblem:
     """The offline pack of B as a timed step: copies of B (and of the packed
     output) rotate past L2, so each pack reads and writes HBM."""
@@ -585,6 +593,7 @@ def run_ours(args):
         "roofline": roofline(prob, per, peaks, peak_kind, traffic_from_profiles(prob.name)),
         "trials": trials,
         "clocks": clock_summary,
+        "gpu": gpu_record(device),
         "pack_b": {"us": round(prob.pack_us, 2), "bytes": prob.packed_bytes,
                    "GB/s": round(2 * prob.packed_bytes / (prob.pack_us * 1e-6) / 1e9, 1)},
     }
