@@ -250,9 +250,12 @@ __global__ void __launch_bounds__(I8_THREADS, i8_ctas_per_sm(NB8))
     for (int nb = 0; nb < NB8; ++nb) f[nb][0] = f[nb][1] = f[nb][2] = f[nb][3] = 0.f;
     if constexpr (W4) {
       // K tile `warp` of A is half of packed B tile warp / 2: lane t's 32 K
-      // values are one 16-byte chunk, 4 * (warp % 2) + t, of each B row.
+      // values are one 16-byte chunk, 4 * (warp % 2) + t, of each B row,
+      // stored at slot chunk ^ g ^ 4 (g % 2) (the W4A8 packing), so the 8
+      // lanes of rows g and g ^ 1 that load together hit 8 distinct bank
+      // groups.
       const uint8_t* sb = base + s * STAGE + A_BYTES + ((warp >> 1) * 8 + g) * 128 +
-                          (((4 * (warp & 1) + t) ^ g) << 4);  // + unit * (BT * 8 * 128)
+                          (((4 * (warp & 1) + t) ^ g ^ ((g & 1) << 2)) << 4);  // + unit * (BT * 8 * 128)
       uint4 bw[NB8];
 #pragma unroll
       for (int nb = 0; nb < NB8; ++nb) bw[nb] = *reinterpret_cast<const uint4*>(sb + nb * (BT * 8 * 128));

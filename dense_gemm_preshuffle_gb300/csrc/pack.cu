@@ -17,7 +17,11 @@
 //     c ^ (r % 8).  This is the 128-byte-swizzled K-major image that tcgen05
 //     descriptors and TMA use, so one bulk copy lands a tile in shared memory
 //     ready for the MMA, and 8 rows reading the same chunk hit 8 distinct
-//     bank groups.
+//     bank groups.  W4A8 stores chunk c at c ^ (r % 8) ^ 4 (r % 2) instead:
+//     its kernel reads chunks c0 .. c0 + 3 of rows 2i and 2i + 1 in one
+//     shared-memory phase, and the flip puts the two rows in different halves
+//     of the banks (with c ^ (r % 8) alone every such read was 2-way
+//     conflicted).
 //   - E2M1 block scales ([N, K/32] bytes) follow the data region.  Per
 //     (tn, tk) they take two 512-byte groups of four K blocks.  Inside a
 //     group, (row r, block j) is at (r%32)*16 + (r/32)*4 + j%4: the 32-lane
@@ -26,11 +30,13 @@
 
 namespace gp {
 
-// rshift = log2(R)
-__device__ __forceinline__ int64_t packed_chunk_offset(int64_t n, int64_t cc, int64_t ktiles, int rshift) {
+// rshift = log2(R).  w4: W4A8's slot rule, which also flips slot bit 2 on
+// odd rows (see the header comment).
+__device__ __forceinline__ int64_t packed_chunk_offset(int64_t n, int64_t cc, int64_t ktiles, int rshift, bool w4) {
   const int64_t tn = n >> rshift, r = n & ((int64_t(1) << rshift) - 1);
   const int64_t tk = cc >> 3, c = cc & 7;
-  return (((tn * ktiles + tk) << rshift) + r) * 128 + ((c ^ (r & 7)) << 4);
+  const int64_t mask = (r & 7) ^ (w4 ? (r & 1) << 2 : 0);
+  return (((tn * ktiles + tk) << rshift) + r) * 128 + ((c ^ mask) << 4);
 }
 
 __device__ __forceinline__ int64_t packed_scale_offset(int64_t n, int64_t j, int64_t nblk) {
@@ -87,7 +93,7 @@ __global__ void __launch_bounds__(32 * PACK_WARPS)
       for (int u = 0; u < PACK_UNROLL; ++u) {
         const int64_t cc = c0 + u * 32 + lane;
         if (cc < cpr) {
-          const int64_t off = UNPACK ? packed_chunk_offset(n, cc, ktiles, rshift) : (n * cpr + cc) * 16;
+          const int64_t off = UNPACK ? packed_chunk_offset(n, cc, ktiles, rshift, w4) : (n * cpr + cc) * 16;
           v[u] = *reinterpret_cast<const uint4*>(src + off);
         }
       }
@@ -105,7 +111,7 @@ __global__ void __launch_bounds__(32 * PACK_WARPS)
           } else {
             x.x ^= bias, x.y ^= bias, x.z ^= bias, x.w ^= bias;
           }
-          const int64_t off = UNPACK ? (n * cpr + cc) * 16 : packed_chunk_offset(n, cc, ktiles, rshift);
+          const int64_t off = UNPACK ? (n * cpr + cc) * 16 : packed_chunk_offset(n, cc, ktiles, rshift, w4);
           *reinterpret_cast<uint4*>(dst + off) = x;
         }
       }

@@ -455,8 +455,13 @@ def band_rows(dtype: str) -> int:
     return 8 if dtype in ("int8", "w4a8") else TILE_ROWS
 
 
-def packed_offset(n: np.ndarray, kb: np.ndarray, Kb: int, rows: int = TILE_ROWS) -> np.ndarray:
-    """Byte offset in the packed buffer of byte (n, kb) of B, for tiles of `rows` rows."""
+def packed_offset(n: np.ndarray, kb: np.ndarray, Kb: int, rows: int = TILE_ROWS, w4: bool = False) -> np.ndarray:
+    """Byte offset in the packed buffer of byte (n, kb) of B, for tiles of `rows` rows.
+
+    The 16-byte chunk c of row r sits at slot c XOR (r mod 8).  W4A8's
+    layout also flips slot bit 2 on odd rows (c XOR (r mod 8) XOR 4 (r mod 2)):
+    its kernel reads four consecutive chunks of rows 2i and 2i + 1 together,
+    and the flip puts the two rows in different halves of the banks."""
     n = np.asarray(n, np.int64)
     kb = np.asarray(kb, np.int64)
     tiles_k = Kb // TILE_BYTES
@@ -464,23 +469,24 @@ def packed_offset(n: np.ndarray, kb: np.ndarray, Kb: int, rows: int = TILE_ROWS)
     tk, col = kb // TILE_BYTES, kb % TILE_BYTES
     chunk, byte = col // 16, col % 16
     tile_index = tn * tiles_k + tk
-    return tile_index * (rows * TILE_BYTES) + r * TILE_BYTES + ((chunk ^ (r % 8)) * 16) + byte
+    mask = (r % 8) ^ (4 * (r % 2)) if w4 else r % 8
+    return tile_index * (rows * TILE_BYTES) + r * TILE_BYTES + ((chunk ^ mask) * 16) + byte
 
 
-def pack_b_bytes(b_bytes: np.ndarray, rows: int = TILE_ROWS) -> np.ndarray:
+def pack_b_bytes(b_bytes: np.ndarray, rows: int = TILE_ROWS, w4: bool = False) -> np.ndarray:
     """Scatter every byte of B [N, Kb] to its packed offset."""
     b = np.ascontiguousarray(b_bytes).view(np.uint8)
     N, Kb = b.shape
     nn, kk = np.meshgrid(np.arange(N), np.arange(Kb), indexing="ij")
     out = np.zeros(N * Kb, dtype=np.uint8)
-    out[packed_offset(nn, kk, Kb, rows).ravel()] = b.ravel()
+    out[packed_offset(nn, kk, Kb, rows, w4).ravel()] = b.ravel()
     return out
 
 
-def unpack_b_bytes(packed: np.ndarray, N: int, Kb: int, rows: int = TILE_ROWS) -> np.ndarray:
+def unpack_b_bytes(packed: np.ndarray, N: int, Kb: int, rows: int = TILE_ROWS, w4: bool = False) -> np.ndarray:
     """Gather B [N, Kb] back from the packed buffer."""
     nn, kk = np.meshgrid(np.arange(N), np.arange(Kb), indexing="ij")
-    return np.asarray(packed, np.uint8)[packed_offset(nn, kk, Kb, rows)]
+    return np.asarray(packed, np.uint8)[packed_offset(nn, kk, Kb, rows, w4)]
 
 
 # Block scales of an MXFP4 B ([N, K/32] UE8M0) are packed per (128-row band,
@@ -546,7 +552,7 @@ def interleave_int4_words(b_packed: np.ndarray) -> np.ndarray:
 def pack_b(b: np.ndarray, dtype: str, scales: Optional[np.ndarray] = None) -> np.ndarray:
     """Whole packed buffer for B (data region, then the scale region for E2M1)."""
     if dtype == "w4a8":
-        return pack_b_bytes(interleave_int4_words(b), band_rows(dtype))
+        return pack_b_bytes(interleave_int4_words(b), band_rows(dtype), w4=True)
     raw = np.ascontiguousarray(b).view(np.uint8).reshape(b.shape[0], -1) ^ np.uint8(byte_bias(dtype))
     data = pack_b_bytes(raw, band_rows(dtype))
     if dtype == "e2m1":

@@ -327,6 +327,28 @@ def check_pack_layout(rows):
             assert len(set(pos[g:g + 8, c * 16].tolist())) == 8
 
 
+def test_w4_layout_spreads_the_kernels_reads_over_all_banks():
+    # The W4A8 kernel's lane (g, t) reads logical chunk c0 + t (c0 = 0 or 4)
+    # of row g.  One 16-byte shared-memory load serves 8 lanes at a time:
+    # rows 2i and 2i + 1, four chunks each.  Those 8 chunks must sit in 8
+    # distinct 16-byte positions of the 128-byte bank window.
+    N, Kb = 16, 256
+    n, k = np.meshgrid(np.arange(N), np.arange(Kb), indexing="ij")
+    pos = (oracle.packed_offset(n, k, Kb, 8, w4=True) % 128) // 16
+    plain = (oracle.packed_offset(n, k, Kb, 8) % 128) // 16
+    for c0 in (0, 4):
+        for i in range(0, 8, 2):
+            chunks = [(c0 + t) * 16 for t in range(4)]
+            assert len({int(pos[r, c]) for r in (i, i + 1) for c in chunks}) == 8
+            # the INT8 slot rule alone puts the two rows on the same 4 positions
+            assert len({int(plain[r, c]) for r in (i, i + 1) for c in chunks}) == 4
+    # a bijection, and every other layout property of the 8-row bands holds
+    offs = oracle.packed_offset(n, k, Kb, 8, w4=True)
+    assert np.array_equal(np.sort(offs.ravel()), np.arange(N * Kb))
+    assert np.all(offs // 1024 == (n // 8) * (Kb // 128) + k // 128)
+    assert np.all((offs % 1024) // 128 == n % 8)
+
+
 def test_pack_band_rows_per_dtype():
     # INT8 packs 8-row bands: a band's K tiles are 1 KiB apart
     assert oracle.band_rows("int8") == 8
@@ -647,7 +669,7 @@ def test_w4a8_pack_word_order():
     pk = oracle.pack_b(bb, "w4a8")
     assert pk.size == bb.size
     il = oracle.interleave_int4_words(bb)
-    assert np.array_equal(pk, oracle.pack_b_bytes(il, 8))
+    assert np.array_equal(pk, oracle.pack_b_bytes(il, 8, w4=True))
 
 
 # ---------------------------------------------------------------- error diagnostic denominator
