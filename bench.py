@@ -403,7 +403,7 @@ def time_quantizers(args, pg, device, peaks, peak_kind):
 
 
 # streams the end-to-end steps alternate over (BENCH_E2E_STREAMS overrides)
-E2E_STREAMS = int(os.environ.get("BENCH_E2E_STREAMS", "4"))
+E2E_STREAMS = int(os.environ.get("BENCH_E2E_STREAMS", "16"))
 
 
 def time_e2e(prob: Problem, steps: int, warmup: int, device):
