@@ -48,6 +48,7 @@ import subprocess
 import sys
 import threading
 import time
+from typing import Optional
 
 import numpy as np
 
@@ -406,13 +407,14 @@ def time_quantizers(args, pg, device, peaks, peak_kind):
 E2E_STREAMS = int(os.environ.get("BENCH_E2E_STREAMS", "16"))
 
 
-def time_e2e(prob: Problem, steps: int, warmup: int, device):
+def time_e2e(prob: Problem, steps: int, warmup: int, device, record: Optional[dict] = None):
     """Through the public call with pinned host buffers: H2D of A (+ its
     scales), gemm_run_ex, D2H of C, every step.  Successive steps alternate
     over E2E_STREAMS streams, so one step's copies overlap another's GEMM
     (each device and host buffer is only ever used by steps of one stream,
     so stream order alone keeps the buffers consistent).  Returns (seconds,
-    h2d bytes, d2h bytes) per step."""
+    h2d bytes, d2h bytes) per step.  `record`, if given, receives the device
+    and host output buffers (for the tests)."""
     import torch
     S = E2E_STREAMS
     ha = prob.host_a.pin_memory()
@@ -476,6 +478,8 @@ def time_e2e(prob: Problem, steps: int, warmup: int, device):
     torch.cuda.synchronize(device)
     h2d = ha.numel() * ha.element_size() + (hsa.numel() * hsa.element_size() if hsa is not None else 0)
     d2h = hc[0].numel() * hc[0].element_size()
+    if record is not None:
+        record["C"], record["host_C"] = C, hc
     return e0.elapsed_time(e1) / 1e3, h2d, d2h
 
 

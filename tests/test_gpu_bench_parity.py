@@ -84,3 +84,30 @@ def test_bench_independent_runs_match_oracle(name):
     assert gp.gemm_last_device_status() == 0
     ops = inputs.workload_operands(name)
     check_outputs(prob, ops, np.arange(ops.M))
+
+
+@pytest.mark.parametrize("name", ["int8_16x7168x4096", "fp8_128x256x512"])
+def test_bench_end_to_end_leg_matches_oracle(name):
+    """The end-to-end leg: host A (and its scales) copied in, gemm_run_ex, C
+    copied out, every step, over the leg's concurrent streams.  Every step
+    computes the same product, so every device output buffer and every host
+    copy must equal the oracle's."""
+    dev = torch.device("cuda", 0)
+    prob = bench.Problem(name, dev)
+    for C in prob.C:
+        C.zero_()
+    rec = {}
+    steps = 4 * bench.E2E_STREAMS
+    bench.time_e2e(prob, steps, 3, dev, record=rec)
+    torch.cuda.synchronize()
+    assert gp.gemm_last_device_status() == 0
+    ops = inputs.workload_operands(name)
+    ref = oracle.gemm_operands(ops)
+    written = rec["C"][:steps]  # step i writes buffer i mod len(C)
+    outs = [c.cpu() for c in written] + list(rec["host_C"])
+    assert len(rec["host_C"]) == bench.E2E_STREAMS
+    for c in outs:
+        if c.dtype == torch.int32:
+            assert np.array_equal(c.numpy().astype(np.int64), ref)
+        else:
+            assert oracle.max_rel_err(c.float().numpy().astype(np.float64), ref) <= TOL
