@@ -3,9 +3,9 @@
 // This layer:
 //   - validates every argument on the host before launching anything;
 //   - builds the TMA tensor maps for A and C;
-//   - picks the kernel (tcgen05 tile kernel, block-scaled MXFP4 kernel, or
-//     the INT8 weight-streaming kernel) and launches it on the caller's
-//     stream.
+//   - picks the kernel (tcgen05 tile kernel, its 2-CTA pair form, split-K
+//     over a cluster, block-scaled MXFP4 kernel, or the INT8
+//     weight-streaming kernel) and launches it on the caller's stream.
 //
 // It owns no per-call memory.  Each device gets a 4-byte status word (a
 // __device__ variable) and a cached SM count.
@@ -323,18 +323,22 @@ int gemm_run_ex(const void* A, const void* B_packed, int dtype, int64_t M, int64
     else
       tc_tile_choice(M, N, d->num_sms, &bm, &bn);
   }
+  // 2-CTA pair tiles replace the single-CTA 128 x 128 and 256 x 256 tiles
+  // where a tile has rows for both CTAs (0: single-CTA tiles).
+  const int pair_bn = (dtype != GP_E2M1 && split == 1) ? pair_choice(M, bm, bn) : 0;
   CUtensorMap tmA, tmC;
-  const int kstep = (dtype != GP_E2M1 && split == 1) ? tc_kstep(bm, bn) : 1;
+  const int kstep = pair_bn != 0 ? kPairKstep : (dtype != GP_E2M1 && split == 1) ? tc_kstep(bm, bn) : 1;
+  const int a_rows = pair_bn != 0 ? 128 : bm;  // rows of A per CTA
   if (kstep == 1) {
     if ((rc = encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, (uint64_t)kb, (uint64_t)M, (uint64_t)kb, 128,
-                        (uint32_t)bm, CU_TENSOR_MAP_SWIZZLE_128B)) != GP_OK)
+                        (uint32_t)a_rows, CU_TENSOR_MAP_SWIZZLE_128B)) != GP_OK)
       return rc;
   } else {
     // A as [K tiles][M rows][128 B] (3-D view, 128-byte swizzle): one copy
-    // brings `kstep` K tiles of a bm-row band.
+    // brings `kstep` K tiles of a CTA's rows.
     cuuint64_t dims[3] = {128, (cuuint64_t)M, (cuuint64_t)(kb / 128)};
     cuuint64_t strides[2] = {(cuuint64_t)kb, 128};
-    cuuint32_t box[3] = {128, (cuuint32_t)bm, (cuuint32_t)kstep};
+    cuuint32_t box[3] = {128, (cuuint32_t)a_rows, (cuuint32_t)kstep};
     cuuint32_t estr[3] = {1, 1, 1};
     if (g_encode(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(A), dims, strides, box, estr,
                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -372,6 +376,21 @@ int gemm_run_ex(const void* A, const void* B_packed, int dtype, int64_t M, int64
   }
   const int kind = dtype == GP_BF16 ? 0 : dtype == GP_E4M3 ? 1 : 2;  // 2: fp16
   if (split > 1) return splitk_gemm_launch(kind, split, tmA, tmC, p, st);
+  if (pair_bn != 0) {
+    // packed B as [tiles][128 rows][128 B] (3-D view, already swizzled):
+    // one copy brings a CTA's pair_bn/2 rows of kPairKstep consecutive tiles
+    // of a band.
+    CUtensorMap tmB;
+    cuuint64_t dims[3] = {128, 128, (cuuint64_t)(N / 128) * (cuuint64_t)(kb / 128)};
+    cuuint64_t strides[2] = {128, 16384};
+    cuuint32_t box[3] = {128, (cuuint32_t)(pair_bn / 2), (cuuint32_t)kPairKstep};
+    cuuint32_t estr[3] = {1, 1, 1};
+    if (g_encode(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(B_packed), dims, strides, box, estr,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return GP_ERR_CUDA;
+    return pair_gemm_launch(kind, pair_bn, tmA, tmB, tmC, p, d->num_sms, st);
+  }
   return tc_gemm_launch(kind, bm, bn, tmA, tmC, p, d->num_sms, st);
 }
 

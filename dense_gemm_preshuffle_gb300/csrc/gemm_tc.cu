@@ -78,17 +78,6 @@ struct TcCfg {
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
-__device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int& mb, int& nb) {
-  constexpr int G = 16;  // M tiles per group: concurrent CTAs cover a compact block of C
-  const int group_size = G * tiles_n;
-  const int group = t / group_size;
-  const int first_m = group * G;
-  const int gm = min(tiles_m - first_m, G);
-  const int r = t - group * group_size;
-  mb = first_m + r % gm;
-  nb = r / gm;
-}
-
 template <int KIND, int BM, int BN, int STAGES, int KSTEP>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmC, TcParams p) {

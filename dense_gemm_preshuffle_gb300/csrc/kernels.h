@@ -42,6 +42,20 @@ struct I8Params {
   int mg0;                // first group of 16 rows of A of this launch (grids hold <= 65535 groups)
 };
 
+// Output tile t of a tiles_m x tiles_n grid, walked in groups of 16 M tiles
+// so that concurrently running CTAs cover a compact block of C and share A
+// rows and B columns in L2.
+__device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int& mb, int& nb) {
+  constexpr int G = 16;  // M tiles per group: concurrent CTAs cover a compact block of C
+  const int group_size = G * tiles_n;
+  const int group = t / group_size;
+  const int first_m = group * G;
+  const int gm = min(tiles_m - first_m, G);
+  const int r = t - group * group_size;
+  mb = first_m + r % gm;
+  nb = r / gm;
+}
+
 void tc_tile_choice(int64_t M, int64_t N, int num_sms, int* bm, int* bn);
 // K tiles per ring stage of the tile kernel: 2 for 128 x 128 tiles (A then
 // travels as one 3-D TMA box [2][128 rows][128 B] and B as one 32 KiB
@@ -49,6 +63,16 @@ void tc_tile_choice(int64_t M, int64_t N, int num_sms, int* bm, int* bn);
 int tc_kstep(int bm, int bn);
 int tc_gemm_launch(int kind, int bm, int bn, const CUtensorMap& tmA, const CUtensorMap& tmC, TcParams p, int num_sms,
                    cudaStream_t stream);
+// Pairs of CTAs (a 2-CTA cluster, tcgen05 cta_group::2) on 256 x BN tiles,
+// BN = 128 or 256, in place of single-CTA 128 x 128 or 256 x 256 tiles.
+// pair_choice returns the pair tile's BN, or 0 to keep the single-CTA tile.
+// tmA views A as [K tiles][M rows][128 B] with a box of [kPairKstep][128 rows]
+// [128 B]; tmB views packed B as [tiles][128 rows][128 B] with a box of
+// [kPairKstep][BN/2 rows][128 B].
+constexpr int kPairKstep = 2;
+int pair_choice(int64_t M, int bm, int bn);
+int pair_gemm_launch(int kind, int bn, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
+                     TcParams p, int num_sms, cudaStream_t stream);
 int splitk_choice(int64_t M, int64_t N, int64_t ktiles, int num_sms);
 int splitk_gemm_launch(int kind, int split, const CUtensorMap& tmA, const CUtensorMap& tmC, TcParams p,
                        cudaStream_t stream);

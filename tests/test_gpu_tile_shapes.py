@@ -1,13 +1,16 @@
 """Tile shapes reorder the work, not the arithmetic.
 
 The tile kernel can cover C with 256x256, 128x256 or 128x128 tiles.  The
-128x128 shape stages two K tiles per ring slot.  Each output element still
-takes the same K steps, in the same order, into the same fp32 accumulator.
-The epilogue is per element.  So, as the "GEMM Optimization Guide" asks of
-reorder-only changes, every shape must give the same bits.
+128x128 shape stages two K tiles per ring slot.  Where a tile has more than
+128 rows, the 128x128 and 256x256 shapes run as pairs of CTAs on 256x128 and
+256x256 tiles (one tcgen05 MMA over both CTAs' halves); GP_TC_PAIR=0 keeps
+the single-CTA kernel.  Each output element still takes the same K steps,
+in the same order, into the same fp32 accumulator.  The epilogue is per
+element.  So, as the "GEMM Optimization Guide" asks of reorder-only changes,
+every shape must give the same bits.
 
-Each shape runs in its own child process, because the GP_TC_TILE override
-is read once per process.  The same seeded inputs are used each time, and
+Each shape runs in its own child process, because the GP_TC_TILE and
+GP_TC_PAIR overrides are read once per process.  The same seeded inputs are used each time, and
 the outputs are compared bit for bit.  Each output is also checked against
 the oracle.
 """
@@ -24,7 +27,10 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 # (dtype, M, N, K, epilogue): ragged M, K tiles that leave a partial
 # two-tile stage, and N a multiple of 256 so that every shape applies.
 CASES = [("bf16", 300, 512, 1088, "none"), ("e4m3", 200, 768, 2176, "none"), ("fp16", 129, 512, 960, "none"),
-         ("bf16", 257, 512, 1024, "bias_gelu")]
+         ("bf16", 257, 512, 1024, "bias_gelu"),
+         # more 128x128 tiles than SMs: each persistent CTA (or pair) takes
+         # several tiles and reuses both accumulator buffers; 17 K tiles
+         ("bf16", 2000, 4096, 1088, "none")]
 
 CHILD = textwrap.dedent("""
     import sys
@@ -58,8 +64,12 @@ CHILD = textwrap.dedent("""
 def run_shape(tile, path):
     env = dict(os.environ)
     env.pop("GP_TC_TILE", None)
+    env.pop("GP_TC_PAIR", None)
     env.pop("GP_SPLITK", None)
-    if tile is not None:
+    if tile is not None and tile.endswith(" single"):  # the single-CTA kernel, pairs off
+        env["GP_TC_TILE"] = tile.split()[0]
+        env["GP_TC_PAIR"] = "0"
+    elif tile is not None:
         env["GP_TC_TILE"] = tile
     code = CHILD.format(root=ROOT, cases=CASES, path=path)
     r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=600)
@@ -76,7 +86,7 @@ def test_tile_shapes_are_bit_identical(tmp_path):
     from dense_gemm_preshuffle_gb300 import build, inputs
     build.build()
     results = {tile: run_shape(tile, str(tmp_path / f"{tile}.npz"))
-               for tile in (None, "256x256", "128x256", "128x128")}
+               for tile in (None, "256x256", "128x256", "128x128", "256x256 single", "128x128 single")}
     base = results[None]
     for i, (dtype, M, N, K, epi) in enumerate(CASES):
         key = "c%d" % i
