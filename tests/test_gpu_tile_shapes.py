@@ -2,9 +2,9 @@
 
 The tile kernel can cover C with 256x256, 128x256 or 128x128 tiles.  The
 128x128 shape stages two K tiles per ring slot.  Where a tile has more than
-128 rows, the 128x128 and 256x256 shapes run as pairs of CTAs on 256x128 and
-256x256 tiles (one tcgen05 MMA over both CTAs' halves); GP_TC_PAIR=0 keeps
-the single-CTA kernel.  Each output element still takes the same K steps,
+128 rows, the 256x256 shape runs as pairs of CTAs (one tcgen05 MMA over both
+CTAs' halves), and so does the 128x128 shape, on 256x128 tiles, with
+GP_TC_PAIR=1; GP_TC_PAIR=0 keeps the single-CTA kernel.  Each output element still takes the same K steps,
 in the same order, into the same fp32 accumulator.  The epilogue is per
 element.  So, as the "GEMM Optimization Guide" asks of reorder-only changes,
 every shape must give the same bits.
@@ -69,6 +69,9 @@ def run_shape(tile, path):
     if tile is not None and tile.endswith(" single"):  # the single-CTA kernel, pairs off
         env["GP_TC_TILE"] = tile.split()[0]
         env["GP_TC_PAIR"] = "0"
+    elif tile is not None and tile.endswith(" pair"):  # 2-CTA pairs for this shape too
+        env["GP_TC_TILE"] = tile.split()[0]
+        env["GP_TC_PAIR"] = "1"
     elif tile is not None:
         env["GP_TC_TILE"] = tile
     code = CHILD.format(root=ROOT, cases=CASES, path=path)
@@ -86,7 +89,7 @@ def test_tile_shapes_are_bit_identical(tmp_path):
     from dense_gemm_preshuffle_gb300 import build, inputs
     build.build()
     results = {tile: run_shape(tile, str(tmp_path / f"{tile}.npz"))
-               for tile in (None, "256x256", "128x256", "128x128", "256x256 single", "128x128 single")}
+               for tile in (None, "256x256", "128x256", "128x128", "256x256 single", "128x128 pair")}
     base = results[None]
     for i, (dtype, M, N, K, epi) in enumerate(CASES):
         key = "c%d" % i
