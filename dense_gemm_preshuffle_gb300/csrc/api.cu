@@ -372,7 +372,34 @@ int gemm_run_ex(const void* A, const void* B_packed, int dtype, int64_t M, int64
     if (N % 256 != 0) return GP_ERR_SHAPE;
     p.Bsf = p.Bp + (size_t)N * (size_t)kb;
     p.sfa = static_cast<const uint8_t*>(scale_a);
-    return mxf4_gemm_launch(tmA, tmC, p, d->num_sms, st);
+    const bool pair = mxf4_pair_choice(M);
+    CUtensorMap tmB = {}, tmSFB = {};
+    if (pair) {
+      // packed B as [tiles][128 rows][128 B]; its scales as [bands][K steps]
+      // [4][256 B] (1 KiB per band and K step, already in the TMEM copy image)
+      const uint64_t bands = (uint64_t)(N / 128), ksteps = (uint64_t)(kb / 128);
+      {
+        cuuint64_t dims[3] = {128, 128, bands * ksteps};
+        cuuint64_t strides[2] = {128, 16384};
+        cuuint32_t box[3] = {128, 128, 1};
+        cuuint32_t estr[3] = {1, 1, 1};
+        if (g_encode(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(B_packed), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+          return GP_ERR_CUDA;
+      }
+      {
+        cuuint64_t dims[4] = {256, 4, ksteps, bands};
+        cuuint64_t strides[3] = {256, 1024, ksteps * 1024};
+        cuuint32_t box[4] = {256, 4, 1, 2};
+        cuuint32_t estr[4] = {1, 1, 1, 1};
+        if (g_encode(&tmSFB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<uint8_t*>(p.Bsf), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+          return GP_ERR_CUDA;
+      }
+    }
+    return mxf4_gemm_launch(pair, tmA, tmB, tmSFB, tmC, p, d->num_sms, st);
   }
   const int kind = dtype == GP_BF16 ? 0 : dtype == GP_E4M3 ? 1 : 2;  // 2: fp16
   if (split > 1) return splitk_gemm_launch(kind, split, tmA, tmC, p, st);

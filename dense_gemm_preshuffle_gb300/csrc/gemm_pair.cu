@@ -380,7 +380,7 @@ int pair_choice(int64_t M, int bm, int bn) {
   // they are taken only with GP_TC_PAIR=1.  GP_TC_PAIR=0 disables pairs.
   static const int mode = [] {
     const char* e = std::getenv("GP_TC_PAIR");
-    return e == nullptr ? -1 : std::atoi(e);
+    return (e == nullptr || *e == '\0') ? -1 : std::atoi(e);
   }();
   if (mode == 0 || M <= 128) return 0;
   if (bm == 256 && bn == 256) return 256;

@@ -76,7 +76,13 @@ int pair_gemm_launch(int kind, int bn, const CUtensorMap& tmA, const CUtensorMap
 int splitk_choice(int64_t M, int64_t N, int64_t ktiles, int num_sms);
 int splitk_gemm_launch(int kind, int split, const CUtensorMap& tmA, const CUtensorMap& tmC, TcParams p,
                        cudaStream_t stream);
-int mxf4_gemm_launch(const CUtensorMap& tmA, const CUtensorMap& tmC, TcParams p, int num_sms, cudaStream_t stream);
+// MXFP4: single-CTA 128 x 256 tiles, or (pair) 2-CTA clusters on 256 x 256
+// tiles.  tmB and tmSFB are used by the pair form only: packed B as
+// [tiles][128 rows][128 B] with a box of one tile, and B's packed scales as
+// [bands][K steps][4][256 B] with a box of one K step of two bands.
+bool mxf4_pair_choice(int64_t M);
+int mxf4_gemm_launch(bool pair, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmSFB,
+                     const CUtensorMap& tmC, TcParams p, int num_sms, cudaStream_t stream);
 int i8_strip_rows(int N, int num_sms);
 int i8_gemm_launch(const CUtensorMap& tmA, const CUtensorMap& tmB, I8Params p, int num_sms, cudaStream_t stream);
 

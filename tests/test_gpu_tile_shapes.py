@@ -4,7 +4,9 @@ The tile kernel can cover C with 256x256, 128x256 or 128x128 tiles.  The
 128x128 shape stages two K tiles per ring slot.  Where a tile has more than
 128 rows, the 256x256 shape runs as pairs of CTAs (one tcgen05 MMA over both
 CTAs' halves), and so does the 128x128 shape, on 256x128 tiles, with
-GP_TC_PAIR=1; GP_TC_PAIR=0 keeps the single-CTA kernel.  Each output element still takes the same K steps,
+GP_TC_PAIR=1; GP_TC_PAIR=0 keeps the single-CTA kernel.  The MXFP4 kernel
+runs 256x256 pairs, or 128x256 single-CTA tiles with GP_TC_PAIR=0 (the
+"... single" runs).  Each output element still takes the same K steps,
 in the same order, into the same fp32 accumulator.  The epilogue is per
 element.  So, as the "GEMM Optimization Guide" asks of reorder-only changes,
 every shape must give the same bits.
@@ -30,7 +32,10 @@ CASES = [("bf16", 300, 512, 1088, "none"), ("e4m3", 200, 768, 2176, "none"), ("f
          ("bf16", 257, 512, 1024, "bias_gelu"),
          # more 128x128 tiles than SMs: each persistent CTA (or pair) takes
          # several tiles and reuses both accumulator buffers; 17 K tiles
-         ("bf16", 2000, 4096, 1088, "none")]
+         ("bf16", 2000, 4096, 1088, "none"),
+         # MXFP4 has one tile shape: 256x256 pairs, or 128x256 single-CTA
+         # tiles with GP_TC_PAIR=0; more tiles than SMs, ragged M
+         ("e2m1", 2500, 4096, 1024, "none"), ("e2m1", 300, 512, 2048, "bias_relu")]
 
 CHILD = textwrap.dedent("""
     import sys
@@ -52,8 +57,12 @@ CHILD = textwrap.dedent("""
         bias = None
         if epi != "none":
             bias = torch.from_numpy(np.linspace(-2.0, 2.0, N, dtype=np.float32)).cuda()
-        Bp = gp.preshuffle_b(B, dtype)
-        C = gp.matmul(A, Bp, dtype, N, K, scale_a=sa, scale_b=sb, epilogue=epi, bias=bias)
+        if dtype == "e2m1":  # B's block scales travel inside the packed B
+            Bp = gp.preshuffle_b(B, dtype, B_scales=sb)
+            C = gp.matmul(A, Bp, dtype, N, K, scale_a=sa, epilogue=epi, bias=bias)
+        else:
+            Bp = gp.preshuffle_b(B, dtype)
+            C = gp.matmul(A, Bp, dtype, N, K, scale_a=sa, scale_b=sb, epilogue=epi, bias=bias)
         torch.cuda.synchronize()
         assert gp.gemm_last_device_status() == 0
         out["c%d" % i] = C.view(torch.int16).cpu().numpy()
