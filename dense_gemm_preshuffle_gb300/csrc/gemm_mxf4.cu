@@ -55,8 +55,10 @@
 //     the barriers of both CTAs.
 //   - The epilogue warps free the accumulator the same way: a fence limited
 //     to shared memory, then a relaxed remote arrive (5305 -> 5483 TFLOP/s).
-//   - Measured at 4096 x 8192 x 8192: about 100 us against 111.6 for the
-//     single-CTA 128 x 256 tiles.
+//   - Eight epilogue warps (two per TMEM lane quarter, 128 columns each)
+//     halve the time the single accumulator is held at each tile's end.
+//   - Measured at 4096 x 8192 x 8192: 5708 TFLOP/s against 4911 for the
+//     single-CTA 128 x 256 tiles on the same GPU.
 #include <cstdlib>
 
 #include "kernels.h"
@@ -67,26 +69,30 @@ namespace gp {
 
 namespace {
 
-constexpr int F4_THREADS = 256;  // producer, MMA, 4 epilogue warps, A-scale warp, scale-copy warp
 constexpr int F4_BN = 256;
 constexpr int F4_SF_LOOKAHEAD = 2;  // stages the A-scale warp keeps in flight
 
 template <bool PAIR>
 struct F4Cfg {
+  // warps: producer, MMA, 4 epilogue warps (2-5), A-scale warp (6),
+  // scale-copy warp (7); the pair form adds 4 epilogue warps (8-11)
+  static constexpr int EPI_WARPS = PAIR ? 8 : 4;
+  static constexpr int THREADS = 32 * (4 + EPI_WARPS);
+  static constexpr int EPI_COLS = F4_BN / (EPI_WARPS / 4);  // accumulator columns per epilogue warp
   static constexpr int STAGES = PAIR ? 5 : 4;
   static constexpr int A_BYTES = 128 * 128;
   static constexpr int B_BYTES = (PAIR ? F4_BN / 2 : F4_BN) * 128;  // this CTA's rows of B
   static constexpr int SFA_BYTES = 1024;          // 2 atoms
   static constexpr int SFB_BYTES = F4_BN * 8;      // (BN/128) bands x 2 atoms: all the tile's columns
   static constexpr int STAGE_TX = A_BYTES + B_BYTES + SFB_BYTES;  // one CTA's copies of a stage
-  static constexpr int EPI_BYTES = 4 * 32 * 128;
+  static constexpr int EPI_BYTES = EPI_WARPS * 32 * 128;
   static constexpr int ACC_COLS = F4_BN;
   static constexpr int SFA_COLS = 8;
   static constexpr int SFB_COLS = 2 * (F4_BN / 32);
   static constexpr int SF_COL0 = ACC_COLS;
   static constexpr int TMEM_COLS = 512;
   static_assert(ACC_COLS + STAGES * (SFA_COLS + SFB_COLS) <= TMEM_COLS, "tensor memory budget");
-  static constexpr int BIAS_BYTES = 4 * F4_BN * 4;  // each epilogue warp's copy of a tile's bias
+  static constexpr int BIAS_BYTES = EPI_WARPS * F4_BN * 4;  // each epilogue warp's copy of a tile's bias
   static constexpr int SMEM =
       STAGES * (A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES) + EPI_BYTES + BIAS_BYTES + 256 + 1024;
   static_assert(SMEM <= 232448, "shared memory budget");
@@ -124,7 +130,7 @@ __device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, uint32
 // [128 B] (box: one tile) and its packed scales as [bands][K steps][4][256 B]
 // (box: one K step of two bands).
 template <bool PAIR>
-__global__ void __launch_bounds__(F4_THREADS, 1)
+__global__ void __launch_bounds__(F4Cfg<PAIR>::THREADS, 1)
     mxf4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmSFB, const __grid_constant__ CUtensorMap tmC, TcParams p) {
   using Cfg = F4Cfg<PAIR>;
@@ -168,7 +174,7 @@ __global__ void __launch_bounds__(F4_THREADS, 1)
       mbar_init(&empty[s], 1);
     }
     mbar_init(accf, 1);
-    mbar_init(acce, PAIR ? 8 : 4);
+    mbar_init(acce, (PAIR ? 2 : 1) * Cfg::EPI_WARPS);
     mbar_init(drain, 1);
     for (int s = 0; s < F4_STAGES; ++s) mbar_init(&sfr[s], 1);
     mbar_init(sfdrain, 1);
@@ -468,11 +474,18 @@ __global__ void __launch_bounds__(F4_THREADS, 1)
       volatile int never = 0;
       wait_bounded(sfdrain, 0, &never, p.status, ST_TIMEOUT_DRAIN, limit);
     }
-  } else if (warp >= 2 && warp <= 5) {
+  } else if ((warp >= 2 && warp <= 5) || warp >= 8) {
     // ------------------------------------------------------------ epilogue
+    // Epilogue warp e reads TMEM lane quarter warp % 4 and the accumulator
+    // columns [col0, col0 + EPI_COLS): all 256 with four warps, one half
+    // each with the pair form's eight, which halves the time the single
+    // accumulator is held at each tile's end.
+    constexpr int CPW = Cfg::EPI_COLS;
+    const int e = warp < 8 ? warp - 2 : warp - 4;
     const int quad = warp & 3;
+    const int col0 = (e / 4) * CPW;
     const bool early_release = p.act == EPI_ACT_NONE || p.act == EPI_ACT_RELU;
-    uint8_t* stg = s_epi + (warp - 2) * 4096;
+    uint8_t* stg = s_epi + e * 4096;
     const uint32_t stg_row = smem_u32(stg) + lane * 128;
     // The accumulator is free once both CTAs' epilogue warps have read it.
     // The reads have completed (tcgen05.wait::ld) and are fenced
@@ -497,7 +510,7 @@ __global__ void __launch_bounds__(F4_THREADS, 1)
       // done (the __syncwarp below orders the overwrite after them).
       const float* bias_t = nullptr;
       if (p.bias != nullptr) {
-        float4* sbuf = reinterpret_cast<float4*>(s_bias + (warp - 2) * F4_BN);
+        float4* sbuf = reinterpret_cast<float4*>(s_bias + e * F4_BN);
         const float4* src = reinterpret_cast<const float4*>(p.bias + nb * F4_BN);
         __syncwarp();
         sbuf[2 * lane] = __ldg(src + 2 * lane);
@@ -510,22 +523,23 @@ __global__ void __launch_bounds__(F4_THREADS, 1)
       const int row0 = mb * tile_rows + (int)rank * 128 + quad * 32;
       const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16);
       if (early_release) {
-        // The whole row of the tile (256 outputs) is read from TMEM and
-        // rounded into 128 packed registers first, and the accumulator is
-        // released: the next tile's MMAs then run while this tile is staged
-        // and stored (the single accumulator otherwise holds them back).
-        uint32_t pk[F4_BN / 2];
+        // The warp's whole share of the row (CPW outputs) is read from TMEM
+        // and rounded into CPW/2 packed registers first, and the
+        // accumulator is released: the next tile's MMAs then run while this
+        // tile is staged and stored (the single accumulator otherwise holds
+        // them back).
+        uint32_t pk[CPW / 2];
 #pragma unroll
-        for (int c = 0; c < F4_BN / 32; ++c) {
+        for (int c = 0; c < CPW / 32; ++c) {
           uint32_t r[32];
-          tmem_ld_32x32b_x32(tbase + (uint32_t)(c * 32), r);
+          tmem_ld_32x32b_x32(tbase + (uint32_t)(col0 + c * 32), r);
           tmem_ld_wait();
           float v[32];
 #pragma unroll
           for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]);
           uint32_t q16[16];
-          epi_row32<true>(v, 1.0f, nullptr, bias_t != nullptr ? bias_t + c * 32 : nullptr, p.act, p.out_f16 != 0,
-                          q16);
+          epi_row32<true>(v, 1.0f, nullptr, bias_t != nullptr ? bias_t + col0 + c * 32 : nullptr, p.act,
+                          p.out_f16 != 0, q16);
 #pragma unroll
           for (int e = 0; e < 16; ++e) pk[c * 16 + e] = q16[e];
         }
@@ -533,8 +547,8 @@ __global__ void __launch_bounds__(F4_THREADS, 1)
         __syncwarp();
         if (lane == 0) release();
 #pragma unroll
-        for (int c = 0; c < F4_BN / 64; ++c) {
-          const int n0 = nb * F4_BN + c * 64;
+        for (int c = 0; c < CPW / 64; ++c) {
+          const int n0 = nb * F4_BN + col0 + c * 64;
           if (lane == 0) bulk_wait_group_read<0>();  // the previous store has read the staging tile
           __syncwarp();
 #pragma unroll
@@ -552,21 +566,21 @@ __global__ void __launch_bounds__(F4_THREADS, 1)
         // SiLU / GELU: computing them for the whole row before the release
         // was slower than storing chunk by chunk and releasing at the end
 #pragma unroll 1
-        for (int c = 0; c < F4_BN / 64; ++c) {
-          const int n0 = nb * F4_BN + c * 64;
+        for (int c = 0; c < CPW / 64; ++c) {
+          const int n0 = nb * F4_BN + col0 + c * 64;
           if (lane == 0) bulk_wait_group_read<0>();
           __syncwarp();
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             uint32_t r[32];
-            tmem_ld_32x32b_x32(tbase + (uint32_t)(c * 64 + h * 32), r);
+            tmem_ld_32x32b_x32(tbase + (uint32_t)(col0 + c * 64 + h * 32), r);
             tmem_ld_wait();
             float v[32];
 #pragma unroll
             for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]);
             uint32_t q16[16];
-            epi_row32<true>(v, 1.0f, nullptr, bias_t != nullptr ? bias_t + c * 64 + h * 32 : nullptr, p.act,
-                            p.out_f16 != 0, q16);
+            epi_row32<true>(v, 1.0f, nullptr, bias_t != nullptr ? bias_t + col0 + c * 64 + h * 32 : nullptr,
+                            p.act, p.out_f16 != 0, q16);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               const int chunk = h * 4 + q;
@@ -621,7 +635,7 @@ static int launch_mxf4(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUt
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(F4_THREADS);
+  cfg.blockDim = dim3(Cfg::THREADS);
   cfg.dynamicSmemBytes = Cfg::SMEM;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
@@ -639,8 +653,8 @@ static int launch_mxf4(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUt
 
 bool mxf4_pair_choice(int64_t M) {
   // 256 x 256 pair tiles where a tile has rows for both CTAs (MXFP4
-  // 4096 x 8192 x 8192: about 100 against 111.6 us); GP_TC_PAIR=0 keeps
-  // the single-CTA 128 x 256 tiles.
+  // 4096 x 8192 x 8192: 5708 against 4911 TFLOP/s); GP_TC_PAIR=0 keeps the
+  // single-CTA 128 x 256 tiles.
   static const bool enabled = [] {
     const char* e = std::getenv("GP_TC_PAIR");
     return !(e != nullptr && e[0] == '0');
