@@ -151,9 +151,11 @@ __global__ void __launch_bounds__(PR_THREADS, 1)
     int mb, nb;
     tile_coords(pair, p.tiles_m, p.tiles_n, mb, nb);
     const int kpre = kstages < STAGES ? kstages : STAGES;
+    const int y = BN == 128 ? (int)rank * 64 : 0;
+    const int band = BN == 128 ? nb : 2 * nb + (int)rank;
     for (int ks = 0; ks < kpre; ++ks) {
       prefetch_l2_tile_3d(&tmA, 0, mb * 256 + (int)rank * 128, ks * KSTEP);
-      prefetch_l2_tile_3d(&tmB, 0, BN == 128 ? (int)rank * 64 : 0, (BN == 128 ? nb : 2 * nb + (int)rank) * p.ktiles + ks * KSTEP);
+      prefetch_l2_tile_3d(&tmB, 0, y, band * p.ktiles + ks * KSTEP);
     }
   }
   // With constant weights the B issuer requests B for the first stages of
