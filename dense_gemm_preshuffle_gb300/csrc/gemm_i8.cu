@@ -400,14 +400,8 @@ static int launch_i8(const CUtensorMap& tmA, const CUtensorMap& tmB, I8Params p,
   constexpr int SMEM = (RING > RED ? RING : RED) + 2 * I8_STAGES * 8 + 16 + 1024;
   static_assert(SMEM * i8_ctas_per_sm(NB8) <= 228 * 1024, "shared memory budget");
   auto kern = i8_gemm_kernel<NB8, W4>;
-  static bool attr_set[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 64 || !attr_set[dev]) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM) != cudaSuccess)
-      return GP_ERR_CUDA;
-    if (dev < 64) attr_set[dev] = true;
-  }
+  static std::atomic<bool> attr_set[64];
+  if (const int rc = smem_attr_once(attr_set, kern, SMEM); rc != GP_OK) return rc;
   p.stages = I8_STAGES;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;

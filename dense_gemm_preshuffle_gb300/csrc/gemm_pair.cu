@@ -347,14 +347,8 @@ static int launch_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUt
                        int grid, cudaStream_t stream) {
   using Cfg = PairCfg<BN, KSTEP, STAGES>;
   auto kern = pair_gemm_kernel<KIND, BN, KSTEP, STAGES>;
-  static bool attr_set[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 64 || !attr_set[dev]) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) != cudaSuccess)
-      return GP_ERR_CUDA;
-    if (dev < 64) attr_set[dev] = true;
-  }
+  static std::atomic<bool> attr_set[64];
+  if (const int rc = smem_attr_once(attr_set, kern, Cfg::SMEM); rc != GP_OK) return rc;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(PR_THREADS);

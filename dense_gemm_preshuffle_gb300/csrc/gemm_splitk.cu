@@ -20,8 +20,19 @@
 //     One cp.async.bulk shared::cta -> shared::cluster copy moves the block
 //     into the owner's ring.  Remote stores from registers measured slower:
 //     st.shared::cluster ~10x, st.async ~1.3x the whole product's time.
-//     The copy completes its bytes on the owner's receive barrier, which
-//     the owner armed with the total it expects.
+//   - Such a copy completes only on an mbarrier of the destination CTA; the
+//     sender has no way to see when it has finished reading its staging
+//     buffer.  So the owner acknowledges every block.  Each (sender, sending
+//     warp, staging buffer) is one stream into the owner with its own
+//     receive barrier (4 KiB per phase, 4 blocks per stream).  At the owner
+//     one lane of the otherwise idle producer warp watches each stream: when
+//     a block has landed it arms the next phase and arrives remotely on the
+//     sender's `sent_free` barrier of that buffer, and after the stream's
+//     last block it arrives on `recv_all`.  A sending warp reuses a staging
+//     buffer only after the acknowledgement of the block it last held, and
+//     waits for both buffers' last acknowledgements before it stages its own
+//     output rows there.  Every lane watches one stream on its own, so no
+//     owner waits on a stream behind another that is itself waiting.
 //   - Owner epilogue: the owner adds its own partial and the SPLIT-1
 //     received ones in a fixed order, so results are deterministic.  It
 //     applies scale_a[m] * scale_b[n] (E4M3), rounds to bf16 and stores
@@ -46,7 +57,10 @@ constexpr int SK_A_BYTES = SK_BM * 128, SK_B_BYTES = SK_BN * 128;
 constexpr int SK_STAGE_BYTES = SK_A_BYTES + SK_B_BYTES;
 constexpr int SK_RING = SK_STAGES * SK_STAGE_BYTES;  // 192 KiB, reused as the receive buffer
 constexpr int SK_EPI = 4 * 2 * 32 * 128;  // two 4 KiB staging buffers per epilogue warp
-constexpr int SK_SMEM = SK_RING + SK_EPI + 256 + 1024;
+constexpr int SK_BAR = 512;               // mbarriers, the TMEM slot and the abort flag
+constexpr int SK_BLOCKS_PER_STREAM = SK_BN / 32 / 2;  // 32-column blocks of a warp's rows per staging buffer
+constexpr int SK_MAX_STREAMS = 16;
+constexpr int SK_SMEM = SK_RING + SK_EPI + SK_BAR + 1024;
 static_assert(SK_SMEM <= 232448, "shared memory budget");
 
 }  // namespace
@@ -57,6 +71,10 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
   constexpr int OWN = SK_BM / SPLIT;           // rows owned per CTA
   constexpr int SLOT_BYTES = OWN * SK_BN * 4;  // one peer's partial of the owned rows
   static_assert((SPLIT - 1) * SLOT_BYTES <= SK_RING, "receive buffer fits in the ring");
+  // Streams into an owner: (peer slot, 32-row block of the owned rows, staging buffer).
+  constexpr int NQ = OWN / 32;
+  constexpr int NSTREAM = (SPLIT - 1) * NQ * 2;
+  static_assert(NSTREAM <= SK_MAX_STREAMS && NSTREAM <= 32, "one watching lane per stream");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* s_a = base;
@@ -67,9 +85,11 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
   uint64_t* empty = full + SK_STAGES;
   uint64_t* accf = empty + SK_STAGES;
   uint64_t* ready = accf + 1;      // peers' rings are free (SPLIT-1 remote arrivals)
-  uint64_t* recv_full = ready + 1; // peers' partials of the owned rows have landed (tx bytes)
-  uint64_t* drain = recv_full + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* drain = ready + 1;
+  uint64_t* recv = drain + 1;      // [stream]: one incoming 4 KiB block per phase (tx bytes)
+  uint64_t* recv_all = recv + SK_MAX_STREAMS;  // every stream's last block has landed
+  uint64_t* sent_free = recv_all + 1;          // [epilogue warp][buffer]: the owner has the block
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sent_free + 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -88,12 +108,15 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
     }
     mbar_init(accf, 1);
     mbar_init(ready, SPLIT - 1);
-    mbar_init(recv_full, 1);
     mbar_init(drain, 1);
+    for (int i = 0; i < NSTREAM; ++i) mbar_init(&recv[i], 1);
+    mbar_init(recv_all, NSTREAM);
+    for (int i = 0; i < 8; ++i) mbar_init(&sent_free[i], 1);
     *abort_flag = 0;
     fence_mbar_init();
-    // the peers' bulk copies will complete (SPLIT-1) x OWN rows x 1 KiB here
-    mbar_arrive_expect_tx(recv_full, (uint32_t)((SPLIT - 1) * SLOT_BYTES));
+    // each stream's first block (its later phases are armed by the lane that
+    // watches it, before the acknowledgement that lets the next block come)
+    for (int i = 0; i < NSTREAM; ++i) mbar_arrive_expect_tx(&recv[i], 32 * 128);
     prefetch_tensormap(&tmA);
     prefetch_tensormap(&tmC);
   }
@@ -165,6 +188,25 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
         }
       }
     }
+    __syncwarp();
+    // ------------------------------------------------------------ acknowledgements
+    // Lane i watches incoming stream i = (peer slot, 32-row block, buffer).
+    if (lane < NSTREAM) {
+      const int b = lane & 1;
+      const int qi = (lane >> 1) % NQ;
+      const int slot = (lane >> 1) / NQ;
+      const int sender = slot < rank ? slot : slot + 1;
+      const int quad = (rank * OWN + qi * 32) % 128 / 32;  // the sending warp's TMEM lane quarter
+      const uint32_t ack = mapa_shared(smem_u32(&sent_free[quad * 2 + b]), (uint32_t)sender);
+      bool ok = true;
+      for (int j = 0; j < SK_BLOCKS_PER_STREAM && ok; ++j) {
+        ok = wait_bounded(&recv[lane], (uint32_t)j & 1, abort_flag, p.status, ST_TIMEOUT_EPILOGUE, limit);
+        if (!ok) break;
+        if (j + 1 < SK_BLOCKS_PER_STREAM) mbar_arrive_expect_tx(&recv[lane], 32 * 128);
+        mbar_arrive_remote(ack);
+      }
+      if (ok) mbar_arrive(recv_all);
+    }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -209,6 +251,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
     // bulk copy into the owner's receive slot [c][row][32 fp32].
     uint8_t* stg = s_epi + (warp - 2) * 8192;
     const uint32_t stg_row = smem_u32(stg) + lane * 128;
+    uint64_t* my_free = &sent_free[quad * 2];
     int nsent = 0;  // blocks sent by this warp; buffer nsent % 2 takes the next one
 #pragma unroll 1
     for (int mh = 0; mh < 2 && ok; ++mh) {
@@ -217,16 +260,21 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
       if (owner == rank) continue;
       const int slot = rank < owner ? rank : rank - 1;  // this CTA's slot at the owner
       const int lr0 = R0 - owner * OWN;
-      const uint32_t rbar = mapa_shared(smem_u32(recv_full), (uint32_t)owner);
       const uint32_t tb = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(mh * SK_BN);
 #pragma unroll 1
-      for (int c = 0; c < SK_BN / 32; ++c) {
+      for (int c = 0; c < SK_BN / 32 && ok; ++c) {
         uint32_t r[32];
         tmem_ld_32x32b_x32(tb + (uint32_t)(c * 32), r);
         tmem_ld_wait();
-        const uint32_t boff = (uint32_t)((nsent & 1) * 4096);
-        if (lane == 0) bulk_wait_group_read<1>();  // the block sent two steps ago has left this buffer
-        __syncwarp();
+        const int b = nsent & 1;
+        const uint32_t boff = (uint32_t)(b * 4096);
+        // the owner has acknowledged the block this buffer held before
+        if (nsent >= 2)
+          ok = wait_cluster_bounded(&my_free[b], (uint32_t)((nsent >> 1) - 1) & 1, abort_flag, p.status,
+                                    ST_TIMEOUT_EPILOGUE, limit);
+        if (!ok) break;
+        const int stream = (slot * NQ + lr0 / 32) * 2 + b;  // at the owner
+        const uint32_t rbar = mapa_shared(smem_u32(&recv[stream]), (uint32_t)owner);
 #pragma unroll
         for (int q = 0; q < 8; ++q)
           st_shared_v4(stg_row + boff + (uint32_t)((q ^ (lane & 7)) << 4), r[4 * q], r[4 * q + 1], r[4 * q + 2],
@@ -241,19 +289,25 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
                   dst),
               "r"(smem_u32(stg) + boff), "r"(rbar)
               : "memory");
-          bulk_commit_group();
         }
         ++nsent;
       }
     }
-    if (lane == 0) bulk_wait_group<0>();  // every outgoing block has fully landed
+    // Both staging buffers are reused below: wait for the acknowledgement of
+    // the last block each of them held.
+    for (int b = 0; b < 2 && ok; ++b) {
+      const int uses = (nsent + 1 - b) / 2;  // blocks this warp sent from buffer b
+      if (uses > 0)
+        ok = wait_cluster_bounded(&my_free[b], (uint32_t)(uses - 1) & 1, abort_flag, p.status, ST_TIMEOUT_EPILOGUE,
+                                  limit);
+    }
     __syncwarp();
     // Owned rows: add the peers' partials, scale, round, store.
 #pragma unroll 1
     for (int mh = 0; mh < 2; ++mh) {
       const int R0 = mh * 128 + quad * 32;  // first tile row of this warp in half mh
       if (R0 / OWN != rank) continue;
-      if (ok) ok = wait_cluster_bounded(recv_full, 0, abort_flag, p.status, ST_TIMEOUT_EPILOGUE, limit);
+      if (ok) ok = wait_bounded(recv_all, 0, abort_flag, p.status, ST_TIMEOUT_EPILOGUE, limit);
       if (!ok) break;
       const int R = R0 + lane;
       const int lr = R - rank * OWN;
@@ -322,14 +376,8 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
 template <int KIND, int SPLIT>
 static int launch_splitk(const CUtensorMap& tmA, const CUtensorMap& tmC, const TcParams& p, cudaStream_t stream) {
   auto kern = splitk_gemm_kernel<KIND, SPLIT>;
-  static bool attr_set[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 64 || !attr_set[dev]) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SK_SMEM) != cudaSuccess)
-      return GP_ERR_CUDA;
-    if (dev < 64) attr_set[dev] = true;
-  }
+  static std::atomic<bool> attr_set[64];
+  if (const int rc = smem_attr_once(attr_set, kern, SK_SMEM); rc != GP_OK) return rc;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.num_tiles * SPLIT);
   cfg.blockDim = dim3(SK_THREADS);

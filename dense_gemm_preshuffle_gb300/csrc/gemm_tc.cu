@@ -364,14 +364,8 @@ static int launch_tc(const CUtensorMap& tmA, const CUtensorMap& tmC, const TcPar
                      cudaStream_t stream) {
   using Cfg = TcCfg<BM, BN, STAGES, KSTEP>;
   auto kern = tc_gemm_kernel<KIND, BM, BN, STAGES, KSTEP>;
-  static bool attr_set[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 64 || !attr_set[dev]) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) != cudaSuccess)
-      return GP_ERR_CUDA;
-    if (dev < 64) attr_set[dev] = true;
-  }
+  static std::atomic<bool> attr_set[64];
+  if (const int rc = smem_attr_once(attr_set, kern, Cfg::SMEM); rc != GP_OK) return rc;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(TC_THREADS);

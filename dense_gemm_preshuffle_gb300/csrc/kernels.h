@@ -1,5 +1,6 @@
 // Internal interface between the C ABI layer (api.cu) and the kernels.
 #pragma once
+#include <atomic>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -7,6 +8,26 @@
 #include "../../include/gemm_preshuffle.h"
 
 namespace gp {
+
+// Raises the dynamic shared-memory limit of `kern` (and, if given, its
+// shared-memory carveout) on the current device the first time its launcher
+// runs there.  `done` is that launcher's own per-device flag array (each
+// launcher is a template instantiation for one kernel).  The flags are
+// atomics because host threads may launch concurrently; two threads that both
+// see a flag clear both set the attribute, which is harmless.
+template <typename Kern>
+inline int smem_attr_once(std::atomic<bool> (&done)[64], Kern kern, int bytes, int carveout = -1) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GP_ERR_CUDA;
+  if (dev >= 0 && dev < 64 && done[dev].load(std::memory_order_acquire)) return GP_OK;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+    return GP_ERR_CUDA;
+  if (carveout >= 0 &&
+      cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, carveout) != cudaSuccess)
+    return GP_ERR_CUDA;
+  if (dev >= 0 && dev < 64) done[dev].store(true, std::memory_order_release);
+  return GP_OK;
+}
 
 struct TcParams {
   const uint8_t* Bp;      // packed B (data region)

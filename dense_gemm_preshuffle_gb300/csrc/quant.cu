@@ -489,17 +489,8 @@ int launch_staged(const XT* X, int64_t M, int64_t K, uint8_t* Q, float* S, int n
                   uint64_t limit_ns, cudaStream_t stream) {
   constexpr int NBUF = QS_NBUF;
   auto kern = quant_e4m3_rows_staged_kernel<XT, NBUF>;
-  static bool attr_set[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return GP_ERR_CUDA;
-  if (dev >= 64 || !attr_set[dev]) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(NBUF * QS_MAX_ROW)) !=
-        cudaSuccess)
-      return GP_ERR_CUDA;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
-      return GP_ERR_CUDA;
-    if (dev < 64) attr_set[dev] = true;
-  }
+  static std::atomic<bool> attr_set[64];
+  if (const int rc = smem_attr_once(attr_set, kern, (int)(NBUF * QS_MAX_ROW), 100); rc != GP_OK) return rc;
   const size_t smem = (size_t)NBUF * (size_t)K * sizeof(XT);
   int per_sm = (int)((228 * 1024) / (smem + 1024 + 256));
   per_sm = per_sm < 1 ? 1 : (per_sm > 8 ? 8 : per_sm);

@@ -47,11 +47,15 @@ Contents:
   The float steps that decide a code are taken in fp32 as the kernel takes
   them: s = fp32(amax / 448) and x / s are IEEE fp32 divisions.
 * The float parity metric max |C - C_ref| / (|C_ref| + 1e-2).
+* ``gemm_dequantized``: the same plain definition for whole products at the
+  workloads' full sizes, dq(A) . dq(B)^T with numpy's fp64 matmul forming
+  the sum (the loops above would stream B once per output row).
 
 Parity pins (tests/test_oracle.py): brute force in exact rational arithmetic,
 identity and permutation operands, library decodes (torch float8/bfloat16),
-the guide's printed worked numbers (tests/golden/), and round trips of the
-pack model.  No function here is "parity unpinned".
+the guide's printed worked numbers (tests/golden/), the byte counts of
+section 8.2 against the sizes of the arrays they count, and round trips of
+the pack model.  No function here is "parity unpinned".
 """
 from __future__ import annotations
 
@@ -259,6 +263,76 @@ def gemm_operands(ops, rows: Optional[np.ndarray] = None, cols: Optional[np.ndar
         return gemm_e4m3_rowcol(a, b, sa, sb)
     if ops.dtype == "e2m1":
         return gemm_mxfp4(a, b, sa, sb, ops.K)
+    raise ValueError(ops.dtype)
+
+
+def expand_block_scales(e: np.ndarray, K: int, blk: int = 32) -> np.ndarray:
+    """UE8M0 block exponents [rows, K/blk] -> per-element scales [rows, K]
+    (fp64): element k takes the scale of block k // blk."""
+    return np.repeat(decode_ue8m0(e), blk, axis=1)[:, :K]
+
+
+def _mx_sum_is_exact(ea: np.ndarray, eb: np.ndarray, K: int) -> bool:
+    """True when every sum over k of dq(A)[m,k] dq(B)[n,k] is exact in fp64.
+
+    E2M1 values are multiples of 1/2 with |v| <= 6, so a product is a multiple
+    of 2^(ea + eb - 254 - 2) with magnitude at most 36 * 2^(ea + eb - 254).
+    Over all (m, n) the exponent sums lie in [lo, hi]; a sum of K products
+    then needs fewer than log2(K * 36) + (hi - lo) + 2 bits, which must stay
+    within fp64's 53."""
+    if ea.size == 0 or eb.size == 0:
+        return True
+    if (ea == 255).any() or (eb == 255).any():
+        return False  # NaN scales
+    lo = int(ea.min()) + int(eb.min())
+    hi = int(ea.max()) + int(eb.max())
+    return np.log2(max(K, 1) * 36.0) + (hi - lo) + 2 < 53
+
+
+def gemm_dequantized(ops, rows: Optional[np.ndarray] = None) -> np.ndarray:
+    """Reference C of a whole large product, from the plain definition
+    C[m,n] = sum_k dq(A)[m,k] dq(B)[n,k] with numpy's fp64 matmul (a library
+    routine) forming the sum over k.  At the full workload sizes the loops of
+    ``gemm_operands`` stream B from memory once per output row and take hours;
+    this takes seconds and reaches the same values:
+
+    * E4M3: the sum of the decoded codes is exact in fp64 in any order (every
+      product is a multiple of 2^-18 and |sum| < K 448^2), then it is scaled
+      by sa[m] and sb[n] exactly as ``gemm_e4m3_rowcol`` does, so the result
+      is bit-identical to it.
+    * MXFP4 ("GEMM Optimization Guide" section 8.2: one UE8M0 scale per 32
+      K-elements of each operand): dq(x)[k] = e2m1(x[k]) * 2^(e[k//32]-127).
+      Summing dq(A) dq(B) over k regroups the block-scaled sum of
+      ``gemm_mxfp4`` term by term; where ``_mx_sum_is_exact`` holds both are
+      the exact value, hence identical.  Otherwise the block loops are used.
+    * BF16 / FP16: the decoded operands summed in fp64; the order differs from
+      the loops, each within K 2^-53 sum |a b|.
+    * INT8 / W4A8: the exact int64 product of ``gemm_operands``.
+    """
+    a, b, sa, sb = ops.a, ops.b, ops.scale_a, ops.scale_b
+    if rows is not None:
+        a = a[rows]
+        sa = None if sa is None else sa[rows]
+    if ops.dtype in ("int8", "w4a8"):
+        return gemm_operands(ops, rows=rows)
+    if ops.dtype == "bf16":
+        return decode_bf16(a) @ decode_bf16(b).T
+    if ops.dtype == "fp16":
+        return decode_fp16(a) @ decode_fp16(b).T
+    if ops.dtype == "e4m3":
+        acc = decode_e4m3(a) @ decode_e4m3(b).T
+        if sa is not None:
+            acc = acc * np.asarray(sa, np.float64)[:, None]
+        if sb is not None:
+            acc = acc * np.asarray(sb, np.float64)[None, :]
+        return acc
+    if ops.dtype == "e2m1":
+        K = ops.K
+        if not _mx_sum_is_exact(sa, sb, K):
+            return gemm_operands(ops, rows=rows)
+        da = decode_e2m1(unpack_e2m1_rows(a, K)) * expand_block_scales(sa, K)
+        db = decode_e2m1(unpack_e2m1_rows(b, K)) * expand_block_scales(sb, K)
+        return da @ db.T
     raise ValueError(ops.dtype)
 
 

@@ -160,6 +160,75 @@ def test_mxfp4_vs_fraction(M, N, K):
             assert Fraction(got[m, n]) == tot  # exact: power-of-two scales, short sums
 
 
+@pytest.mark.parametrize("M,N,K", [(2, 3, 64), (4, 4, 96), (3, 2, 160)])
+def test_dequantized_matmul_vs_fraction(M, N, K):
+    """The full-size path (dq(A) . dq(B)^T through numpy's matmul) against
+    exact rational brute force: bit-exact for E4M3 (before the two scalings)
+    and MXFP4, within K 2^-52 sum|ab| for BF16."""
+    table = load_e2m1_golden()
+    ops = inputs.make_operands("e2m1", M, N, K, seed=17 + K)
+    # non-uniform block exponents, so a wrong block mapping changes the sum
+    rng = np.random.default_rng(K)
+    ops.scale_a = rng.integers(120, 131, size=ops.scale_a.shape).astype(np.uint8)
+    ops.scale_b = rng.integers(120, 131, size=ops.scale_b.shape).astype(np.uint8)
+    ca = oracle.unpack_e2m1_rows(ops.a, K)
+    cb = oracle.unpack_e2m1_rows(ops.b, K)
+    got = oracle.gemm_dequantized(ops)
+    for m in range(M):
+        for n in range(N):
+            tot = sum((Fraction(table[int(ca[m, k])]) * Fraction(table[int(cb[n, k])]) *
+                       Fraction(2) ** (int(ops.scale_a[m, k // 32]) + int(ops.scale_b[n, k // 32]) - 254)
+                       for k in range(K)), Fraction(0))
+            assert Fraction(got[m, n]) == tot
+    ops8 = inputs.make_operands("e4m3", M, N, K, seed=19 + K)
+    vals = torch_e4m3_values()
+    acc = frac_gemm(to_frac(vals[ops8.a]), to_frac(vals[ops8.b]))
+    got8 = oracle.gemm_dequantized(ops8)
+    for m in range(M):
+        for n in range(N):
+            want = float(acc[m][n]) * np.float64(ops8.scale_a[m]) * np.float64(ops8.scale_b[n])
+            assert got8[m, n] == want  # exact sum, then the same two roundings
+    opsb = inputs.make_operands("bf16", M, N, K, seed=23 + K)
+    av = torch.from_numpy(opsb.a.view(np.int16)).view(torch.bfloat16).double().numpy()
+    bv = torch.from_numpy(opsb.b.view(np.int16)).view(torch.bfloat16).double().numpy()
+    exact = frac_gemm(to_frac(av), to_frac(bv))
+    gotb = oracle.gemm_dequantized(opsb)
+    for m in range(M):
+        for n in range(N):
+            bound = sum(abs(Fraction(float(av[m, k])) * Fraction(float(bv[n, k]))) for k in range(K))
+            assert abs(Fraction(gotb[m, n]) - exact[m][n]) <= bound * K * Fraction(1, 2 ** 52)
+
+
+@pytest.mark.parametrize("dtype,M,N,K", [("e4m3", 70, 384, 1024), ("e2m1", 65, 512, 2048)])
+def test_dequantized_matmul_equals_the_loops(dtype, M, N, K):
+    """Where the sums are exact, the matmul path and the plain loops agree bit
+    for bit, on all rows and on a subset."""
+    ops = inputs.make_operands(dtype, M, N, K, seed=29)
+    assert np.array_equal(oracle.gemm_dequantized(ops), oracle.gemm_operands(ops))
+    rows = np.array([0, 3, M - 1])
+    assert np.array_equal(oracle.gemm_dequantized(ops, rows=rows), oracle.gemm_operands(ops, rows=rows))
+
+
+def test_mx_exactness_guard():
+    K = 8192
+    ea = np.full((2, K // 32), 127, np.uint8)
+    assert oracle._mx_sum_is_exact(ea, ea, K)
+    wide = ea.copy()
+    wide[0, 0], wide[1, 1] = 10, 240  # exponent sums spanning ~460 binades
+    assert not oracle._mx_sum_is_exact(wide, ea, K)
+    # with a span the fp64 sum could not hold, the block loops are used instead
+    ops = inputs.make_operands("e2m1", 2, 256, K, seed=3)
+    ops.scale_a = wide
+    assert np.array_equal(oracle.gemm_dequantized(ops), oracle.gemm_operands(ops))
+
+
+def test_planted_block_scale_mapping_is_caught(monkeypatch):
+    # element k takes block (k mod K/32) instead of k // 32
+    _pins_fail(monkeypatch, "expand_block_scales",
+               lambda e, K, blk=32: np.tile(oracle.decode_ue8m0(e), (1, blk))[:, :K],
+               lambda: test_dequantized_matmul_vs_fraction(2, 3, 64))
+
+
 def test_block_scaled_reduces_to_plain_when_scales_are_one():
     rng = np.random.default_rng(3)
     M, N, K = 5, 6, 128
@@ -280,6 +349,44 @@ def test_worked_numbers(row):
     elif how.startswith("trunc:"):
         d = int(how.split(":")[1])
         assert int(got * 10 ** d) / 10 ** d == pytest.approx(printed)
+
+
+@pytest.mark.parametrize("M,N,K", [(16, 7168, 4096), (128, 256, 512), (4096, 8192, 8192), (3, 128, 64)])
+def test_bytes_moved_counts_the_operand_arrays(M, N, K):
+    """Section 8.2's three byte counts against the sizes of the arrays they
+    count, built independently: A and B as stored (int8 one byte per value;
+    int4 and E2M1 two values per byte), a bf16 C [M, N], and the scales
+    (fp32 per row of A and of B; one UE8M0 byte per 32 K-elements of each
+    operand for MXFP4)."""
+    a8 = np.zeros((M, K), np.int8)
+    b8 = np.zeros((N, K), np.int8)
+    b4 = np.zeros((N, K // 2), np.uint8)
+    a_fp4 = np.zeros((M, K // 2), np.uint8)
+    b_fp4 = np.zeros((N, K // 2), np.uint8)
+    c = np.zeros((M, N), np.uint16)
+    row_scales = np.zeros(M + N, np.float32)
+    mx_scales = [np.zeros((M, K // 32), np.uint8), np.zeros((N, K // 32), np.uint8)]
+    assert oracle.bytes_moved(M, N, K, "int8") == a8.nbytes + b8.nbytes + c.nbytes + row_scales.nbytes
+    assert oracle.bytes_moved(M, N, K, "fp8") == a8.nbytes + b8.nbytes + c.nbytes + row_scales.nbytes
+    assert oracle.bytes_moved(M, N, K, "int4") == a8.nbytes + b4.nbytes + c.nbytes + row_scales.nbytes
+    assert oracle.bytes_moved(M, N, K, "mxfp4") == (a_fp4.nbytes + b_fp4.nbytes + c.nbytes +
+                                                    sum(x.nbytes for x in mx_scales))
+
+
+def test_bytes_moved_int4_and_mxfp4_by_hand():
+    """Hand-worked from the section 8.2 counts for M = N = K = 1024 (MB =
+    1e6 B): int4 = 1,048,576 (A) + 524,288 (B) + 2,097,152 (C) + 8,192
+    (scales) = 3,678,208; MXFP4 = 524,288 + 524,288 + 2,097,152 + 65,536
+    (2 x 1024 x 32 scale bytes) = 3,211,264."""
+    assert oracle.bytes_moved(1024, 1024, 1024, "int4") == 3678208
+    assert oracle.bytes_moved(1024, 1024, 1024, "mxfp4") == 3211264
+
+
+def test_planted_mxfp4_scale_bytes_are_caught(monkeypatch):
+    good = oracle.bytes_moved
+    _pins_fail(monkeypatch, "bytes_moved",
+               lambda M, N, K, kind: good(M, N, K, kind) - (M + N) * (K // 32) * (kind == "mxfp4"),
+               lambda: test_bytes_moved_counts_the_operand_arrays(128, 256, 512))
 
 
 def test_tflops_formula():
