@@ -20,9 +20,10 @@ it once per weight, not per product.
 - JSON line keys:
   - "e2e": the same metric through the public call, with pinned host
     buffers.  A and its scales are copied host->device and C device->host
-    every step; successive steps alternate over four streams, so the copies
-    of one step overlap the GEMM of another, and the steps are replayed
-    from a CUDA graph (copies included), as a serving loop would.
+    every step; successive steps alternate over 16 streams (independent
+    requests), so the copies of one step overlap the GEMM of another, and
+    the steps are replayed from CUDA graphs (copies included), as a serving
+    loop would.
   - "roofline": the GEMM kernel against the measured HBM or tensor peak.
   - "cpu_baseline": the oracle, timed on this host's cores on a bounded
     sample.
@@ -36,6 +37,9 @@ it once per weight, not per product.
     back-to-back steps; median, p10 and p90 of the time per step.
   - "independent_stream": the INT8 and W4A8 workloads as runs of calls with
     GP_RUN_INDEPENDENT (each on its own weights and output).
+  - "b_default": the headline workload through plain gemm_run (no flag).
+  - "measured_peaks_extra": FP8 and FP4 library GEMM peaks measured in the
+    run; each tensor roofline adds its fraction of the same-dtype one.
 """
 from __future__ import annotations
 
@@ -87,6 +91,11 @@ def algorithmic_bytes(dtype: str, M: int, N: int, K: int) -> int:
     if dtype == "e2m1":
         return M * K // 2 + N * K // 2 + M * N * 2 + (M + N) * (K // 32)
     raise ValueError(dtype)
+
+
+def workload_config(name: str, M: int, N: int, K: int) -> dict:
+    """The JSON line's `config`, the same keys in both arms."""
+    return {"workload": name, "M": M, "N": N, "K": K}
 
 
 def bound_of(dtype: str, M: int) -> str:
@@ -306,14 +315,26 @@ def time_device(prob: Problem, steps: int, warmup: int, pg, device, graph_len: i
     graph.replay()  # untimed warm replay
     torch.cuda.synchronize(device)
     full, rest = divmod(steps, g_len)
+    tail = None
+    if rest:
+        # the last `rest` steps as a graph of their own (no host gaps)
+        tail = torch.cuda.CUDAGraph()
+        s.wait_stream(stream)
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(tail, stream=s):
+                for i in range(rest):
+                    prob.step(i)
+        stream.wait_stream(s)
+        tail.replay()
+        torch.cuda.synchronize(device)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(pg, device.index if pg is not None else None)
     torch.cuda.synchronize(device)
     e0.record(stream)
     for _ in range(full):
         graph.replay()
-    for i in range(rest):
-        prob.step(i)
+    if tail is not None:
+        tail.replay()
     e1.record(stream)
     torch.cuda.synchronize(device)
     barrier(pg, device.index if pg is not None else None)
@@ -464,16 +485,28 @@ def time_e2e(prob: Problem, steps: int, warmup: int, device, record: Optional[di
     graph.replay()  # untimed warm replay
     torch.cuda.synchronize(device)
     full, rest = divmod(steps, G)
+    tail = None
+    if rest:
+        # the last `rest` steps as a graph of their own, so every timed step
+        # is a replayed step whatever the step count
+        tail = torch.cuda.CUDAGraph()
+        cap.wait_stream(main)
+        with torch.cuda.graph(tail, stream=cap):
+            for st in streams:
+                st.wait_stream(cap)
+            for i in range(rest):
+                one(i)
+            for st in streams:
+                cap.wait_stream(st)
+        main.wait_stream(cap)
+        tail.replay()  # untimed warm replay
+        torch.cuda.synchronize(device)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(main)
     for _ in range(full):
         graph.replay()
-    for st in streams:
-        st.wait_stream(main)
-    for i in range(rest):
-        one(i)
-    for st in streams:
-        main.wait_stream(st)
+    if tail is not None:
+        tail.replay()
     e1.record(main)
     torch.cuda.synchronize(device)
     h2d = ha.numel() * ha.element_size() + (hsa.numel() * hsa.element_size() if hsa is not None else 0)
@@ -504,6 +537,12 @@ def roofline(prob: Problem, sec_per_step: float, peaks: dict, peak_kind: str, tr
         sus = float(peaks["bf16_tflops_sustained"]) * ratio
         out["peak_sustained"] = round(sus, 1)
         out["frac_of_sustained"] = round(achieved / sus, 4)
+    lib = (peaks.get("library") or {}).get(f"{prob.dtype}_tflops")
+    if lib:
+        # beside it, the same-dtype library GEMM measured in this run
+        out["peak_library"] = lib
+        out["frac_of_library"] = round(achieved / lib, 4)
+        out["peak_library_source"] = f"torch._scaled_mm {prob.dtype} 8192^3 burst, this run"
     return out
 
 
@@ -540,6 +579,76 @@ def cpu_baseline(name: str, budget_s: float = 12.0):
     return {"value": flops / total / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
             "sample": f"{reps} x C rows [0,{rows}) of {ops.M} ({rows * ops.N} outputs, K={ops.K}), "
                       f"{total:.1f} s wall"}
+
+
+def library_peaks(device, n: int = 10) -> dict:
+    """Dense tensor peaks of the FP8 and FP4 types measured in this run, the
+    way the bf16 peak of MEASURED_PEAKS.json is measured: a library GEMM
+    (torch._scaled_mm, i.e. cuBLASLt) at 8192^3, best of `n` after warm-up,
+    CUDA events.  MXFP4 (E2M1 with one UE8M0 scale per 32 K-elements, the
+    workload's format) and NVFP4 (E2M1 with one E4M3 scale per 16) are both
+    timed, to show whether the MX form runs at the NVFP4 rate.  A type the
+    installed torch or cuBLASLt does not offer is reported with its error."""
+    import torch
+    M = N = K = 8192
+    flops = 2.0 * M * N * K
+    out = {"how": "torch._scaled_mm (cuBLASLt) 8192^3, best of %d, CUDA events" % n,
+           "torch": torch.__version__}
+
+    def best(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize(device)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t = float("inf")
+        for _ in range(n):
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize(device)
+            t = min(t, e0.elapsed_time(e1) / 1e3)
+        return round(flops / t / 1e12, 1)
+
+    def blocked(rows, cols):  # elements of a scale matrix in the 128 x 4 blocked layout
+        return -(-rows // 128) * 128 * (-(-cols // 4) * 4)
+
+    tries = {}
+    try:
+        a = torch.randn(M, K, device=device).to(torch.float8_e4m3fn)
+        b = torch.randn(N, K, device=device).to(torch.float8_e4m3fn)
+        one = torch.ones((), device=device, dtype=torch.float32)
+        tries["e4m3_tensorwise"] = lambda: torch._scaled_mm(a, b.t(), scale_a=one, scale_b=one,
+                                                            out_dtype=torch.bfloat16)
+        sa = torch.ones((M, 1), device=device, dtype=torch.float32)
+        sb = torch.ones((1, N), device=device, dtype=torch.float32)
+        tries["e4m3_rowwise"] = lambda: torch._scaled_mm(a, b.t(), scale_a=sa, scale_b=sb, out_dtype=torch.bfloat16)
+    except Exception as e:
+        out["e4m3_error"] = f"{type(e).__name__}: {e}"[:200]
+    try:
+        f4 = torch.float4_e2m1fn_x2
+        a4 = torch.randint(0, 256, (M, K // 2), dtype=torch.uint8, device=device).view(f4)
+        b4 = torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, device=device).view(f4)
+        mx_a = torch.full((blocked(M, K // 32),), 127, dtype=torch.uint8, device=device).view(torch.float8_e8m0fnu)
+        mx_b = torch.full((blocked(N, K // 32),), 127, dtype=torch.uint8, device=device).view(torch.float8_e8m0fnu)
+        tries["mxfp4"] = lambda: torch._scaled_mm(a4, b4.t(), mx_a, mx_b, out_dtype=torch.bfloat16)
+        nv_a = torch.ones((blocked(M, K // 16),), device=device).to(torch.float8_e4m3fn)
+        nv_b = torch.ones((blocked(N, K // 16),), device=device).to(torch.float8_e4m3fn)
+        tries["nvfp4"] = lambda: torch._scaled_mm(a4, b4.t(), nv_a, nv_b, out_dtype=torch.bfloat16)
+    except Exception as e:
+        out["fp4_error"] = f"{type(e).__name__}: {e}"[:200]
+    for key, fn in tries.items():
+        try:
+            out[key + "_tflops"] = best(fn)
+        except Exception as e:
+            out[key + "_error"] = f"{type(e).__name__}: {e}"[:200]
+    fp8 = [out[k] for k in ("e4m3_tensorwise_tflops", "e4m3_rowwise_tflops") if k in out]
+    if fp8:
+        out["e4m3_tflops"] = max(fp8)
+    if "mxfp4_tflops" in out:
+        out["e2m1_tflops"] = out["mxfp4_tflops"]
+    tries.clear()
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_ours(args):
@@ -582,18 +691,19 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": prob.dtype,
         "data": "synthetic, seeded (workload recipe)",
-        "config": {"workload": prob.name, "M": prob.M, "N": prob.N, "K": prob.K,
-                   "parallelism": f"replicas x{world}",
-                   "l2": f"inputs larger than L2: {prob.copies} rotating packed-B/A copies "
-                         f"({prob.copies * prob.packed_bytes / 1e6:.0f} MB)",
-                   "timing": "CUDA-graph replay of back-to-back gemm_run_ex launches, CUDA events",
-                   "flags": "GP_RUN_DEFAULT" if B_DEFAULT_FLAGS else "GP_RUN_B_CONSTANT (weights packed once)"},
+        "config": workload_config(prob.name, prob.M, prob.N, prob.K),
+        "setup": {"parallelism": f"replicas x{world}",
+                  "l2": f"inputs larger than L2: {prob.copies} rotating packed-B/A copies "
+                        f"({prob.copies * prob.packed_bytes / 1e6:.0f} MB)",
+                  "timing": "CUDA-graph replay of back-to-back gemm_run_ex launches, CUDA events",
+                  "flags": "GP_RUN_DEFAULT" if B_DEFAULT_FLAGS else "GP_RUN_B_CONSTANT (weights packed once)"},
         "gpu_launches": args.steps,
         "e2e": {"value": None if args.no_e2e else round(world * prob.flops * e2e_steps / e2e_sec / 1e12, 3),
                 "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_sec / e2e_steps * 1e3, 5), "steps": e2e_steps,
-                "streams": E2E_STREAMS, "timing": "CUDA-graph replay of H2D copy + gemm_run_ex + D2H copy per step"},
+                "streams": E2E_STREAMS, "timing": "CUDA-graph replay of H2D copy + gemm_run_ex + D2H copy per step",
+                "kind": f"{E2E_STREAMS} concurrent independent requests (throughput, not single-call latency)"},
         "roofline": roofline(prob, per, peaks, peak_kind, traffic_from_profiles(prob.name)),
         "trials": trials,
         "clocks": clock_summary,
@@ -604,6 +714,21 @@ def run_ours(args):
     del prob
     torch.cuda.empty_cache()
     if not args.no_others:
+        # same-dtype tensor peaks (library GEMMs), for the tensor-bound lines below
+        peaks["library"] = library_peaks(device)
+        out["measured_peaks_extra"] = peaks["library"]
+        # the headline workload through plain gemm_run (no scheduling flag)
+        try:
+            pd = Problem(args.workload, device)
+            pd.flags = gp.GP_RUN_DEFAULT
+            sd = max_over_ranks(pg, time_device(pd, args.steps, args.warmup, pg, device), device)
+            out["b_default"] = {"us_per_step": round(sd / args.steps * 1e6, 3),
+                                "roofline": roofline(pd, sd / args.steps, peaks, peak_kind, None),
+                                "steps": args.steps, "flags": "GP_RUN_DEFAULT (plain gemm_run)"}
+            del pd
+            torch.cuda.empty_cache()
+        except Exception as e:
+            out["b_default"] = {"unavailable": f"{type(e).__name__}: {e}"[:200]}
         others = {}
         from dense_gemm_preshuffle_gb300 import inputs
         for name in inputs.ALL_WORKLOADS:
@@ -714,7 +839,7 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": ops.dtype,
         "data": "synthetic, seeded (workload recipe)",
-        "config": {"workload": args.workload, "M": ops.M, "N": ops.N, "K": ops.K},
+        "config": workload_config(args.workload, ops.M, ops.N, ops.K),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": f"each step: {n_out} of the {ops.M * ops.N} outputs of C "
                                    f"(rows [0,{len(rows)}), {'all' if cols is None else len(cols)} columns; K={ops.K})"},

@@ -15,10 +15,12 @@
 //     hold a single strip: they warm L2 with their weights and, for constant
 //     weights (GP_RUN_B_CONSTANT), fill their ring with B before the wait on
 //     this kernel.
-//   - One producer warp: lane 0 issues the B copies and lane 1 the A copies
-//     (each thread's bulk copies complete one after another, so the two
-//     operands travel in parallel).  Stages of 8 K tiles (up to 48 KiB) go
-//     into a ring of 2, with full/empty mbarriers.
+//   - One producer warp.  Each thread's bulk copies complete one after
+//     another, so every copy of a stage has its own lane: INT8 B as one
+//     plain bulk copy per 8-row unit (the unit's 8 K tiles are adjacent in
+//     the packed layout), W4A8 B as one TMA box, and A from the next lane.
+//     Stages of 8 K tiles (up to 48 KiB) go into a ring of 2, with
+//     full/empty mbarriers.
 //   - Eight consumer warps; warp w computes K tile w of every stage.  sm_103a
 //     has no tcgen05 integer MMA and its int8 tensor and dp4a rates (~150
 //     TOPS measured) cannot keep pace with the weight stream, so the
@@ -47,6 +49,7 @@
 //     stored as coalesced int32 rows of C.
 #include <cstdlib>
 
+#include "i8_math.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -60,40 +63,6 @@ constexpr int I8_STAGES = 2;
 // Two CTAs share an SM for strips of up to 32 rows (three for 16 rows).
 constexpr int I8_CTAS_PER_SM = 2;
 __host__ __device__ constexpr int i8_ctas_per_sm(int nb8) { return nb8 <= 2 ? 3 : (nb8 <= 4 ? 2 : 1); }
-
-// Offset-binary bytes u -> fp16 subnormals u * 2^-24 (bit pattern 0x00uu):
-// lo holds bytes 0 and 1, hi bytes 2 and 3.
-__device__ __forceinline__ void u8x4_to_f16x2_sub(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(lo) : "r"(w), "r"(0u));
-  asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(hi) : "r"(w), "r"(0u));
-}
-
-// x = f * 2^24 is an integer with |x| < 2^22: x + 1.5 * 2^23 lies in
-// [2^23, 2^24), where the fp32 ulp is 1, so the FMA is exact and the low
-// bits of the result are x + 0x400000.
-__device__ __forceinline__ int scaled_to_int(float f) {
-  return (int)(__float_as_uint(__fmaf_rn(f, 16777216.0f, 12582912.0f)) - 0x4B400000u);
-}
-
-__device__ __forceinline__ void i8x4_to_f16x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  const uint32_t u = w ^ 0x80808080u;  // each byte b -> b + 128 in [0, 255]
-  uint32_t l, h;
-  // fp16 0x64XX is exactly 1024 + XX
-  asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(l) : "r"(u), "r"(0x64646464u));
-  asm("prmt.b32 %0, %1, %2, 0x7362;" : "=r"(h) : "r"(u), "r"(0x64646464u));
-  // subtract 1024 + 128 (fp16 0x6480): exact, the results are integers in [-128, 127]
-  asm("sub.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(l), "r"(0x64806480u));
-  asm("sub.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(h), "r"(0x64806480u));
-}
-
-// Pure function of its register operands (no side effects), so ptxas may
-// interleave independent accumulator chains freely.
-__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                          uint32_t b0, uint32_t b1) {
-  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
 
 // NB8: eight-row units per strip.  W4: B is W4A8's int4 (a packed 128-byte
 // B tile then spans two 128-element K tiles of A).
@@ -133,9 +102,16 @@ __global__ void __launch_bounds__(I8_THREADS, i8_ctas_per_sm(NB8))
     }
   }
 
+  // B issuers: INT8 B travels as one plain bulk copy per 8-row unit (its K
+  // tiles are adjacent in the packed layout), each issued by the unit's own
+  // producer lane, since one thread's bulk copies complete one after
+  // another; W4A8's B (half the bytes) as one 4-D TMA box.  The A issuer is
+  // the next lane.
+  constexpr int B_ISSUERS = W4 ? 1 : NB8;
+  static_assert(B_ISSUERS + 1 <= 32, "one producer lane per copy");
   if (threadIdx.x == 0) {
     for (int s = 0; s < I8_STAGES; ++s) {
-      mbar_init(&full[s], 2);  // the B and the A issuer
+      mbar_init(&full[s], B_ISSUERS + 1);  // the B issuers and the A issuer
       mbar_init(&empty[s], I8_CW);
     }
     *abort_flag = 0;
@@ -143,9 +119,24 @@ __global__ void __launch_bounds__(I8_THREADS, i8_ctas_per_sm(NB8))
     prefetch_tensormap(&tmA);
     prefetch_tensormap(&tmB);
   }
-  // B: NB8 units x BT packed tiles of 8 rows; units past N read as zeros
-  auto load_b = [&](int q) {
+  // B for stage q from issuer lane `bl`.  INT8: unit u0 + bl, its K tiles
+  // [8q, 8q + 8) (fewer at the end of K), one contiguous run; a unit past N
+  // or K tiles past the end are not read, and the consumers never use their
+  // bytes.  W4A8: NB8 units x BT packed tiles of 8 rows in one TMA box, units
+  // past N read as zeros.
+  auto load_b = [&](int q, int bl) {
     const int s = q % I8_STAGES;
+    if constexpr (!W4) {
+      const int u = u0 + bl;
+      const int kt0 = q * I8_KT;
+      const int nkt = min(I8_KT, p.ktiles - kt0);
+      const uint32_t bytes = (u < units && nkt > 0) ? (uint32_t)nkt * 1024u : 0u;
+      mbar_arrive_expect_tx(&full[s], bytes);
+      if (bytes != 0)
+        bulk_load(base + s * STAGE + A_BYTES + bl * (I8_KT * 8 * 128), p.Bp + ((size_t)u * p.ktiles + kt0) * 1024,
+                  bytes, &full[s]);
+      return;
+    }
     mbar_arrive_expect_tx(&full[s], B_BYTES);
     asm volatile(
         "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];" ::
@@ -192,14 +183,14 @@ __global__ void __launch_bounds__(I8_THREADS, i8_ctas_per_sm(NB8))
   // stage debug_skip_load - 1, so the consumers' waits on that stage must
   // time out. The bound is computed once, off the per-stage path.
   const int b_end = p.debug_skip_load > 0 ? min(nstages, p.debug_skip_load - 1) : nstages;
-  if (threadIdx.x == I8_PRODUCER * 32)
-    for (int q = 0; q < min(early, b_end); ++q) load_b(q);
+  if (warp == I8_PRODUCER && lane < B_ISSUERS)
+    for (int q = 0; q < min(early, b_end); ++q) load_b(q, lane);
   if (!p.independent) pdl_wait();  // A may be produced, and C read, by the previous kernel
 
   if (warp == I8_PRODUCER) {
     // ------------------------------------------------------------ producers
-    if (lane < 2) {
-      const bool is_b = lane == 0;
+    if (lane <= B_ISSUERS) {
+      const bool is_b = lane < B_ISSUERS;
       int q = is_b ? min(early, b_end) : 0;
       const int q_end = is_b ? b_end : nstages;
       bool ok = true;
@@ -211,7 +202,7 @@ __global__ void __launch_bounds__(I8_THREADS, i8_ctas_per_sm(NB8))
           break;
         }
         if (is_b)
-          load_b(q);
+          load_b(q, lane);
         else
           load_a(q);
       }
@@ -279,17 +270,18 @@ __global__ void __launch_bounds__(I8_THREADS, i8_ctas_per_sm(NB8))
             rs_lo = __dp4a((int)aw[j], 0x01010101, rs_lo);
             rs_hi = __dp4a((int)a8w[j], 0x01010101, rs_hi);
           }
+          // Units innermost: consecutive MMAs use different accumulators, so
+          // their latencies overlap.  Units past N (zeros from the TMA box)
+          // are computed too and never stored.
 #pragma unroll
-          for (int nb = 0; nb < NB8; ++nb) {
-            if (nb < nu) {  // uniform: units past N are skipped
-              const uint32_t w2[2] = {h == 0 ? bw[nb].x : bw[nb].z, h == 0 ? bw[nb].y : bw[nb].w};
+          for (int j = 0; j < 4; ++j) {
 #pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                // A word j holds K values 4j..4j+3 of this half: B word j / 2,
-                // nibble pairs (0,1),(2,3) or (4,5),(6,7) as fp16 subnormals
-                const uint32_t w = w2[j >> 1] >> ((j & 1) * 8);
-                mma_16816(f[nb], alo[j], a8lo[j], ahi[j], a8hi[j], w & 0x000F000Fu, (w >> 4) & 0x000F000Fu);
-              }
+            for (int nb = 0; nb < NB8; ++nb) {
+              // A word j holds K values 4j..4j+3 of this half: B word j / 2,
+              // nibble pairs (0,1),(2,3) or (4,5),(6,7) as fp16 subnormals
+              const uint32_t w = (h == 0 ? (j < 2 ? bw[nb].x : bw[nb].y) : (j < 2 ? bw[nb].z : bw[nb].w)) >>
+                                 ((j & 1) * 8);
+              mma_16816(f[nb], alo[j], a8lo[j], ahi[j], a8hi[j], w & 0x000F000Fu, (w >> 4) & 0x000F000Fu);
             }
           }
         }
@@ -320,16 +312,17 @@ __global__ void __launch_bounds__(I8_THREADS, i8_ctas_per_sm(NB8))
             rs_lo = __dp4a((int)aw[j], 0x01010101, rs_lo);
             rs_hi = __dp4a((int)a8w[j], 0x01010101, rs_hi);
           }
+          // Units innermost: consecutive MMAs use different accumulators, so
+          // their latencies overlap.  Units past N (zeros from the TMA box)
+          // are computed too and never stored.
 #pragma unroll
-          for (int nb = 0; nb < NB8; ++nb) {
-            if (nb < nu) {  // uniform: units past N are skipped
-              const uint32_t w[4] = {bw[nb].x, bw[nb].y, bw[nb].z, bw[nb].w};
+          for (int j = 0; j < 4; ++j) {
 #pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                uint32_t blo, bhi;
-                u8x4_to_f16x2_sub(w[j], blo, bhi);
-                mma_16816(f[nb], alo[j], a8lo[j], ahi[j], a8hi[j], blo, bhi);
-              }
+            for (int nb = 0; nb < NB8; ++nb) {
+              const uint32_t w = j == 0 ? bw[nb].x : j == 1 ? bw[nb].y : j == 2 ? bw[nb].z : bw[nb].w;
+              uint32_t blo, bhi;
+              u8x4_to_f16x2_sub(w, blo, bhi);
+              mma_16816(f[nb], alo[j], a8lo[j], ahi[j], a8hi[j], blo, bhi);
             }
           }
         }

@@ -36,6 +36,17 @@
 //     columns, which a single CTA's 256 x 256 tile needs for one buffer.
 //     The kernel checks that both CTAs received the same address; if not, it
 //     does no work and reports GP_ERR_DEVICE_CHECK.
+// Long K (KSPLIT = 2): each tile's K range is split in two halves, the first
+// accumulated in one TMEM buffer and the second in the other, and the
+// epilogue adds the halves in fp32 (round to nearest) before scaling.  The
+// tensor core's own accumulation is coarser than a round-to-nearest fp32 sum:
+// at FP8 8192^3 a single chain over all of K reached 8.8e-3 of the parity
+// metric on outputs near zero, where an fp32 chain stays under 4e-3.  Two
+// chains of half the length, with half the magnitude swing each, cut that
+// error.  Both buffers then belong to one tile, so the next tile's MMAs wait
+// for the epilogue; to keep that short the epilogue reads both halves of its
+// columns, rounds them into registers, frees TMEM, and only then stages and
+// stores.
 // Every wait is bounded, as in the other kernels, and a cluster barrier before
 // the end keeps each CTA's shared and tensor memory alive while its peer may
 // still use them.  The odd CTA cannot wait for its own copies (they complete
@@ -75,11 +86,12 @@ struct PairCfg {
 
 }  // namespace
 
-template <int KIND, int BN, int KSTEP, int STAGES>
+template <int KIND, int BN, int KSTEP, int STAGES, int KSPLIT>
 __global__ void __launch_bounds__(PR_THREADS, 1)
     pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmC, TcParams p) {
   using Cfg = PairCfg<BN, KSTEP, STAGES>;
+  static_assert(KSPLIT == 1 || KSPLIT == 2, "one chain per buffer, or one tile's two halves");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* s_a = base;
@@ -231,28 +243,32 @@ __global__ void __launch_bounds__(PR_THREADS, 1)
       uint32_t ph = 0;
       int local = 0;
       bool ok = true;
+      // KSPLIT = 2: stages [0, kh) go to buffer 0 and [kh, kstages) to buffer 1
+      const int kh = KSPLIT == 2 ? kstages / 2 : kstages;
       for (int t = pair; t < p.num_tiles && ok; t += npairs, ++local) {
-        const int buf = local & 1;
-        const uint32_t use = (uint32_t)(local >> 1);
+        const int buf = KSPLIT == 2 ? 0 : local & 1;
+        const uint32_t use = KSPLIT == 2 ? (uint32_t)local : (uint32_t)(local >> 1);
         if (!wait_cluster_bounded(&acce[buf], (use & 1) ^ 1, abort_flag, p.status, ST_TIMEOUT_MMA, limit)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t d = tmem_base + (uint32_t)(buf * Cfg::ACC_COLS);
         for (int ks = 0; ks < kstages; ++ks) {
           if (!wait_cluster_bounded(&full[s], ph, abort_flag, p.status, ST_TIMEOUT_MMA, limit)) {
             ok = false;
             break;
           }
           tc_fence_after();
+          const bool second = ks >= kh;  // KSPLIT = 2: the second half's chain
+          const uint32_t d = tmem_base + (uint32_t)((second ? 1 : buf) * Cfg::ACC_COLS);
+          const int k0 = second ? kh : 0;  // first stage of this chain
           const uint32_t a0 = smem_u32(s_a + s * Cfg::A_BYTES);
           const uint32_t b0 = smem_u32(s_b + s * Cfg::B_BYTES);
           const int nk = stage_ktiles(ks);
           for (int kk = 0; kk < nk; ++kk) {
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-              const uint32_t acc = (ks | kk | k) != 0 ? 1u : 0u;
+              const uint32_t acc = ((ks - k0) | kk | k) != 0 ? 1u : 0u;
               umma_pair<KIND>(d, smem_desc_sw128(a0 + kk * 16384 + 32 * k),
                               smem_desc_sw128(b0 + kk * (Cfg::B_ROWS * 128) + 32 * k), idesc, acc);
             }
@@ -282,14 +298,63 @@ __global__ void __launch_bounds__(PR_THREADS, 1)
     for (int t = pair; t < p.num_tiles; t += npairs, ++local) {
       int mb, nb;
       tile_coords(t, p.tiles_m, p.tiles_n, mb, nb);
-      const int buf = local & 1;
-      const uint32_t use = (uint32_t)(local >> 1);
+      const int buf = KSPLIT == 2 ? 0 : local & 1;
+      const uint32_t use = KSPLIT == 2 ? (uint32_t)local : (uint32_t)(local >> 1);
       if (!wait_bounded(&accf[buf], use & 1, abort_flag, p.status, ST_TIMEOUT_EPILOGUE, limit)) break;
       tc_fence_after();
       const int row0 = mb * 256 + (int)rank * 128 + quad * 32;
       const int m = row0 + lane;
       const float sa = (p.sa != nullptr && m < p.M) ? __ldg(p.sa + m) : 1.0f;
       const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(buf * Cfg::ACC_COLS);
+      if constexpr (KSPLIT == 2) {
+        // This warp's BN/2 columns (64-column chunks c = chalf, chalf + 2, ...):
+        // both halves' sums, added in fp32, through the epilogue into packed
+        // registers; then TMEM is freed and the rows are staged and stored.
+        constexpr int NC = BN / 128;  // chunks of this warp
+        uint32_t pk[NC][2][16];
+#pragma unroll
+        for (int ci = 0; ci < NC; ++ci) {
+          const int c = chalf + 2 * ci;
+          const int n0 = nb * BN + c * 64;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t r0[32], r1[32];
+            tmem_ld_32x32b_x32(tbase + (uint32_t)(c * 64 + h * 32), r0);
+            tmem_ld_32x32b_x32(tbase + (uint32_t)(Cfg::ACC_COLS + c * 64 + h * 32), r1);
+            tmem_ld_wait();
+            float v[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r0[e]) + __uint_as_float(r1[e]);
+            epi_row32(v, sa, p.sb != nullptr ? p.sb + n0 + h * 32 : nullptr,
+                      p.bias != nullptr ? p.bias + n0 + h * 32 : nullptr, p.act, p.out_f16 != 0, pk[ci][h]);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote(acce_leader);  // both buffers read: the next tile may start
+#pragma unroll
+        for (int ci = 0; ci < NC; ++ci) {
+          const int c = chalf + 2 * ci;
+          const int n0 = nb * BN + c * 64;
+          if (lane == 0) bulk_wait_group_read<0>();  // the previous store from this staging tile has read it
+          __syncwarp();
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int c16 = h * 4 + q;
+              st_shared_v4(stg_row + (uint32_t)(((c16 ^ (lane & 7)) * 16)), pk[ci][h][4 * q], pk[ci][h][4 * q + 1],
+                           pk[ci][h][4 * q + 2], pk[ci][h][4 * q + 3]);
+            }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && row0 < p.M) {
+            tma_store_2d(&tmC, n0, row0, stg);
+            bulk_commit_group();
+          }
+        }
+        continue;
+      }
 #pragma unroll 1
       for (int c = chalf; c < BN / 64; c += 2) {
         const int n0 = nb * BN + c * 64;
@@ -342,11 +407,11 @@ __global__ void __launch_bounds__(PR_THREADS, 1)
 
 // ---------------------------------------------------------------- host side
 
-template <int KIND, int BN, int KSTEP, int STAGES>
+template <int KIND, int BN, int KSTEP, int STAGES, int KSPLIT = 1>
 static int launch_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, const TcParams& p,
                        int grid, cudaStream_t stream) {
   using Cfg = PairCfg<BN, KSTEP, STAGES>;
-  auto kern = pair_gemm_kernel<KIND, BN, KSTEP, STAGES>;
+  auto kern = pair_gemm_kernel<KIND, BN, KSTEP, STAGES, KSPLIT>;
   static std::atomic<bool> attr_set[64];
   if (const int rc = smem_attr_once(attr_set, kern, Cfg::SMEM); rc != GP_OK) return rc;
   cudaLaunchConfig_t cfg = {};
@@ -384,6 +449,19 @@ int pair_choice(int64_t M, int bm, int bn) {
   return 0;
 }
 
+bool pair_ksplit(int ktiles) {
+  // Split each 256 x 256 tile's K range over the two accumulator buffers
+  // from 64 K tiles of 128 bytes on (FP8 K >= 8192, 16-bit K >= 4096): the
+  // tensor core's accumulation error grows with the chain's length.
+  // GP_PAIR_KSPLIT=0 keeps one chain per tile, =1 splits every tile.
+  static const int mode = [] {
+    const char* e = std::getenv("GP_PAIR_KSPLIT");
+    return (e == nullptr || *e == '\0') ? -1 : std::atoi(e);
+  }();
+  if (mode == 0) return false;
+  return mode == 1 ? ktiles >= 2 * kPairKstep : ktiles >= 64;
+}
+
 int pair_gemm_launch(int kind, int bn, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
                      TcParams p, int num_sms, cudaStream_t stream) {
   p.tiles_m = (p.M + 255) / 256;
@@ -399,6 +477,13 @@ int pair_gemm_launch(int kind, int bn, const CUtensorMap& tmA, const CUtensorMap
     }
   }
   if (bn == 256) {
+    if (pair_ksplit(p.ktiles)) {
+      switch (kind) {
+        case 0: return launch_pair<0, 256, kPairKstep, 3, 2>(tmA, tmB, tmC, p, grid, stream);
+        case 1: return launch_pair<1, 256, kPairKstep, 3, 2>(tmA, tmB, tmC, p, grid, stream);
+        default: return launch_pair<2, 256, kPairKstep, 3, 2>(tmA, tmB, tmC, p, grid, stream);
+      }
+    }
     switch (kind) {
       case 0: return launch_pair<0, 256, kPairKstep, 3>(tmA, tmB, tmC, p, grid, stream);
       case 1: return launch_pair<1, 256, kPairKstep, 3>(tmA, tmB, tmC, p, grid, stream);

@@ -92,6 +92,9 @@ int tc_gemm_launch(int kind, int bm, int bn, const CUtensorMap& tmA, const CUten
 // [kPairKstep][BN/2 rows][128 B].
 constexpr int kPairKstep = 2;
 int pair_choice(int64_t M, int bm, int bn);
+// Whether a 256 x 256 pair tile splits its K range over its two accumulator
+// buffers (summed in fp32 by the epilogue) for a product of `ktiles` K tiles.
+bool pair_ksplit(int ktiles);
 int pair_gemm_launch(int kind, int bn, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
                      TcParams p, int num_sms, cudaStream_t stream);
 int splitk_choice(int64_t M, int64_t N, int64_t ktiles, int num_sms);
