@@ -38,8 +38,6 @@ it once per weight, not per product.
   - "independent_stream": the INT8 and W4A8 workloads as runs of calls with
     GP_RUN_INDEPENDENT (each on its own weights and output).
   - "b_default": the headline workload through plain gemm_run (no flag).
-  - "measured_peaks_extra": FP8 and FP4 library GEMM peaks measured in the
-    run; each tensor roofline adds its fraction of the same-dtype one.
 """
 from __future__ import annotations
 
@@ -537,12 +535,6 @@ def roofline(prob: Problem, sec_per_step: float, peaks: dict, peak_kind: str, tr
         sus = float(peaks["bf16_tflops_sustained"]) * ratio
         out["peak_sustained"] = round(sus, 1)
         out["frac_of_sustained"] = round(achieved / sus, 4)
-    lib = (peaks.get("library") or {}).get(f"{prob.dtype}_tflops")
-    if lib:
-        # beside it, the same-dtype library GEMM measured in this run
-        out["peak_library"] = lib
-        out["frac_of_library"] = round(achieved / lib, 4)
-        out["peak_library_source"] = f"torch._scaled_mm {prob.dtype} 8192^3 burst, this run"
     return out
 
 
@@ -579,76 +571,6 @@ def cpu_baseline(name: str, budget_s: float = 12.0):
     return {"value": flops / total / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
             "sample": f"{reps} x C rows [0,{rows}) of {ops.M} ({rows * ops.N} outputs, K={ops.K}), "
                       f"{total:.1f} s wall"}
-
-
-def library_peaks(device, n: int = 10) -> dict:
-    """Dense tensor peaks of the FP8 and FP4 types measured in this run, the
-    way the bf16 peak of MEASURED_PEAKS.json is measured: a library GEMM
-    (torch._scaled_mm, i.e. cuBLASLt) at 8192^3, best of `n` after warm-up,
-    CUDA events.  MXFP4 (E2M1 with one UE8M0 scale per 32 K-elements, the
-    workload's format) and NVFP4 (E2M1 with one E4M3 scale per 16) are both
-    timed, to show whether the MX form runs at the NVFP4 rate.  A type the
-    installed torch or cuBLASLt does not offer is reported with its error."""
-    import torch
-    M = N = K = 8192
-    flops = 2.0 * M * N * K
-    out = {"how": "torch._scaled_mm (cuBLASLt) 8192^3, best of %d, CUDA events" % n,
-           "torch": torch.__version__}
-
-    def best(fn):
-        for _ in range(3):
-            fn()
-        torch.cuda.synchronize(device)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        t = float("inf")
-        for _ in range(n):
-            e0.record()
-            fn()
-            e1.record()
-            torch.cuda.synchronize(device)
-            t = min(t, e0.elapsed_time(e1) / 1e3)
-        return round(flops / t / 1e12, 1)
-
-    def blocked(rows, cols):  # elements of a scale matrix in the 128 x 4 blocked layout
-        return -(-rows // 128) * 128 * (-(-cols // 4) * 4)
-
-    tries = {}
-    try:
-        a = torch.randn(M, K, device=device).to(torch.float8_e4m3fn)
-        b = torch.randn(N, K, device=device).to(torch.float8_e4m3fn)
-        one = torch.ones((), device=device, dtype=torch.float32)
-        tries["e4m3_tensorwise"] = lambda: torch._scaled_mm(a, b.t(), scale_a=one, scale_b=one,
-                                                            out_dtype=torch.bfloat16)
-        sa = torch.ones((M, 1), device=device, dtype=torch.float32)
-        sb = torch.ones((1, N), device=device, dtype=torch.float32)
-        tries["e4m3_rowwise"] = lambda: torch._scaled_mm(a, b.t(), scale_a=sa, scale_b=sb, out_dtype=torch.bfloat16)
-    except Exception as e:
-        out["e4m3_error"] = f"{type(e).__name__}: {e}"[:200]
-    try:
-        f4 = torch.float4_e2m1fn_x2
-        a4 = torch.randint(0, 256, (M, K // 2), dtype=torch.uint8, device=device).view(f4)
-        b4 = torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, device=device).view(f4)
-        mx_a = torch.full((blocked(M, K // 32),), 127, dtype=torch.uint8, device=device).view(torch.float8_e8m0fnu)
-        mx_b = torch.full((blocked(N, K // 32),), 127, dtype=torch.uint8, device=device).view(torch.float8_e8m0fnu)
-        tries["mxfp4"] = lambda: torch._scaled_mm(a4, b4.t(), mx_a, mx_b, out_dtype=torch.bfloat16)
-        nv_a = torch.ones((blocked(M, K // 16),), device=device).to(torch.float8_e4m3fn)
-        nv_b = torch.ones((blocked(N, K // 16),), device=device).to(torch.float8_e4m3fn)
-        tries["nvfp4"] = lambda: torch._scaled_mm(a4, b4.t(), nv_a, nv_b, out_dtype=torch.bfloat16)
-    except Exception as e:
-        out["fp4_error"] = f"{type(e).__name__}: {e}"[:200]
-    for key, fn in tries.items():
-        try:
-            out[key + "_tflops"] = best(fn)
-        except Exception as e:
-            out[key + "_error"] = f"{type(e).__name__}: {e}"[:200]
-    fp8 = [out[k] for k in ("e4m3_tensorwise_tflops", "e4m3_rowwise_tflops") if k in out]
-    if fp8:
-        out["e4m3_tflops"] = max(fp8)
-    if "mxfp4_tflops" in out:
-        out["e2m1_tflops"] = out["mxfp4_tflops"]
-    tries.clear()
-    torch.cuda.empty_cache()
-    return out
 
 
 def run_ours(args):
@@ -714,9 +636,6 @@ def run_ours(args):
     del prob
     torch.cuda.empty_cache()
     if not args.no_others:
-        # same-dtype tensor peaks (library GEMMs), for the tensor-bound lines below
-        peaks["library"] = library_peaks(device)
-        out["measured_peaks_extra"] = peaks["library"]
         # the headline workload through plain gemm_run (no scheduling flag)
         try:
             pd = Problem(args.workload, device)
