@@ -14,7 +14,8 @@ it once per weight, not per product.
 - Timing: W warm-up steps, then exactly K steps, replayed from a CUDA graph
   of back-to-back gemm_run launches (no host gaps).  The K steps sit between
   a barrier and torch.cuda.synchronize() on both sides and are timed with
-  CUDA events on the launch stream.
+  CUDA events on the launch stream; a short device spin queued ahead of the
+  start event keeps the host's graph submission out of the device time.
 - Reported value: the maximum over ranks.  Under torchrun every rank runs the
   same independent problem on its own GPU (weak scaling, no collective).
 - JSON line keys:
@@ -64,6 +65,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # nominal dense tensor-rate ratios to bf16 (2.25 PF): fp8 4.5, fp4 13.5
 DTYPE_RATIO = {"bf16": 1.0, "fp16": 1.0, "e4m3": 2.0, "e2m1": 6.0}
 B_DEFAULT_FLAGS = False  # --b-default: time gemm_run without GP_RUN_B_CONSTANT
+HOST_COVER_CYCLES = 200_000  # ~0.1 ms of device spin before a timed region (see time_device)
 
 
 def load_peaks():
@@ -328,6 +330,10 @@ def time_device(prob: Problem, steps: int, warmup: int, pg, device, graph_len: i
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(pg, device.index if pg is not None else None)
     torch.cuda.synchronize(device)
+    # A short device spin ahead of the start event: the event is then taken
+    # once the host has submitted the graph, so the host's submission latency
+    # is not counted as device time (it would be ~10 us in a 20-step run).
+    torch.cuda._sleep(HOST_COVER_CYCLES)
     e0.record(stream)
     for _ in range(full):
         graph.replay()
@@ -362,6 +368,7 @@ def time_trials(prob, warmup: int, device, R: int = 80, n: int = 7):
     per = []
     for _ in range(n):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(HOST_COVER_CYCLES)
         e0.record(stream)
         graph.replay()
         e1.record(stream)

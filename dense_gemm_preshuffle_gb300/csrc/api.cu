@@ -124,6 +124,17 @@ uint64_t wait_limit_ns() {
 
 std::atomic<int> g_debug_skip_load{0};
 
+// M tiles per group of the persistent tile order (tile_coords); GP_RASTER_G
+// overrides the default 16, for sweeps.
+int raster_group() {
+  static const int g = [] {
+    const char* e = std::getenv("GP_RASTER_G");
+    const int v = e == nullptr ? 0 : std::atoi(e);
+    return v > 0 ? v : kRasterG;
+  }();
+  return g;
+}
+
 }  // namespace
 }  // namespace gp
 
@@ -358,6 +369,7 @@ int gemm_run_ex(const void* A, const void* B_packed, int dtype, int64_t M, int64
   p.ktiles = (int)(kb / 128);
   p.debug_skip_load = g_debug_skip_load.exchange(0);
   p.b_constant = b_constant;
+  p.raster_g = raster_group();
   p.bias = static_cast<const float*>(bias);
   p.out_f16 = c_dtype == GP_FP16 ? 1 : 0;
   p.act = epilogue == GP_EPI_BIAS_RELU ? EPI_ACT_RELU

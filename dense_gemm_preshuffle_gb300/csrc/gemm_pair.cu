@@ -161,7 +161,7 @@ __global__ void __launch_bounds__(PR_THREADS, 1)
     // Warm L2 with the first K steps of this CTA's first tile while the
     // previous kernel may still run (a prefetch never changes later loads).
     int mb, nb;
-    tile_coords(pair, p.tiles_m, p.tiles_n, mb, nb);
+    tile_coords(pair, p.tiles_m, p.tiles_n, p.raster_g, mb, nb);
     const int kpre = kstages < STAGES ? kstages : STAGES;
     const int y = BN == 128 ? (int)rank * 64 : 0;
     const int band = BN == 128 ? nb : 2 * nb + (int)rank;
@@ -175,7 +175,7 @@ __global__ void __launch_bounds__(PR_THREADS, 1)
   const int early = (!bad && p.b_constant && pair < p.num_tiles) ? min(kstages, STAGES) : 0;
   if (threadIdx.x == 0 && early > 0) {  // warp 0 lane 0, the B issuer
     int mb, nb;
-    tile_coords(pair, p.tiles_m, p.tiles_n, mb, nb);
+    tile_coords(pair, p.tiles_m, p.tiles_n, p.raster_g, mb, nb);
     for (int ks = 0; ks < early; ++ks) {
       if (p.debug_skip_load == 1 + ks) continue;
       if (leader) mbar_arrive_expect_tx(&full[ks], 2 * Cfg::B_BYTES);
@@ -198,7 +198,7 @@ __global__ void __launch_bounds__(PR_THREADS, 1)
       bool ok = true;
       for (int t = pair; t < p.num_tiles && ok; t += npairs) {
         int mb, nb;
-        tile_coords(t, p.tiles_m, p.tiles_n, mb, nb);
+        tile_coords(t, p.tiles_m, p.tiles_n, p.raster_g, mb, nb);
         for (int ks = 0; ks < kstages; ++ks) {
           const bool b_done = is_b && (int)issued < early;
           if (!b_done && !wait_bounded(&empty[s], ph ^ 1, abort_flag, p.status, ST_TIMEOUT_PRODUCER, limit)) {
@@ -297,7 +297,7 @@ __global__ void __launch_bounds__(PR_THREADS, 1)
     int local = 0;
     for (int t = pair; t < p.num_tiles; t += npairs, ++local) {
       int mb, nb;
-      tile_coords(t, p.tiles_m, p.tiles_n, mb, nb);
+      tile_coords(t, p.tiles_m, p.tiles_n, p.raster_g, mb, nb);
       const int buf = KSPLIT == 2 ? 0 : local & 1;
       const uint32_t use = KSPLIT == 2 ? (uint32_t)local : (uint32_t)(local >> 1);
       if (!wait_bounded(&accf[buf], use & 1, abort_flag, p.status, ST_TIMEOUT_EPILOGUE, limit)) break;

@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     // Warm L2 with the first K steps of this CTA's first tile while the
     // previous kernel may still run (a prefetch never changes later loads).
     int mb, nb;
-    tile_coords(blockIdx.x, p.tiles_m, p.tiles_n, mb, nb);
+    tile_coords(blockIdx.x, p.tiles_m, p.tiles_n, p.raster_g, mb, nb);
     const int kpre = kstages < STAGES ? kstages : STAGES;
     for (int ks = 0; ks < kpre; ++ks) {
       if constexpr (KSTEP == 1)
@@ -148,7 +148,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   const int early = (p.b_constant && (int)blockIdx.x < p.num_tiles) ? min(kstages, STAGES) : 0;
   if (threadIdx.x == 0 && early > 0) {  // the producer thread, which initialised the barriers
     int mb, nb;
-    tile_coords(blockIdx.x, p.tiles_m, p.tiles_n, mb, nb);
+    tile_coords(blockIdx.x, p.tiles_m, p.tiles_n, p.raster_g, mb, nb);
     const uint8_t* bsrc = p.Bp + (size_t)nb * (BN / 128) * p.ktiles * 16384;
     const uint64_t pol_b = policy_evict_first();
     for (int ks = 0; ks < early; ++ks) {
@@ -180,7 +180,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       bool ok = true;
       for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
         int mb, nb;
-        tile_coords(t, p.tiles_m, p.tiles_n, mb, nb);
+        tile_coords(t, p.tiles_m, p.tiles_n, p.raster_g, mb, nb);
         const uint8_t* bsrc = p.Bp + (size_t)nb * Cfg::BANDS * p.ktiles * 16384;
         for (int ks = 0; ks < kstages; ++ks) {
           // B's first `early` stages are free and already requested
@@ -297,7 +297,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     int local = 0;
     for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++local) {
       int mb, nb;
-      tile_coords(t, p.tiles_m, p.tiles_n, mb, nb);
+      tile_coords(t, p.tiles_m, p.tiles_n, p.raster_g, mb, nb);
       const int buf = local % NBUF;
       const uint32_t use = (uint32_t)(local / NBUF);
       if (!wait_bounded(&accf[buf], use & 1, abort_flag, p.status, ST_TIMEOUT_EPILOGUE, limit)) break;

@@ -45,6 +45,7 @@ struct TcParams {
   int tiles_m, tiles_n, num_tiles;
   int debug_skip_load;    // 0 = off; i > 0: the producer skips its i-th stage load
   int b_constant;         // 1: B may be read before the previous kernel on the stream completes
+  int raster_g;           // M tiles per group of the tile order (tile_coords)
 };
 
 struct I8Params {
@@ -63,11 +64,11 @@ struct I8Params {
   int mg0;                // first group of 16 rows of A of this launch (grids hold <= 65535 groups)
 };
 
-// Output tile t of a tiles_m x tiles_n grid, walked in groups of 16 M tiles
-// so that concurrently running CTAs cover a compact block of C and share A
-// rows and B columns in L2.
-__device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int& mb, int& nb) {
-  constexpr int G = 16;  // M tiles per group: concurrent CTAs cover a compact block of C
+// Output tile t of a tiles_m x tiles_n grid, walked in groups of G M tiles
+// (16 unless GP_RASTER_G sets it) so that concurrently running CTAs cover a
+// compact block of C and share A rows and B columns in L2.
+constexpr int kRasterG = 16;
+__device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int G, int& mb, int& nb) {
   const int group_size = G * tiles_n;
   const int group = t / group_size;
   const int first_m = group * G;
