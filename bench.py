@@ -507,6 +507,10 @@ def time_e2e(prob: Problem, steps: int, warmup: int, device, record: Optional[di
         tail.replay()  # untimed warm replay
         torch.cuda.synchronize(device)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # as in time_device: the graphs are submitted while the device spins,
+    # so the host's submission latency is not part of the measured time (a
+    # serving loop submits its next graph while the previous one runs)
+    torch.cuda._sleep(HOST_COVER_CYCLES)
     e0.record(main)
     for _ in range(full):
         graph.replay()
