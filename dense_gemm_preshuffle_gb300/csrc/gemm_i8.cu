@@ -418,7 +418,8 @@ int i8_strip_rows(int N, int num_sms) {
   // 16 x 7168 x 4096).  Wider problems take one strip per SM, at most 64
   // rows.  GP_I8_STRIP (16, 32, 48 or 64) overrides.
   static const int strip_override = env_int("GP_I8_STRIP", 0);
-  if (strip_override == 16 || strip_override == 32 || strip_override == 48 || strip_override == 64)
+  if (strip_override == 16 || strip_override == 24 || strip_override == 32 || strip_override == 48 ||
+      strip_override == 64)
     return strip_override;
   const int two_per_sm = 16 * ((N + 16 * I8_CTAS_PER_SM * num_sms - 1) / (16 * I8_CTAS_PER_SM * num_sms));
   if (two_per_sm <= 32) return two_per_sm;
@@ -452,6 +453,7 @@ static int i8_gemm_launch_groups(const CUtensorMap& tmA, const CUtensorMap& tmB,
   if (p.w4) {
     switch (strip) {
       case 16: return launch_i8<2, true>(tmA, tmB, p, grid, stream);
+      case 24: return launch_i8<3, true>(tmA, tmB, p, grid, stream);
       case 32: return launch_i8<4, true>(tmA, tmB, p, grid, stream);
       case 48: return launch_i8<6, true>(tmA, tmB, p, grid, stream);
       default: return launch_i8<8, true>(tmA, tmB, p, grid, stream);
@@ -459,6 +461,7 @@ static int i8_gemm_launch_groups(const CUtensorMap& tmA, const CUtensorMap& tmB,
   }
   switch (strip) {
     case 16: return launch_i8<2, false>(tmA, tmB, p, grid, stream);
+    case 24: return launch_i8<3, false>(tmA, tmB, p, grid, stream);
     case 32: return launch_i8<4, false>(tmA, tmB, p, grid, stream);
     case 48: return launch_i8<6, false>(tmA, tmB, p, grid, stream);
     default: return launch_i8<8, false>(tmA, tmB, p, grid, stream);
