@@ -43,10 +43,10 @@
 // at FP8 8192^3 a single chain over all of K reached 8.8e-3 of the parity
 // metric on outputs near zero, where an fp32 chain stays under 4e-3.  Two
 // chains of half the length, with half the magnitude swing each, cut that
-// error.  Both buffers then belong to one tile, so the next tile's MMAs wait
-// for the epilogue; to keep that short the epilogue reads both halves of its
-// columns, rounds them into registers, frees TMEM, and only then stages and
-// stores.
+// error.  Each buffer then holds one half of every tile: the first half is
+// signalled at mid-tile and the epilogue reads it into registers at once,
+// freeing buffer 0 for the next tile's first half; buffer 1 is read, and
+// freed, at the tile's end, half a tile before the next tile needs it.
 // Every wait is bounded, as in the other kernels, and a cluster barrier before
 // the end keeps each CTA's shared and tensor memory alive while its peer may
 // still use them.  The odd CTA cannot wait for its own copies (they complete
@@ -254,6 +254,16 @@ __global__ void __launch_bounds__(PR_THREADS, 1)
         }
         tc_fence_after();
         for (int ks = 0; ks < kstages; ++ks) {
+          if (KSPLIT == 2 && ks == kh) {
+            // the first half is issued: signal it, then take buffer 1 once
+            // the epilogue has read the previous tile's second half
+            umma_commit_pair(&accf[0], 0x3);
+            if (!wait_cluster_bounded(&acce[1], (use & 1) ^ 1, abort_flag, p.status, ST_TIMEOUT_MMA, limit)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+          }
           if (!wait_cluster_bounded(&full[s], ph, abort_flag, p.status, ST_TIMEOUT_MMA, limit)) {
             ok = false;
             break;
@@ -280,7 +290,7 @@ __global__ void __launch_bounds__(PR_THREADS, 1)
           }
         }
         if (!ok) break;
-        umma_commit_pair(&accf[buf], 0x3);
+        umma_commit_pair(&accf[KSPLIT == 2 ? 1 : buf], 0x3);
       }
       // Every issued MMA must complete before either CTA releases TMEM.
       umma_commit_pair(drain, 0x1);
@@ -307,31 +317,32 @@ __global__ void __launch_bounds__(PR_THREADS, 1)
       const float sa = (p.sa != nullptr && m < p.M) ? __ldg(p.sa + m) : 1.0f;
       const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(buf * Cfg::ACC_COLS);
       if constexpr (KSPLIT == 2) {
-        // This warp's BN/2 columns (64-column chunks c = chalf, chalf + 2, ...):
-        // both halves' sums, added in fp32, through the epilogue into packed
-        // registers; then TMEM is freed and the rows are staged and stored.
+        // This warp's BN/2 columns (64-column chunks c = chalf, chalf + 2,
+        // ...).  The first half's sums (buffer 0) are complete at mid-tile:
+        // they are read into registers then and buffer 0 is freed, so the
+        // next tile's first half never waits.  At the tile's end the second
+        // half's sums (buffer 1) are added in fp32, 16 columns at a time,
+        // rounded and staged; buffer 1 is freed after its last read, half a
+        // tile before the next tile needs it.
         constexpr int NC = BN / 128;  // chunks of this warp
-        uint32_t pk[NC][2][16];
+        float held[NC][64];
 #pragma unroll
         for (int ci = 0; ci < NC; ++ci) {
           const int c = chalf + 2 * ci;
-          const int n0 = nb * BN + c * 64;
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            uint32_t r0[32], r1[32];
-            tmem_ld_32x32b_x32(tbase + (uint32_t)(c * 64 + h * 32), r0);
-            tmem_ld_32x32b_x32(tbase + (uint32_t)(Cfg::ACC_COLS + c * 64 + h * 32), r1);
+          for (int pc = 0; pc < 4; ++pc) {
+            uint32_t r[16];
+            tmem_ld_32x32b_x16(tbase + (uint32_t)(c * 64 + pc * 16), r);
             tmem_ld_wait();
-            float v[32];
 #pragma unroll
-            for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r0[e]) + __uint_as_float(r1[e]);
-            epi_row32(v, sa, p.sb != nullptr ? p.sb + n0 + h * 32 : nullptr,
-                      p.bias != nullptr ? p.bias + n0 + h * 32 : nullptr, p.act, p.out_f16 != 0, pk[ci][h]);
+            for (int e = 0; e < 16; ++e) held[ci][pc * 16 + e] = __uint_as_float(r[e]);
           }
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive_remote(acce_leader);  // both buffers read: the next tile may start
+        if (lane == 0) mbar_arrive_remote(acce_leader);  // buffer 0 read: the next tile may start
+        if (!wait_bounded(&accf[1], use & 1, abort_flag, p.status, ST_TIMEOUT_EPILOGUE, limit)) break;
+        tc_fence_after();
 #pragma unroll
         for (int ci = 0; ci < NC; ++ci) {
           const int c = chalf + 2 * ci;
@@ -339,13 +350,32 @@ __global__ void __launch_bounds__(PR_THREADS, 1)
           if (lane == 0) bulk_wait_group_read<0>();  // the previous store from this staging tile has read it
           __syncwarp();
 #pragma unroll
-          for (int h = 0; h < 2; ++h)
+          for (int h = 0; h < 2; ++h) {
+#pragma unroll
+            for (int pc = 0; pc < 2; ++pc) {
+              uint32_t r[16];
+              tmem_ld_32x32b_x16(tbase + (uint32_t)(Cfg::ACC_COLS + c * 64 + h * 32 + pc * 16), r);
+              tmem_ld_wait();
+#pragma unroll
+              for (int e = 0; e < 16; ++e) held[ci][h * 32 + pc * 16 + e] += __uint_as_float(r[e]);
+            }
+            if (ci == NC - 1 && h == 1) {
+              // this warp's last reads of buffer 1
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive_remote(acce_leader + 8u);
+            }
+            uint32_t pk[16];
+            epi_row32(*reinterpret_cast<float(*)[32]>(&held[ci][h * 32]), sa,
+                      p.sb != nullptr ? p.sb + n0 + h * 32 : nullptr,
+                      p.bias != nullptr ? p.bias + n0 + h * 32 : nullptr, p.act, p.out_f16 != 0, pk);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               const int c16 = h * 4 + q;
-              st_shared_v4(stg_row + (uint32_t)(((c16 ^ (lane & 7)) * 16)), pk[ci][h][4 * q], pk[ci][h][4 * q + 1],
-                           pk[ci][h][4 * q + 2], pk[ci][h][4 * q + 3]);
+              st_shared_v4(stg_row + (uint32_t)(((c16 ^ (lane & 7)) * 16)), pk[4 * q], pk[4 * q + 1], pk[4 * q + 2],
+                           pk[4 * q + 3]);
             }
+          }
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0 && row0 < p.M) {
