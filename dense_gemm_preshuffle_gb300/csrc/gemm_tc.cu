@@ -34,9 +34,9 @@
 //     acc * scale_a[m] * scale_b[n] (+ bias[n], then the activation of a
 //     fused epilogue) in fp32.  It rounds to bf16 (RNE) and writes 32 x 64
 //     staging tiles with the 128-byte swizzle: the 8 lanes of each store
-//     phase hit 8 distinct bank groups (ncu: 0 store conflicts for this
-//     kernel; the pair kernels, whose stores meet their rings' TMA writes,
-//     show 3-12% extra store wavefronts).  A TMA store writes the tiles out and
+//     phase hit 8 distinct bank groups (ncu: 0 store conflicts when no TMA
+//     writes land beside the stores; extra wavefronts appear only where an
+//     epilogue overlaps the next tile's ring copies).  A TMA store writes the tiles out and
 //     clips rows >= M.  With the single 512-column accumulator of 256 x 256
 //     tiles the epilogue is not overlapped, so eight warps halve it.
 //
