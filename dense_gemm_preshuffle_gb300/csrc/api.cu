@@ -289,6 +289,7 @@ int gemm_run_ex(const void* A, const void* B_packed, int dtype, int64_t M, int64
     p.K = (int)K;
     p.ktiles = (int)(K / 128);  // 128-element K tiles of A (int8: K bytes a row)
     p.strip = i8_strip_rows((int)N, d->num_sms);
+    p.split = i8_split_k(((N + p.strip - 1) / p.strip) * ((M + 15) / 16), p.ktiles, p.strip, d->num_sms);
     p.b_constant = b_constant;
     p.independent = independent;
     p.w4 = w4 ? 1 : 0;

@@ -65,15 +65,21 @@ constexpr int I8_CTAS_PER_SM = 2;
 __host__ __device__ constexpr int i8_ctas_per_sm(int nb8) { return nb8 <= 2 ? 3 : (nb8 <= 4 ? 2 : 1); }
 
 // NB8: eight-row units per strip.  W4: B is W4A8's int4 (a packed 128-byte
-// B tile then spans two 128-element K tiles of A).
-template <int NB8, bool W4>
+// B tile then spans two 128-element K tiles of A).  SPLIT: CTAs of a
+// thread-block cluster that share one strip, each over a contiguous range of
+// its K stages (1: no split).
+template <int NB8, bool W4, int SPLIT>
 __global__ void __launch_bounds__(I8_THREADS, i8_ctas_per_sm(NB8))
     i8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, I8Params p) {
+  static_assert(SPLIT == 1 || SPLIT == 2 || SPLIT == 4, "cluster sizes of the K split");
   constexpr int SN = NB8 * 8;                    // rows of B per CTA
   constexpr int BT = W4 ? I8_KT / 2 : I8_KT;     // packed B tiles (128 B per row) per stage
   constexpr int A_BYTES = I8_KT * 16 * 128;      // [kt][16 rows][128 B], 128-byte swizzle
   constexpr int B_BYTES = BT * SN * 128;         // [unit][B tile][8 rows][128 B], packed swizzle
   constexpr int STAGE = A_BYTES + B_BYTES;
+  // K split: this CTA's int32 partial [16][SN], after the ring's barriers
+  constexpr int PART_OFF = I8_STAGES * STAGE + 64;
+  constexpr int PART_BYTES = SPLIT > 1 ? 16 * SN * 4 : 0;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(base + I8_STAGES * STAGE);
@@ -83,19 +89,30 @@ __global__ void __launch_bounds__(I8_THREADS, i8_ctas_per_sm(NB8))
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int units = p.N >> 3;
-  const int u0 = blockIdx.x * NB8;
+  // K split: the SPLIT CTAs of a cluster share strip blockIdx.x / SPLIT, and
+  // rank r takes K stages [q0, q1) of the strip's nst (all of them, and
+  // rank 0, without a split).
+  const uint32_t rank = SPLIT > 1 ? cluster_ctarank() : 0u;
+  const int u0 = ((int)blockIdx.x / SPLIT) * NB8;
   const int nu = min(NB8, units - u0);  // units of this strip that exist (the last strip may be short)
   const int mg = p.mg0 + (int)blockIdx.y;  // this CTA's group of 16 rows of A
-  const int nstages = (p.ktiles + I8_KT - 1) / I8_KT;
+  const int nst = (p.ktiles + I8_KT - 1) / I8_KT;
+  const int q0 = (int)rank * nst / SPLIT;
+  const int nstages = ((int)rank + 1) * nst / SPLIT - q0;  // this CTA's stages, q0 + [0, nstages)
   const uint64_t limit = p.wait_limit_ns;
   {
-    // Launch self-check (uniform over the CTA, before any copy): the strip
-    // exists, the rows of A exist, and the ring fits the dynamic shared
-    // memory.  A mismatch is recorded and the CTA returns.
-    uint32_t dyn;
+    // Launch self-check (uniform over the CTA, and over its cluster, before
+    // any copy): the strip exists, the rows of A exist, every rank of the
+    // split has a stage, the cluster has SPLIT CTAs, and the ring fits the
+    // dynamic shared memory.  A mismatch is recorded and the CTA returns;
+    // the whole cluster then returns, so no CTA is left at a cluster barrier.
+    uint32_t dyn, ncta = 1;
     asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
-    const uint32_t need = (uint32_t)(reinterpret_cast<const volatile uint8_t*>(abort_flag + 1) - smem_raw);
-    if (nu < 1 || mg * 16 >= p.M || p.ktiles < 1 || need > dyn || (int)blockDim.x != I8_THREADS) {
+    if constexpr (SPLIT > 1) asm("mov.u32 %0, %%cluster_nctarank;" : "=r"(ncta));
+    const uint32_t need = SPLIT > 1 ? (uint32_t)(base + PART_OFF + PART_BYTES - smem_raw)
+                                     : (uint32_t)(reinterpret_cast<const volatile uint8_t*>(abort_flag + 1) - smem_raw);
+    if (nu < 1 || mg * 16 >= p.M || p.ktiles < 1 || nst < SPLIT || ncta != (uint32_t)SPLIT || need > dyn ||
+        (int)blockDim.x != I8_THREADS) {
       if (threadIdx.x == 0) atomicOr(p.status, ST_BAD_LAUNCH);
       pdl_wait();  // complete after the previous kernel all the same
       return;
@@ -124,8 +141,9 @@ __global__ void __launch_bounds__(I8_THREADS, i8_ctas_per_sm(NB8))
   // or K tiles past the end are not read, and the consumers never use their
   // bytes.  W4A8: NB8 units x BT packed tiles of 8 rows in one TMA box, units
   // past N read as zeros.
-  auto load_b = [&](int q, int bl) {
-    const int s = q % I8_STAGES;
+  auto load_b = [&](int lq, int bl) {
+    const int s = lq % I8_STAGES;
+    const int q = q0 + lq;
     if constexpr (!W4) {
       const int u = u0 + bl;
       const int kt0 = q * I8_KT;
@@ -145,8 +163,9 @@ __global__ void __launch_bounds__(I8_THREADS, i8_ctas_per_sm(NB8))
         : "memory");
   };
   // A: I8_KT K tiles x 16 rows x 128 B (rows >= M and K tiles >= ktiles read as zeros)
-  auto load_a = [&](int q) {
-    const int s = q % I8_STAGES;
+  auto load_a = [&](int lq) {
+    const int s = lq % I8_STAGES;
+    const int q = q0 + lq;
     mbar_arrive_expect_tx(&full[s], A_BYTES);
     asm volatile(
         "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::
@@ -162,7 +181,7 @@ __global__ void __launch_bounds__(I8_THREADS, i8_ctas_per_sm(NB8))
   const int early = p.b_constant ? min(nstages, I8_STAGES) : 0;
   if (threadIdx.x == I8_PRODUCER * 32) {
     // A prefetch is only a cache hint: safe while the previous kernel runs.
-    for (int q = early; q < nstages; ++q)
+    for (int q = q0 + early; q < q0 + nstages; ++q)
       asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
                        reinterpret_cast<uint64_t>(&tmB)),
                    "r"(0), "r"(0), "r"(q * BT), "r"(u0)
@@ -171,7 +190,7 @@ __global__ void __launch_bounds__(I8_THREADS, i8_ctas_per_sm(NB8))
   if (threadIdx.x == 32) {
     // A is warmed in L2 too (the previous kernel may still write it; L2
     // stays coherent, so the hint is harmless).
-    for (int q = 0; q < nstages; ++q)
+    for (int q = q0; q < q0 + nstages; ++q)
       asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
                        reinterpret_cast<uint64_t>(&tmA)),
                    "r"(0), "r"(mg * 16), "r"(q * I8_KT)
@@ -217,7 +236,13 @@ __global__ void __launch_bounds__(I8_THREADS, i8_ctas_per_sm(NB8))
         }
       }
     }
-    return;  // the producer takes no part in the reduction below
+    if constexpr (SPLIT > 1) {
+      // the producer takes no part in the reduction below, but every thread
+      // of the cluster passes both of its cluster barriers
+      cluster_sync_all();
+      cluster_sync_all();
+    }
+    return;
   }
 
   // ------------------------------------------------------------ consumers
@@ -234,7 +259,7 @@ __global__ void __launch_bounds__(I8_THREADS, i8_ctas_per_sm(NB8))
     const int s = q % I8_STAGES;
     const uint32_t ph = (uint32_t)(q / I8_STAGES) & 1;
     if (!wait_bounded(&full[s], ph, abort_flag, p.status, ST_TIMEOUT_CONSUMER, limit)) break;
-    const bool live = q * I8_KT + warp < p.ktiles;
+    const bool live = (q0 + q) * I8_KT + warp < p.ktiles;
     const uint8_t* sa = base + s * STAGE + warp * (16 * 128);
     float f[NB8][4];
 #pragma unroll
@@ -363,13 +388,43 @@ __global__ void __launch_bounds__(I8_THREADS, i8_ctas_per_sm(NB8))
   named_bar_sync(1, I8_CW * 32);
   const int cols = nu * 8;
   const int n0 = u0 * 8;
-  for (int i = threadIdx.x; i < 16 * cols; i += I8_CW * 32) {
-    const int m = i / cols, n = i - m * cols;
-    int sum = 0;
+  if constexpr (SPLIT == 1) {
+    for (int i = threadIdx.x; i < 16 * cols; i += I8_CW * 32) {
+      const int m = i / cols, n = i - m * cols;
+      int sum = 0;
 #pragma unroll
-    for (int w = 0; w < I8_CW; ++w) sum += red[(w * 16 + m) * RS + n];
-    const int gm = mg * 16 + m;
-    if (gm < p.M) p.C[(size_t)gm * p.N + n0 + n] = sum;
+      for (int w = 0; w < I8_CW; ++w) sum += red[(w * 16 + m) * RS + n];
+      const int gm = mg * 16 + m;
+      if (gm < p.M) p.C[(size_t)gm * p.N + n0 + n] = sum;
+    }
+  } else {
+    // K split: this CTA's partial [16][SN] goes to its own buffer beside the
+    // ring; after a cluster barrier (release / acquire) rank r sums columns
+    // [r cols / SPLIT, (r + 1) cols / SPLIT) of every rank's partial, read
+    // through distributed shared memory in rank order, and stores them.
+    // Integer sums: exact in any order.  A second cluster barrier keeps
+    // every partial alive until its last remote read.
+    int32_t* part = reinterpret_cast<int32_t*>(base + PART_OFF);
+    for (int i = threadIdx.x; i < 16 * cols; i += I8_CW * 32) {
+      const int m = i / cols, n = i - m * cols;
+      int sum = 0;
+#pragma unroll
+      for (int w = 0; w < I8_CW; ++w) sum += red[(w * 16 + m) * RS + n];
+      part[m * SN + n] = sum;
+    }
+    cluster_sync_all();
+    const int c0 = (int)rank * cols / SPLIT;
+    const int nc = ((int)rank + 1) * cols / SPLIT - c0;
+    for (int i = threadIdx.x; i < 16 * nc; i += I8_CW * 32) {
+      const int m = i / nc, n = c0 + (i - m * nc);
+      const uint32_t addr = smem_u32(part + m * SN + n);
+      int sum = 0;
+#pragma unroll
+      for (int j = 0; j < SPLIT; ++j) sum += (int)ld_shared_cluster_u32(mapa_shared(addr, (uint32_t)j));
+      const int gm = mg * 16 + m;
+      if (gm < p.M) p.C[(size_t)gm * p.N + n0 + n] = sum;
+    }
+    cluster_sync_all();
   }
   // An independent call completes only after the kernel before it, so a
   // later kernel's wait on this one covers everything earlier on the stream.
@@ -385,27 +440,34 @@ static int env_int(const char* name, int dflt) {
   return v > 0 ? v : dflt;
 }
 
-template <int NB8, bool W4>
+template <int NB8, bool W4, int SPLIT = 1>
 static int launch_i8(const CUtensorMap& tmA, const CUtensorMap& tmB, I8Params p, dim3 grid, cudaStream_t stream) {
   constexpr int STAGE = I8_KT * 16 * 128 + (W4 ? I8_KT / 2 : I8_KT) * NB8 * 8 * 128;
   constexpr int RED = I8_CW * 16 * NB8 * 8 * 4;
   constexpr int RING = I8_STAGES * STAGE;
-  constexpr int SMEM = (RING > RED ? RING : RED) + 2 * I8_STAGES * 8 + 16 + 1024;
+  static_assert(RED <= RING, "the reduction reuses the ring");
+  // the ring, its barriers (64 bytes), the K split's partial, alignment slack
+  constexpr int SMEM = RING + 64 + (SPLIT > 1 ? 16 * NB8 * 8 * 4 : 0) + 1024;
   static_assert(SMEM * i8_ctas_per_sm(NB8) <= 228 * 1024, "shared memory budget");
-  auto kern = i8_gemm_kernel<NB8, W4>;
+  auto kern = i8_gemm_kernel<NB8, W4, SPLIT>;
   static std::atomic<bool> attr_set[64];
   if (const int rc = smem_attr_once(attr_set, kern, SMEM); rc != GP_OK) return rc;
   p.stages = I8_STAGES;
+  grid.x *= SPLIT;  // SPLIT consecutive CTAs, one cluster, per strip
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(I8_THREADS);
   cfg.dynamicSmemBytes = (size_t)SMEM;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = SPLIT;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = SPLIT > 1 ? 2 : 1;
   if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, p) != cudaSuccess) return GP_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? GP_OK : GP_ERR_CUDA;
 }
@@ -446,10 +508,46 @@ int i8_gemm_launch(const CUtensorMap& tmA, const CUtensorMap& tmB, I8Params p, i
   return i8_gemm_launch_groups(tmA, tmB, p, groups, stream);
 }
 
+int i8_split_k(int64_t ctas, int ktiles, int strip, int num_sms) {
+  // K split over a cluster for products whose strips alone leave SMs
+  // without a CTA (narrow N): the largest split in {2, 4} that keeps the
+  // grid within one wave of resident CTAs and gives every rank at least two
+  // stages of 8 K tiles, so that each CTA's two-stage ring still overlaps
+  // its copies with its MMAs.  Built for 16- and 32-row strips.
+  // GP_I8_SPLITK (1, 2 or 4) forces a split where it is valid, for sweeps.
+  static const int forced = env_int("GP_I8_SPLITK", 0);
+  const int nst = (ktiles + I8_KT - 1) / I8_KT;
+  if (strip != 16 && strip != 32) return 1;
+  if (forced == 1 || forced == 2 || forced == 4) return nst >= forced ? forced : 1;
+  if (ctas >= num_sms) return 1;
+  const int64_t slots = (int64_t)num_sms * i8_ctas_per_sm(strip / 8);
+  int split = 1;
+  for (int s : {2, 4})
+    if (ctas * s <= slots && nst >= 2 * s) split = s;
+  return split;
+}
+
 static int i8_gemm_launch_groups(const CUtensorMap& tmA, const CUtensorMap& tmB, I8Params p, int ngroups,
                                  cudaStream_t stream) {
   const int strip = p.strip;
   dim3 grid((unsigned)((p.N + strip - 1) / strip), (unsigned)ngroups);
+  const int split = p.split;
+  if (split == 2 || split == 4) {
+    // strips of 16 or 32 rows only (i8_split_k)
+    if (strip == 16) {
+      if (p.w4) return split == 2 ? launch_i8<2, true, 2>(tmA, tmB, p, grid, stream)
+                                  : launch_i8<2, true, 4>(tmA, tmB, p, grid, stream);
+      return split == 2 ? launch_i8<2, false, 2>(tmA, tmB, p, grid, stream)
+                        : launch_i8<2, false, 4>(tmA, tmB, p, grid, stream);
+    }
+    if (strip == 32) {
+      if (p.w4) return split == 2 ? launch_i8<4, true, 2>(tmA, tmB, p, grid, stream)
+                                  : launch_i8<4, true, 4>(tmA, tmB, p, grid, stream);
+      return split == 2 ? launch_i8<4, false, 2>(tmA, tmB, p, grid, stream)
+                        : launch_i8<4, false, 4>(tmA, tmB, p, grid, stream);
+    }
+    return GP_ERR_UNSUPPORTED;
+  }
   if (p.w4) {
     switch (strip) {
       case 16: return launch_i8<2, true>(tmA, tmB, p, grid, stream);

@@ -62,6 +62,7 @@ struct I8Params {
   int w4;                 // 1: B is int4 (W4A8), packed as PACK_W4
   int debug_skip_load;    // 0 = off; i > 0: the B producer stops before its i-th stage load
   int mg0;                // first group of 16 rows of A of this launch (grids hold <= 65535 groups)
+  int split;              // CTAs of a cluster sharing one strip along K (1, 2 or 4)
 };
 
 // Output tile t of a tiles_m x tiles_n grid, walked in groups of G M tiles
@@ -109,6 +110,7 @@ bool mxf4_pair_choice(int64_t M);
 int mxf4_gemm_launch(bool pair, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmSFB,
                      const CUtensorMap& tmC, TcParams p, int num_sms, cudaStream_t stream);
 int i8_strip_rows(int N, int num_sms);
+int i8_split_k(int64_t ctas, int ktiles, int strip, int num_sms);
 int i8_gemm_launch(const CUtensorMap& tmA, const CUtensorMap& tmB, I8Params p, int num_sms, cudaStream_t stream);
 
 int quant_launch(const void* X, bool x_bf16, int64_t M, int64_t K, bool to_e2m1, void* Q, void* S, int num_sms,

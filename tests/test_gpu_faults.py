@@ -62,14 +62,16 @@ CHILD = textwrap.dedent("""
 # One case per kernel: the tcgen05 tile kernel (128 x 128 tiles), its 2-CTA
 # pair form (256 x 256 tiles: both CTAs of every pair skip the stage), the
 # INT8 weight-streaming kernel (its B producer skips the stage), the MXFP4
-# kernel (M = 128) and its pair form (M = 200), and the split-K cluster
-# kernel (every CTA of every cluster skips the stage).
+# kernel (M = 128) and its pair form (M = 200), the split-K cluster kernel
+# (every CTA of every cluster skips the stage), and the INT8 kernel split
+# along K over 4-CTA clusters (narrow N: every rank skips its stage, and all
+# of them still meet at the cluster barriers of the reduction).
 CASES = [("e4m3", 256, 512, 1024), ("e4m3", 2048, 4096, 1024), ("int8", 16, 7168, 4096), ("e2m1", 128, 512, 2048),
-         ("e2m1", 200, 512, 2048), ("bf16", 400, 4096, 8192)]
+         ("e2m1", 200, 512, 2048), ("bf16", 400, 4096, 8192), ("int8", 16, 1024, 16384)]
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("case", CASES, ids=lambda c: f"{c[0]}-{c[1]}")
+@pytest.mark.parametrize("case", CASES, ids=lambda c: f"{c[0]}-{c[1]}x{c[2]}x{c[3]}")
 def test_bounded_wait_timeout_reported_and_context_survives(case):
     torch = pytest.importorskip("torch")
     if not torch.cuda.is_available():
