@@ -7,9 +7,14 @@
 //
 //   - The grid is one wave.  Each CTA owns a strip of `strip` consecutive
 //     rows of B (a multiple of 16, chosen so that two strips share an SM
-//     where N allows) and all of K, for one group of 16 rows of A.  No
-//     split-K, so no cross-CTA reduction.  The INT8 packed layout stores
-//     8-row bands, so a strip's rows for 8 K tiles are one 4-D TMA box.
+//     where N allows) and all of K, for one group of 16 rows of A.  The
+//     INT8 packed layout stores 8-row bands, so a strip's rows for 8 K tiles
+//     are one 4-D TMA box.
+//   - Narrow N (fewer strips than SMs): the strip's K stages are split over
+//     the 2, 4 or 8 CTAs of a thread-block cluster.  Each rank streams its
+//     range of B and A; the int32 partials (each with its own offset
+//     correction) are summed exactly through distributed shared memory,
+//     every rank storing a slice of the strip's columns.
 //   - A CTA takes under half of an SM, so with programmatic dependent
 //     launch the next GEMM's CTAs start beside this one's on the SMs that
 //     hold a single strip: they warm L2 with their weights and, for constant
@@ -71,7 +76,7 @@ __host__ __device__ constexpr int i8_ctas_per_sm(int nb8) { return nb8 <= 2 ? 3 
 template <int NB8, bool W4, int SPLIT>
 __global__ void __launch_bounds__(I8_THREADS, i8_ctas_per_sm(NB8))
     i8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, I8Params p) {
-  static_assert(SPLIT == 1 || SPLIT == 2 || SPLIT == 4, "cluster sizes of the K split");
+  static_assert(SPLIT == 1 || SPLIT == 2 || SPLIT == 4 || SPLIT == 8, "cluster sizes of the K split");
   constexpr int SN = NB8 * 8;                    // rows of B per CTA
   constexpr int BT = W4 ? I8_KT / 2 : I8_KT;     // packed B tiles (128 B per row) per stage
   constexpr int A_BYTES = I8_KT * 16 * 128;      // [kt][16 rows][128 B], 128-byte swizzle
@@ -510,20 +515,22 @@ int i8_gemm_launch(const CUtensorMap& tmA, const CUtensorMap& tmB, I8Params p, i
 
 int i8_split_k(int64_t ctas, int ktiles, int strip, int num_sms) {
   // K split over a cluster for products whose strips alone leave SMs
-  // without a CTA (narrow N): the largest split in {2, 4} that keeps the
+  // without a CTA (narrow N): the largest split in {2, 4, 8} that keeps the
   // grid within one wave of resident CTAs and gives every rank at least two
   // stages of 8 K tiles, so that each CTA's two-stage ring still overlaps
-  // its copies with its MMAs.  Built for 16- and 32-row strips.
-  // GP_I8_SPLITK (1, 2 or 4) forces a split where it is valid, for sweeps.
+  // its copies with its MMAs.  Built for 16- and 32-row strips (a split of
+  // 8, the portable cluster limit, for 16-row strips only).
+  // GP_I8_SPLITK (1, 2, 4 or 8) forces a split where it is valid, for sweeps.
   static const int forced = env_int("GP_I8_SPLITK", 0);
   const int nst = (ktiles + I8_KT - 1) / I8_KT;
   if (strip != 16 && strip != 32) return 1;
-  if (forced == 1 || forced == 2 || forced == 4) return nst >= forced ? forced : 1;
+  auto built = [&](int s) { return s != 8 || strip == 16; };
+  if (forced == 1 || forced == 2 || forced == 4 || forced == 8) return (nst >= forced && built(forced)) ? forced : 1;
   if (ctas >= num_sms) return 1;
   const int64_t slots = (int64_t)num_sms * i8_ctas_per_sm(strip / 8);
   int split = 1;
-  for (int s : {2, 4})
-    if (ctas * s <= slots && nst >= 2 * s) split = s;
+  for (int s : {2, 4, 8})
+    if (built(s) && ctas * s <= slots && nst >= 2 * s) split = s;
   return split;
 }
 
@@ -532,6 +539,11 @@ static int i8_gemm_launch_groups(const CUtensorMap& tmA, const CUtensorMap& tmB,
   const int strip = p.strip;
   dim3 grid((unsigned)((p.N + strip - 1) / strip), (unsigned)ngroups);
   const int split = p.split;
+  if (split == 8) {
+    // 16-row strips only (i8_split_k)
+    if (strip != 16) return GP_ERR_UNSUPPORTED;
+    return p.w4 ? launch_i8<2, true, 8>(tmA, tmB, p, grid, stream) : launch_i8<2, false, 8>(tmA, tmB, p, grid, stream);
+  }
   if (split == 2 || split == 4) {
     // strips of 16 or 32 rows only (i8_split_k)
     if (strip == 16) {

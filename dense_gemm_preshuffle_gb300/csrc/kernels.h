@@ -62,7 +62,7 @@ struct I8Params {
   int w4;                 // 1: B is int4 (W4A8), packed as PACK_W4
   int debug_skip_load;    // 0 = off; i > 0: the B producer stops before its i-th stage load
   int mg0;                // first group of 16 rows of A of this launch (grids hold <= 65535 groups)
-  int split;              // CTAs of a cluster sharing one strip along K (1, 2 or 4)
+  int split;              // CTAs of a cluster sharing one strip along K (1, 2, 4 or 8)
 };
 
 // Output tile t of a tiles_m x tiles_n grid, walked in groups of G M tiles

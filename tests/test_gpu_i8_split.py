@@ -3,12 +3,12 @@
 The "GEMM Optimization Guide" (section 1.3) asks small batches to stream the
 weights with a large K tile; with a narrow N the strips of B rows alone
 leave SMs idle, so the weight-streaming kernel splits each strip's K stages
-over 2 or 4 CTAs of a cluster and sums their int32 partials exactly through
+over 2, 4 or 8 CTAs of a cluster and sums their int32 partials exactly through
 distributed shared memory.  Integer sums do not depend on the order, so
 every split must give the same bits as the oracle's exact product.
 
-In-process cases take the library's own choice (narrow N: a split of 2 or
-4; the shapes are chosen so that each split occurs, with ragged M, several
+In-process cases take the library's own choice (narrow N: a split of 2, 4
+or 8; the shapes are chosen so that each split occurs, with ragged M, several
 row groups, ranks with unequal stage counts, and a last stage with fewer
 than 8 K tiles).  A child process per forced split (GP_I8_SPLITK, read once
 per process) runs shared inputs, the 16 x 7168 x 4096 workload included,
@@ -63,6 +63,8 @@ AUTO = [
     ("int8", 32, 1024, 8192),    # two row groups, 128 CTAs: split 2
     ("w4a8", 16, 1024, 8192),    # int4 weights: split 4
     ("w4a8", 7, 1152, 4864),     # int4, ragged M, 38 K tiles: split 2, the last stage has 6 K tiles
+    ("int8", 16, 512, 16384),    # 32 strips: split 8 (the portable cluster limit), 2 stages a rank
+    ("w4a8", 16, 512, 16384),    # int4 weights: split 8
 ]
 
 
@@ -103,7 +105,7 @@ def test_split_k_extremes(dtype):
 
 
 FORCED = [("int8", 16, 7168, 4096), ("int8", 5, 1152, 4736), ("int8", 16, 512, 2176), ("w4a8", 16, 7168, 4096),
-          ("w4a8", 9, 1152, 4864)]
+          ("w4a8", 9, 1152, 4864), ("int8", 16, 1024, 8192)]
 
 CHILD = textwrap.dedent("""
     import sys
@@ -137,10 +139,12 @@ def run_forced(split, path):
 
 
 def test_forced_splits_bit_identical(tmp_path):
-    """Splits 1, 2 and 4 forced on the same inputs: identical bits, and the
-    oracle's exact product.  17 K tiles (3 stages) admit a split of 2 but
-    not 4 (that case then runs unsplit)."""
-    results = {s: run_forced(s, str(tmp_path / f"split{s}.npz")) for s in (1, 2, 4)}
+    """Splits 1, 2, 4 and 8 forced on the same inputs: identical bits, and
+    the oracle's exact product.  A split runs only where every rank gets a
+    stage and, for 8, the strip has 16 rows (otherwise the case runs
+    unsplit): 17 K tiles (3 stages) admit a split of 2 only, and 16 x 1024 x
+    8192 (8 stages) a split of 8 with one stage a rank."""
+    results = {s: run_forced(s, str(tmp_path / f"split{s}.npz")) for s in (1, 2, 4, 8)}
     for i, (dtype, M, N, K) in enumerate(FORCED):
         key = "c%d" % i
         ref = oracle.gemm_operands(inputs.make_operands(dtype, M, N, K, seed=60 + i))
