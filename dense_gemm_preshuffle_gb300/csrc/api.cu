@@ -327,17 +327,19 @@ int gemm_run_ex(const void* A, const void* B_packed, int dtype, int64_t M, int64
   // Tile height: 256 rows (two 128-row MMAs sharing each B tile) when that
   // still gives every SM several tiles, or when K is split over a cluster
   // (few tiles); the E2M1 kernel uses 128.
-  const int split = dtype == GP_E2M1 ? 1 : splitk_choice(M, N, kb / 128, d->num_sms);
+  // Few 256 x 256 tiles with a long K: two pairs per tile, one per half of K.
+  const bool xpair = dtype != GP_E2M1 && xpair_choice(M, N, (int)(kb / 128), d->num_sms);
+  const int split = (dtype == GP_E2M1 || xpair) ? 1 : splitk_choice(M, N, kb / 128, d->num_sms);
   int bm = 128, bn = 256;
   if (dtype != GP_E2M1) {
-    if (split > 1)
+    if (split > 1 || xpair)
       bm = 256;
     else
       tc_tile_choice(M, N, d->num_sms, &bm, &bn);
   }
   // 2-CTA pair tiles replace the single-CTA 128 x 128 and 256 x 256 tiles
   // where a tile has rows for both CTAs (0: single-CTA tiles).
-  const int pair_bn = (dtype != GP_E2M1 && split == 1) ? pair_choice(M, bm, bn) : 0;
+  const int pair_bn = xpair ? 256 : (dtype != GP_E2M1 && split == 1) ? pair_choice(M, bm, bn) : 0;
   CUtensorMap tmA, tmC;
   const int kstep = pair_bn != 0 ? kPairKstep : (dtype != GP_E2M1 && split == 1) ? tc_kstep(bm, bn) : 1;
   const int a_rows = pair_bn != 0 ? 128 : bm;  // rows of A per CTA
@@ -429,6 +431,7 @@ int gemm_run_ex(const void* A, const void* B_packed, int dtype, int64_t M, int64
                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return GP_ERR_CUDA;
+    if (xpair) return xpair_gemm_launch(kind, tmA, tmB, tmC, p, st);
     return pair_gemm_launch(kind, pair_bn, tmA, tmB, tmC, p, d->num_sms, st);
   }
   return tc_gemm_launch(kind, bm, bn, tmA, tmC, p, d->num_sms, st);

@@ -97,6 +97,12 @@ int pair_choice(int64_t M, int bm, int bn);
 // Whether a 256 x 256 pair tile splits its K range over its two accumulator
 // buffers (summed in fp32 by the epilogue) for a product of `ktiles` K tiles.
 bool pair_ksplit(int ktiles);
+// Few 256 x 256 tiles with a long K: a 4-CTA cluster per tile, two pairs
+// (one per half of K) whose partials are summed through distributed shared
+// memory.  Same tensor maps as the pair kernel with BN = 256.
+bool xpair_choice(int64_t M, int64_t N, int ktiles, int num_sms);
+int xpair_gemm_launch(int kind, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, TcParams p,
+                      cudaStream_t stream);
 int pair_gemm_launch(int kind, int bn, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
                      TcParams p, int num_sms, cudaStream_t stream);
 int splitk_choice(int64_t M, int64_t N, int64_t ktiles, int num_sms);

@@ -65,9 +65,11 @@ CHILD = textwrap.dedent("""
 # kernel (M = 128) and its pair form (M = 200), the split-K cluster kernel
 # (every CTA of every cluster skips the stage), and the INT8 kernel split
 # along K over 4-CTA clusters (narrow N: every rank skips its stage, and all
-# of them still meet at the cluster barriers of the reduction).
+# of them still meet at the cluster barriers of the reduction), and the
+# K split over two pairs of CTAs (512 x 4096 x 4096: both pairs of every
+# cluster skip the stage; the exchange and both cluster barriers still end).
 CASES = [("e4m3", 256, 512, 1024), ("e4m3", 2048, 4096, 1024), ("int8", 16, 7168, 4096), ("e2m1", 128, 512, 2048),
-         ("e2m1", 200, 512, 2048), ("bf16", 400, 4096, 8192), ("int8", 16, 1024, 16384)]
+         ("e2m1", 200, 512, 2048), ("bf16", 400, 4096, 8192), ("int8", 16, 1024, 16384), ("bf16", 512, 4096, 4096)]
 
 
 @pytest.mark.gpu
