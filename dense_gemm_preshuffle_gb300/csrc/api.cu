@@ -341,9 +341,12 @@ int gemm_run_ex(const void* A, const void* B_packed, int dtype, int64_t M, int64
   // where a tile has rows for both CTAs (0: single-CTA tiles).
   const int pair_bn = xpair ? 256 : (dtype != GP_E2M1 && split == 1) ? pair_choice(M, bm, bn) : 0;
   CUtensorMap tmA, tmC;
-  const int kstep = pair_bn != 0 ? kPairKstep : (dtype != GP_E2M1 && split == 1) ? tc_kstep(bm, bn) : 1;
+  const int kstep = xpair                     ? kXpairKstep
+                    : pair_bn != 0              ? kPairKstep
+                    : (dtype != GP_E2M1 && split == 1) ? tc_kstep(bm, bn)
+                                                : 1;
   const int a_rows = pair_bn != 0 ? 128 : bm;  // rows of A per CTA
-  if (kstep == 1) {
+  if (kstep == 1 && !xpair) {  // (the two-pair kernel reads A through the 3-D view)
     if ((rc = encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, (uint64_t)kb, (uint64_t)M, (uint64_t)kb, 128,
                         (uint32_t)a_rows, CU_TENSOR_MAP_SWIZZLE_128B)) != GP_OK)
       return rc;
@@ -425,7 +428,7 @@ int gemm_run_ex(const void* A, const void* B_packed, int dtype, int64_t M, int64
     CUtensorMap tmB;
     cuuint64_t dims[3] = {128, 128, (cuuint64_t)(N / 128) * (cuuint64_t)(kb / 128)};
     cuuint64_t strides[2] = {128, 16384};
-    cuuint32_t box[3] = {128, (cuuint32_t)(pair_bn / 2), (cuuint32_t)kPairKstep};
+    cuuint32_t box[3] = {128, (cuuint32_t)(pair_bn / 2), (cuuint32_t)kstep};
     cuuint32_t estr[3] = {1, 1, 1};
     if (g_encode(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(B_packed), dims, strides, box, estr,
                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

@@ -51,10 +51,12 @@ namespace {
 
 constexpr int XP_EPI_WARPS = 8;  // warps 2..9: two per TMEM lane quarter, one 64-column chunk of each half
 constexpr int XP_THREADS = 32 * (2 + XP_EPI_WARPS);
-constexpr int XP_STAGES = 3;
-constexpr int XP_A_BYTES = kPairKstep * 128 * 128;  // [K tile][128 rows][128 B]
-constexpr int XP_B_BYTES = kPairKstep * 128 * 128;  // [K tile][128 rows of the tile's 256][128 B]
-constexpr int XP_RING = XP_STAGES * (XP_A_BYTES + XP_B_BYTES);
+template <int KSTEP, int STAGES>
+struct XpCfg {
+  static constexpr int A_BYTES = KSTEP * 128 * 128;  // [K tile][128 rows][128 B]
+  static constexpr int B_BYTES = KSTEP * 128 * 128;  // [K tile][128 rows of the tile's 256][128 B]
+  static constexpr int RING = STAGES * (A_BYTES + B_BYTES);
+};
 // After the main loop the ring holds: the partial for the K peer (8 warps x
 // 32 rows x 64 fp32), the peer's partial for this CTA, and the output
 // staging (8 warps x 32 rows x 64 16-bit values).
@@ -62,17 +64,21 @@ constexpr int XP_SLOT = 32 * 64 * 4;
 constexpr int XP_OUT_OFF = 0;
 constexpr int XP_IN_OFF = XP_EPI_WARPS * XP_SLOT;
 constexpr int XP_STG_OFF = 2 * XP_EPI_WARPS * XP_SLOT;
-static_assert(XP_STG_OFF + XP_EPI_WARPS * 32 * 128 <= XP_RING, "exchange buffers fit in the ring");
 constexpr int XP_BAR_BYTES = 256;
-constexpr int XP_SMEM = XP_RING + XP_BAR_BYTES + 1024;
 constexpr uint32_t XP_TMEM_COLS = 256;
 
 }  // namespace
 
-template <int KIND>
+template <int KIND, int KSTEP, int STAGES>
 __global__ void __launch_bounds__(XP_THREADS, 1)
     xpair_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmC, TcParams p) {
+  using Cfg = XpCfg<KSTEP, STAGES>;
+  constexpr int XP_STAGES = STAGES;
+  constexpr int XP_A_BYTES = Cfg::A_BYTES;
+  constexpr int XP_B_BYTES = Cfg::B_BYTES;
+  constexpr int XP_RING = Cfg::RING;
+  static_assert(XP_STG_OFF + XP_EPI_WARPS * 32 * 128 <= XP_RING, "exchange buffers fit in the ring");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* s_a = base;
@@ -98,7 +104,7 @@ __global__ void __launch_bounds__(XP_THREADS, 1)
   const uint64_t limit = p.wait_limit_ns;
   const int kt0 = (int)half * p.ktiles / 2;
   const int kt1 = ((int)half + 1) * p.ktiles / 2;
-  const int kstages = (kt1 - kt0 + kPairKstep - 1) / kPairKstep;
+  const int kstages = (kt1 - kt0 + KSTEP - 1) / KSTEP;
   {
     // Launch self-check, uniform over the cluster: four CTAs a cluster, one
     // tile per cluster, a K tile for each half, and the ring in the dynamic
@@ -148,10 +154,10 @@ __global__ void __launch_bounds__(XP_THREADS, 1)
   const int a_row = mb * 256 + (int)sub * 128;
   const int b_tile0 = (2 * nb + (int)sub) * p.ktiles;  // this band's first K tile in packed B
   auto load_a = [&](int st, int ks) {
-    tma_load_3d_pair(s_a + st * XP_A_BYTES, &tmA, 0, a_row, kt0 + ks * kPairKstep, full_lead + (uint32_t)(st * 8));
+    tma_load_3d_pair(s_a + st * XP_A_BYTES, &tmA, 0, a_row, kt0 + ks * KSTEP, full_lead + (uint32_t)(st * 8));
   };
   auto load_b = [&](int st, int ks) {
-    tma_load_3d_pair(s_b + st * XP_B_BYTES, &tmB, 0, 0, b_tile0 + kt0 + ks * kPairKstep,
+    tma_load_3d_pair(s_b + st * XP_B_BYTES, &tmB, 0, 0, b_tile0 + kt0 + ks * KSTEP,
                      full_lead + (uint32_t)(st * 8));
   };
 
@@ -159,8 +165,8 @@ __global__ void __launch_bounds__(XP_THREADS, 1)
     // warm L2 with the first stages while the previous kernel may still run
     const int kpre = kstages < XP_STAGES ? kstages : XP_STAGES;
     for (int ks = 0; ks < kpre; ++ks) {
-      prefetch_l2_tile_3d(&tmA, 0, a_row, kt0 + ks * kPairKstep);
-      prefetch_l2_tile_3d(&tmB, 0, 0, b_tile0 + kt0 + ks * kPairKstep);
+      prefetch_l2_tile_3d(&tmA, 0, a_row, kt0 + ks * KSTEP);
+      prefetch_l2_tile_3d(&tmB, 0, 0, b_tile0 + kt0 + ks * KSTEP);
     }
   }
   // With constant weights the B issuer requests the first stages of B
@@ -235,8 +241,8 @@ __global__ void __launch_bounds__(XP_THREADS, 1)
         const uint32_t a0 = smem_u32(s_a + s * XP_A_BYTES);
         const uint32_t b0 = smem_u32(s_b + s * XP_B_BYTES);
         // the last stage of a half may hold a K tile of the other half: not used
-        const int nk = min(kPairKstep, kt1 - (kt0 + ks * kPairKstep));
-        for (int kk = 0; kk < nk; ++kk) {
+        const int nk = min(KSTEP, kt1 - (kt0 + ks * KSTEP));
+        for (int kk = 0; kk < nk; ++kk) {  // K tile kk of the stage
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const uint32_t acc = (ks | kk | k) != 0 ? 1u : 0u;
@@ -388,10 +394,12 @@ bool xpair_choice(int64_t M, int64_t N, int ktiles, int num_sms) {
   return tiles * 4 <= num_sms && ktiles >= 64;
 }
 
-template <int KIND>
+template <int KIND, int KSTEP, int STAGES>
 static int launch_xpair(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, const TcParams& p,
                         cudaStream_t stream) {
-  auto kern = xpair_gemm_kernel<KIND>;
+  constexpr int XP_SMEM = XpCfg<KSTEP, STAGES>::RING + XP_BAR_BYTES + 1024;
+  static_assert(XP_SMEM <= 232448, "shared memory budget");
+  auto kern = xpair_gemm_kernel<KIND, KSTEP, STAGES>;
   static std::atomic<bool> attr_set[64];
   if (const int rc = smem_attr_once(attr_set, kern, XP_SMEM); rc != GP_OK) return rc;
   cudaLaunchConfig_t cfg = {};
@@ -418,10 +426,14 @@ int xpair_gemm_launch(int kind, const CUtensorMap& tmA, const CUtensorMap& tmB, 
   p.tiles_n = p.N / 256;
   p.num_tiles = p.tiles_m * p.tiles_n;
   if ((int64_t)p.num_tiles * 4 > 0x7fffffff) return GP_ERR_SHAPE;
+  // Six stages of one K tile (32 KiB a CTA): against three of two K tiles
+  // 18.74 against 18.98 us at BF16 512 x 4096 x 4096, 28.68 against 29.06
+  // at 512 x 4096 x 8192 (seven stages, 224 KiB: no better than three).
+  static_assert(kXpairKstep == 1, "the ring below stages one K tile");
   switch (kind) {
-    case 0: return launch_xpair<0>(tmA, tmB, tmC, p, stream);
-    case 1: return launch_xpair<1>(tmA, tmB, tmC, p, stream);
-    default: return launch_xpair<2>(tmA, tmB, tmC, p, stream);
+    case 0: return launch_xpair<0, 1, 6>(tmA, tmB, tmC, p, stream);
+    case 1: return launch_xpair<1, 1, 6>(tmA, tmB, tmC, p, stream);
+    default: return launch_xpair<2, 1, 6>(tmA, tmB, tmC, p, stream);
   }
 }
 

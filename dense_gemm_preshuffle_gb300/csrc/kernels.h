@@ -99,8 +99,11 @@ int pair_choice(int64_t M, int bm, int bn);
 bool pair_ksplit(int ktiles);
 // Few 256 x 256 tiles with a long K: a 4-CTA cluster per tile, two pairs
 // (one per half of K) whose partials are summed through distributed shared
-// memory.  Same tensor maps as the pair kernel with BN = 256.
+// memory.  The pair kernel's tensor maps with BN = 256, their K boxes of
+// kXpairKstep tiles.
 bool xpair_choice(int64_t M, int64_t N, int ktiles, int num_sms);
+// Its tensor maps' boxes hold kXpairKstep K tiles (A: a 3-D box of 128 rows).
+constexpr int kXpairKstep = 1;
 int xpair_gemm_launch(int kind, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, TcParams p,
                       cudaStream_t stream);
 int pair_gemm_launch(int kind, int bn, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
