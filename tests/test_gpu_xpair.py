@@ -12,8 +12,8 @@ BF16 / FP16 512 x 4096 x 4096 workloads, whose every output the parity
 tests in test_gpu_gemm.py compare).  Here GP_XPAIR=1 forces it, in a child
 process (the switch is read once per process), on ragged M, an odd number
 of K tiles (the halves differ by one and a stage straddles the split),
-E4M3 with row / column scales, FP16, fused epilogues and more clusters than
-fit at once.
+E4M3 with row / column scales, FP16, fused epilogues, more clusters than
+fit at once, and K ranges of one or two K tiles a half.
 """
 import os
 import subprocess
@@ -30,7 +30,9 @@ pytestmark = pytest.mark.gpu
 # (dtype, M, N, K, epilogue)
 CASES = [("bf16", 512, 4096, 4096, "none"), ("bf16", 300, 512, 1088, "none"), ("e4m3", 200, 768, 2176, "none"),
          ("fp16", 129, 512, 960, "none"), ("bf16", 257, 512, 1024, "bias_gelu"), ("e4m3", 384, 1024, 4224, "bias"),
-         ("bf16", 2000, 4096, 1088, "none"), ("fp16", 512, 1024, 8192, "bias_silu")]
+         ("bf16", 2000, 4096, 1088, "none"), ("fp16", 512, 1024, 8192, "bias_silu"),
+         # the shortest K ranges: one K tile a half (2 tiles), one and two (3)
+         ("bf16", 256, 256, 128, "none"), ("e4m3", 512, 512, 384, "bias_relu")]
 
 CHILD = textwrap.dedent("""
     import sys
