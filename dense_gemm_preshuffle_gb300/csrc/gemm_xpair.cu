@@ -69,7 +69,7 @@ constexpr uint32_t XP_TMEM_COLS = 256;
 
 }  // namespace
 
-template <int KIND, int KSTEP, int STAGES>
+template <int KIND, int KSTEP, int STAGES, int NP>
 __global__ void __launch_bounds__(XP_THREADS, 1)
     xpair_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmC, TcParams p) {
@@ -169,11 +169,12 @@ __global__ void __launch_bounds__(XP_THREADS, 1)
       prefetch_l2_tile_3d(&tmB, 0, 0, b_tile0 + kt0 + ks * KSTEP);
     }
   }
-  // With constant weights the B issuer requests the first stages of B
+  // With constant weights the B issuers request the first stages of B
   // before the wait on the previous kernel.
   const int early = (!bad && p.b_constant) ? min(kstages, XP_STAGES) : 0;
-  if (threadIdx.x == 0 && early > 0) {
-    for (int ks = 0; ks < early; ++ks) {
+  constexpr int np = NP;  // issuing lane pairs of the producer warp
+  if (warp == 0 && lane < 2 * np && (lane & 1) == 0 && early > 0) {
+    for (int ks = lane >> 1; ks < early; ks += np) {
       if (p.debug_skip_load == 1 + ks) continue;
       if (leader) mbar_arrive_expect_tx(&full[ks], 2 * XP_B_BYTES);
       load_b(ks, ks);
@@ -187,12 +188,14 @@ __global__ void __launch_bounds__(XP_THREADS, 1)
     // nothing to do: fall through to the cluster barriers
   } else if (warp == 0) {
     // ------------------------------------------------------------ producers
-    // Lane 0 issues this CTA's rows of B, lane 1 its rows of A.
-    if (lane < 2) {
-      const bool is_b = lane == 0;
-      int ks = 0;
+    // Lanes 2j and 2j + 1 issue this CTA's rows of B and of A for the stages
+    // ks = j (mod NP): one thread's copies complete one after another, so
+    // NP pairs of issuers keep more of the ring's copies moving.
+    if (lane < 2 * np) {
+      const bool is_b = (lane & 1) == 0;
+      int ks = lane >> 1;
       bool ok = true;
-      for (; ks < kstages; ++ks) {
+      for (; ks < kstages; ks += np) {
         const int s = ks % XP_STAGES;
         const uint32_t ph = (uint32_t)(ks / XP_STAGES) & 1u;
         const bool b_done = is_b && ks < early;
@@ -214,9 +217,7 @@ __global__ void __launch_bounds__(XP_THREADS, 1)
       if (leader && (!ok || *abort_flag)) {
         // wait (bounded) for the loads still in flight, so nothing lands in
         // shared memory after exit
-        const int n = ks < XP_STAGES ? ks : XP_STAGES;
-        for (int i = 0; i < n; ++i) {
-          const int q = ks - 1 - i;
+        for (int q = ks - np; q >= 0 && q >= ks - XP_STAGES; q -= np) {
           volatile int never = 0;
           if (p.debug_skip_load == 1 + q) continue;
           wait_bounded(&full[q % XP_STAGES], (uint32_t)(q / XP_STAGES) & 1u, &never, p.status, ST_TIMEOUT_DRAIN,
@@ -394,12 +395,12 @@ bool xpair_choice(int64_t M, int64_t N, int ktiles, int num_sms) {
   return tiles * 4 <= num_sms && ktiles >= 64;
 }
 
-template <int KIND, int KSTEP, int STAGES>
+template <int KIND, int KSTEP, int STAGES, int NP>
 static int launch_xpair(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, const TcParams& p,
                         cudaStream_t stream) {
   constexpr int XP_SMEM = XpCfg<KSTEP, STAGES>::RING + XP_BAR_BYTES + 1024;
   static_assert(XP_SMEM <= 232448, "shared memory budget");
-  auto kern = xpair_gemm_kernel<KIND, KSTEP, STAGES>;
+  auto kern = xpair_gemm_kernel<KIND, KSTEP, STAGES, NP>;
   static std::atomic<bool> attr_set[64];
   if (const int rc = smem_attr_once(attr_set, kern, XP_SMEM); rc != GP_OK) return rc;
   cudaLaunchConfig_t cfg = {};
@@ -430,10 +431,13 @@ int xpair_gemm_launch(int kind, const CUtensorMap& tmA, const CUtensorMap& tmB, 
   // 18.74 against 18.98 us at BF16 512 x 4096 x 4096, 28.68 against 29.06
   // at 512 x 4096 x 8192 (seven stages, 224 KiB: no better than three).
   static_assert(kXpairKstep == 1, "the ring below stages one K tile");
+  // Two issuing lane pairs (even and odd stages): 18.45 against 18.65 us
+  // at BF16 512 x 4096 x 4096 with one pair, 28.33 against 28.52 at
+  // 512 x 4096 x 8192 (three pairs: in between).
   switch (kind) {
-    case 0: return launch_xpair<0, 1, 6>(tmA, tmB, tmC, p, stream);
-    case 1: return launch_xpair<1, 1, 6>(tmA, tmB, tmC, p, stream);
-    default: return launch_xpair<2, 1, 6>(tmA, tmB, tmC, p, stream);
+    case 0: return launch_xpair<0, 1, 6, 2>(tmA, tmB, tmC, p, stream);
+    case 1: return launch_xpair<1, 1, 6, 2>(tmA, tmB, tmC, p, stream);
+    default: return launch_xpair<2, 1, 6, 2>(tmA, tmB, tmC, p, stream);
   }
 }
 
