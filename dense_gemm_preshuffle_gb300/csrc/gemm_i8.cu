@@ -436,8 +436,8 @@ __global__ void __launch_bounds__(I8_THREADS, i8_ctas_per_sm(NB8))
   if (p.independent) pdl_wait();
 }
 
-// Tuning override, read once per process: GP_I8_STRIP (rows of B per CTA:
-// 16, 32, 48 or 64).
+// Tuning overrides, read once per process: GP_I8_STRIP (rows of B per CTA:
+// 16, 24, 32, 48 or 64) and GP_I8_SPLITK (1, 2, 4 or 8).
 static int env_int(const char* name, int dflt) {
   const char* e = std::getenv(name);
   if (e == nullptr) return dflt;
@@ -483,7 +483,7 @@ int i8_strip_rows(int N, int num_sms) {
   // next product's CTAs then sit beside this one's and stream while it
   // computes (measured 8.5 us against 9.5 us for one 48-row strip per SM at
   // 16 x 7168 x 4096).  Wider problems take one strip per SM, at most 64
-  // rows.  GP_I8_STRIP (16, 32, 48 or 64) overrides.
+  // rows.  GP_I8_STRIP (16, 24, 32, 48 or 64) overrides.
   static const int strip_override = env_int("GP_I8_STRIP", 0);
   if (strip_override == 16 || strip_override == 24 || strip_override == 32 || strip_override == 48 ||
       strip_override == 64)
