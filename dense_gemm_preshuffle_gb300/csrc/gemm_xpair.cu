@@ -171,7 +171,10 @@ __global__ void __launch_bounds__(XP_THREADS, 1)
   }
   // With constant weights the B issuers request the first stages of B
   // before the wait on the previous kernel.
-  const int early = (!bad && p.b_constant) ? min(kstages, XP_STAGES) : 0;
+  // Two stages, not the whole ring: A's first copies, issued after the wait,
+  // then queue behind fewer B copies (BF16 512 x 4096 x 4096: 18.37 against
+  // 18.6 us with all six stages requested early, 18.5 with none).
+  const int early = (!bad && p.b_constant) ? min(kstages, min(XP_STAGES, 2)) : 0;
   constexpr int np = NP;  // issuing lane pairs of the producer warp
   if (warp == 0 && lane < 2 * np && (lane & 1) == 0 && early > 0) {
     for (int ks = lane >> 1; ks < early; ks += np) {
