@@ -27,7 +27,8 @@ it once per weight, not per product.
     loop would.
   - "roofline": the GEMM kernel against the measured HBM or tensor peak.
   - "cpu_baseline": the oracle, timed on this host's cores on a bounded
-    sample.
+    sample; "cpu_oracle_others": the same for each other workload (a
+    shorter sample each).
   - "others": the other workloads, each with its own device-timed TFLOP/s
     and roofline fraction.
   - "epilogues": each float workload with the fused bias + GELU epilogue,
@@ -745,6 +746,12 @@ def run_ours(args):
     if rank == 0:
         if not args.no_cpu:
             out["cpu_baseline"] = cpu_baseline(args.workload)
+            if not args.no_others:
+                # the oracle on the other workloads too, a short bounded
+                # sample each (rows of C), for its rate per workload
+                from dense_gemm_preshuffle_gb300 import inputs
+                out["cpu_oracle_others"] = {name: cpu_baseline(name, budget_s=1.5)
+                                            for name in inputs.ALL_WORKLOADS if name != args.workload}
         print(json.dumps(out), flush=True)
     if pg is not None:
         pg.destroy_process_group()
