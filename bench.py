@@ -550,6 +550,15 @@ def roofline(prob: Problem, sec_per_step: float, peaks: dict, peak_kind: str, tr
         sus = float(peaks["bf16_tflops_sustained"]) * ratio
         out["peak_sustained"] = round(sus, 1)
         out["frac_of_sustained"] = round(achieved / sus, 4)
+    # the other roofline too: the algorithmic bytes against the measured HBM
+    # bandwidth, and the attainable rate min(peak, AI x bandwidth)
+    hbm = float(peaks["hbm_gbs"])
+    gbs = prob.bytes / sec_per_step / 1e9
+    attainable = min(peak, prob.flops / prob.bytes * hbm / 1e3)
+    out["hbm_GB/s"] = round(gbs, 1)
+    out["frac_of_hbm"] = round(gbs / hbm, 4)
+    out["attainable"] = round(attainable, 1)
+    out["frac_of_attainable"] = round(achieved / attainable, 4)
     return out
 
 
