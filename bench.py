@@ -26,6 +26,10 @@ it once per weight, not per product.
     the steps are replayed from CUDA graphs (copies included), as a serving
     loop would.
   - "roofline": the GEMM kernel against the measured HBM or tensor peak.
+  - "tensor_rates": this GPU's tcgen05 MMA rate per kind (a loop with no
+    memory traffic, rates/mma_rate.cu in the package) and its ratio to
+    bf16; tensor rooflines add "frac_of_measured_ratio_peak", the measured
+    bf16 peak times that ratio, beside "frac" (the nominal ratio).
   - "cpu_baseline": the oracle, timed on this host's cores on a bounded
     sample; "cpu_oracle_others": the same for each other workload (a
     shorter sample each).
@@ -69,7 +73,35 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # nominal dense tensor-rate ratios to bf16 (2.25 PF): fp8 4.5, fp4 13.5
 DTYPE_RATIO = {"bf16": 1.0, "fp16": 1.0, "e4m3": 2.0, "e2m1": 6.0}
 B_DEFAULT_FLAGS = False  # --b-default: time gemm_run without GP_RUN_B_CONSTANT
+# tcgen05 MMA rates of this GPU by kind (rates/mma_rate.cu), measured once per
+# run on rank 0: the ratios of FP8 and MXFP4 to bf16 beside the nominal ones
+MMA_RATES = None
 HOST_COVER_CYCLES = 200_000  # ~0.1 ms of device spin before a timed region (see time_device)
+
+
+def tensor_rates():
+    """Run the library's tensor-pipe rate probe (built beside it by build()):
+    TFLOP/s of back-to-back MMAs of each kind with no memory traffic, in the
+    single-CTA and the 2-CTA (pair) form.  Returns {kind: TFLOP/s} (the
+    higher of the two forms), the ratio of each kind to bf16, and the lines
+    it printed; None if the probe is missing or fails."""
+    import subprocess
+    exe = os.path.join(ROOT, "dense_gemm_preshuffle_gb300", "_lib", "mma_rate")
+    if not os.path.exists(exe):
+        return None
+    try:
+        r = subprocess.run([exe, "20000", "1"], capture_output=True, text=True, timeout=120)
+    except (OSError, subprocess.TimeoutExpired):
+        return None
+    lines = [json.loads(l) for l in r.stdout.splitlines() if l.startswith("{")]
+    best = {}
+    for d in lines:
+        if d.get("ok") and "tflops" in d:
+            best[d["kind"]] = max(best.get(d["kind"], 0.0), d["tflops"])
+    if r.returncode != 0 or "bf16" not in best:
+        return None
+    return {"tflops": best, "ratio_to_bf16": {k: round(v / best["bf16"], 3) for k, v in best.items()},
+            "runs": lines, "source": "dense_gemm_preshuffle_gb300/rates/mma_rate.cu, 20000 loops, this run"}
 
 
 def load_peaks():
@@ -550,6 +582,17 @@ def roofline(prob: Problem, sec_per_step: float, peaks: dict, peak_kind: str, tr
         sus = float(peaks["bf16_tflops_sustained"]) * ratio
         out["peak_sustained"] = round(sus, 1)
         out["frac_of_sustained"] = round(achieved / sus, 4)
+    kind = {"bf16": "bf16", "fp16": "fp16", "e4m3": "e4m3", "e2m1": "e2m1"}.get(prob.dtype)
+    if MMA_RATES is not None and kind in MMA_RATES["ratio_to_bf16"]:
+        # the same measured bf16 peak times this GPU's measured MMA ratio for
+        # the dtype, in place of the nominal ratio
+        mr = MMA_RATES["ratio_to_bf16"][kind]
+        out["measured_mma_ratio"] = mr
+        out["peak_measured_ratio"] = round(base * mr, 1)
+        out["frac_of_measured_ratio_peak"] = round(achieved / (base * mr), 4)
+        if peaks.get("bf16_tflops_sustained"):
+            out["frac_of_measured_ratio_sustained"] = round(
+                achieved / (float(peaks["bf16_tflops_sustained"]) * mr), 4)
     # the other roofline too: the algorithmic bytes against the measured HBM
     # bandwidth, and the attainable rate min(peak, AI x bandwidth)
     hbm = float(peaks["hbm_gbs"])
@@ -603,6 +646,9 @@ def run_ours(args):
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
     peaks, peak_kind = load_peaks()
+    global MMA_RATES
+    if int(os.environ.get("RANK", "0")) == 0 and not args.no_others:
+        MMA_RATES = tensor_rates()
     import dense_gemm_preshuffle_gb300 as gp
     gp.load_library()
 
@@ -752,6 +798,8 @@ def run_ours(args):
                 epi[name] = {"unavailable": f"{type(e).__name__}: {e}"[:200]}
         out["epilogues"] = epi
         out["quantize"] = time_quantizers(args, pg, device, peaks, peak_kind)
+        if MMA_RATES is not None:
+            out["tensor_rates"] = MMA_RATES
     if rank == 0:
         if not args.no_cpu:
             out["cpu_baseline"] = cpu_baseline(args.workload)

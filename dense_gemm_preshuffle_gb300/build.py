@@ -4,7 +4,9 @@ Every ``csrc/*.cu`` file is compiled in parallel with one ``-gencode``
 (``arch=compute_103a,code=sm_103a``) into ``_lib/``, then linked into
 ``_lib/libgemm_preshuffle.so`` with the CUDA runtime linked statically.  The
 library therefore loads without a GPU or a driver, and it needs libcuda only
-on its first CUDA call.
+on its first CUDA call.  ``rates/mma_rate.cu``, the tensor-pipe rate probe the
+benchmark runs for its FP8 and MXFP4 roofline denominators, is built beside
+it as the executable ``_lib/mma_rate``.
 """
 from __future__ import annotations
 
@@ -18,6 +20,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(OUT_DIR, "libgemm_preshuffle.so")
+RATES_SRC = os.path.join(HERE, "rates", "mma_rate.cu")
+RATES_BIN = os.path.join(OUT_DIR, "mma_rate")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--use_fast_math",
          "-Xptxas", "-warn-spills"]
@@ -43,13 +47,13 @@ def _sources():
 def _deps():
     return sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cuh")) +
                   glob.glob(os.path.join(CSRC, "*.h")) +
-                  glob.glob(os.path.join(HERE, "..", "include", "*.h")))
+                  glob.glob(os.path.join(HERE, "..", "include", "*.h")) + [RATES_SRC])
 
 
 def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+    if not os.path.exists(LIB) or not os.path.exists(RATES_BIN):
         return False
-    t = os.path.getmtime(LIB)
+    t = min(os.path.getmtime(LIB), os.path.getmtime(RATES_BIN))
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
@@ -73,8 +77,18 @@ def build(verbose: bool = False, force: bool = False, extra_flags=()) -> str:
             print(r.stdout + r.stderr, flush=True)
         return obj
 
-    with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
+    def compile_rates():
+        tmp_bin = RATES_BIN + f".tmp{os.getpid()}"
+        cmd = [nvcc, *ARCH, "-O3", "-std=c++17", RATES_SRC, "-o", tmp_bin]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc failed on {RATES_SRC}:\n{r.stdout}\n{r.stderr}")
+        os.replace(tmp_bin, RATES_BIN)
+
+    with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs) + 1)) as ex:
+        rates = ex.submit(compile_rates)
         objs = list(ex.map(compile_one, srcs))
+        rates.result()
     tmp = LIB + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", *objs, "-o", tmp]
     if verbose:
