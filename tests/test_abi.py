@@ -23,6 +23,12 @@ def test_exports_every_declared_symbol(lib):
         assert hasattr(lib, n), n
 
 
+def test_rate_probe_is_built(lib):
+    """build() also compiles the tensor-pipe rate probe the bench runs."""
+    import os
+    assert os.access(build.RATES_BIN, os.X_OK), build.RATES_BIN
+
+
 def test_status_strings(lib):
     for code in range(8):
         assert gp.gemm_status_string(code).startswith("GP_")
