@@ -600,7 +600,7 @@ __global__ void __launch_bounds__(F4Cfg<PAIR>::THREADS, 1)
         if (lane == 0) release();
       }
     }
-    if (lane == 0) bulk_wait_group<0>();
+    if (lane == 0) bulk_wait_group_read<0>();  // staging read; the writes complete with the grid
   }
 
   tc_fence_before();

@@ -32,11 +32,13 @@
 //     the result does not depend on which half finishes first), applies the
 //     scales / bias / activation, rounds, and stores through a swizzled
 //     staging tile with TMA.
-// Every wait is bounded.  Two cluster barriers end the kernel: after the
-// first, every copy that will ever be issued has been issued; a CTA whose
-// wait for its peer's partial gave up waits for it once more (bounded), and
-// after the second no copy reads or writes a CTA's shared memory any more.
-// The TMEM columns are then freed by both CTAs of each pair.
+// Every wait is bounded.  A cluster barrier ends the kernel: after it every
+// copy that will ever be issued has been issued, and when every partial has
+// landed, no copy reads or writes a CTA's shared memory any more.  If any
+// epilogue warp gave up on its peer's partial it marks all four CTAs before
+// the barrier; then a CTA that gave up waits for the partial once more
+// (bounded) and a second barrier follows.  The TMEM columns are then freed
+// by both CTAs of each pair.
 //
 // KIND as in the tile kernel: 0 = bf16, 1 = e4m3, 2 = fp16.
 #include <cstdlib>
@@ -91,6 +93,7 @@ __global__ void __launch_bounds__(XP_THREADS, 1)
   uint64_t* drain = xrecv + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile uint32_t* fail = reinterpret_cast<volatile uint32_t*>(abort_flag + 1);  // set by any CTA of the cluster
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -113,7 +116,7 @@ __global__ void __launch_bounds__(XP_THREADS, 1)
     uint32_t dyn, ncta;
     asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
     asm("mov.u32 %0, %%cluster_nctarank;" : "=r"(ncta));
-    const uint32_t need = (uint32_t)(reinterpret_cast<const volatile uint8_t*>(abort_flag + 1) - smem_raw);
+    const uint32_t need = (uint32_t)(reinterpret_cast<const volatile uint8_t*>(fail + 1) - smem_raw);
     if (ncta != 4 || (int)(blockIdx.x >> 2) >= p.num_tiles || p.ktiles < 2 || need > dyn ||
         (int)blockDim.x != XP_THREADS) {
       if (threadIdx.x == 0) atomicOr(p.status, ST_BAD_LAUNCH);
@@ -134,6 +137,7 @@ __global__ void __launch_bounds__(XP_THREADS, 1)
     mbar_init(xrecv, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
+    *fail = 0;
     fence_mbar_init();
     // the K peer's eight copies of 8 KiB complete this barrier's only phase
     mbar_arrive_expect_tx(xrecv, (uint32_t)(XP_EPI_WARPS * XP_SLOT));
@@ -356,7 +360,7 @@ __global__ void __launch_bounds__(XP_THREADS, 1)
         if (lane == 0 && row0 < p.M) {
           tma_store_2d(&tmC, n0, row0, stg);
           bulk_commit_group();
-          bulk_wait_group<0>();
+          bulk_wait_group_read<0>();  // the staging tile is read; the writes complete with the grid
         }
         __syncwarp();
       }
@@ -365,15 +369,24 @@ __global__ void __launch_bounds__(XP_THREADS, 1)
     }
   }
 
+  // A warp that gave up on its peer's partial marks all four CTAs, so that
+  // after the barrier every CTA of the cluster takes the same path.
+  if (!bad && warp >= 2 && !recv_ok && lane == 0)
+    for (uint32_t r = 0; r < 4; ++r) st_shared_cluster_u32(mapa_shared(smem_u32((const void*)fail), r), 1u);
   tc_fence_before();
   cluster_sync_all();  // every copy that will be issued has been issued
-  if (!bad && warp >= 2 && !recv_ok) {
-    // this CTA gave up on its peer's partial: let any copy already issued
-    // into its ring land before the peer or this CTA may exit
-    volatile int never = 0;
-    wait_bounded(xrecv, 0, &never, p.status, ST_TIMEOUT_DRAIN, limit);
+  // When every partial has landed, every copy between the CTAs is complete
+  // (a copy's arrival on its destination's barrier follows its last read of
+  // the source): no CTA's shared memory is touched by another after this.
+  if (*fail != 0) {
+    if (!bad && warp >= 2 && !recv_ok) {
+      // this CTA gave up on its peer's partial: let any copy already issued
+      // into its ring land before the peer or this CTA may exit
+      volatile int never = 0;
+      wait_bounded(xrecv, 0, &never, p.status, ST_TIMEOUT_DRAIN, limit);
+    }
+    cluster_sync_all();  // no copy touches any CTA's shared memory after this
   }
-  cluster_sync_all();  // no copy touches any CTA's shared memory after this
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc_pair<XP_TMEM_COLS>(tmem_base);

@@ -455,6 +455,10 @@ __device__ __forceinline__ uint32_t ld_shared_cluster_u32(uint32_t caddr) {
   return v;
 }
 
+__device__ __forceinline__ void st_shared_cluster_u32(uint32_t caddr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(caddr), "r"(v) : "memory");
+}
+
 // Arrive on `bar` once every previously issued tcgen05 op of this thread completes.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
