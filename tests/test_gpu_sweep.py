@@ -9,6 +9,13 @@
   process): random M (129-1024), N (multiples of 256 up to 1536) and K
   (any number of 128-byte K tiles from 2 to 80), BF16 / FP16 / E4M3.
   Within the float bound.
+* The library's own choice of float kernel (128 x 128 or 128 x 256 tiles,
+  2-CTA pairs, split-K clusters, the two-pair K split): random M (1-1500),
+  N (multiples of 128 up to 3072) and K (1-40 K tiles of 128 bytes),
+  BF16 / FP16 / E4M3.  Within the float bound.
+* MXFP4 (single-CTA 128 x 256 tiles for M <= 128, 2-CTA pairs above):
+  random M (1-700), N (multiples of 256 up to 1536) and K (multiples of
+  256 up to 6144).  Within the float bound.
 
 The shapes come from a fixed seed, so every run checks the same ones.
 """
@@ -126,3 +133,71 @@ def test_two_pair_random_shapes(lib, tmp_path):
         assert not np.isnan(c).any(), f"{dtype} {M}x{N}x{K}: outputs left unwritten"
         err = oracle.max_rel_err(c, ref)
         assert err <= oracle.FLOAT_TOL, f"{dtype} {M}x{N}x{K}: max rel err {err:.3e}"
+
+
+def _dev(x):
+    if x is None:
+        return None
+    if x.dtype == np.uint16:
+        x = x.view(np.int16)
+    return torch.from_numpy(np.ascontiguousarray(x)).cuda()
+
+
+def _float_result(c, dtype):
+    return c.view(torch.float16 if dtype == "fp16" else torch.bfloat16).float().cpu().numpy().astype(np.float64)
+
+
+def dispatch_shapes(n=12):
+    rng = np.random.default_rng(6104)
+    out = []
+    for i in range(n):
+        dtype = ("bf16", "e4m3", "fp16")[i % 3]
+        M = int(rng.integers(1, 1501))
+        N = 128 * int(rng.integers(1, 25))
+        ktiles = int(rng.integers(1, 41))
+        K = ktiles * (128 if dtype == "e4m3" else 64)
+        out.append((dtype, M, N, K))
+    return out
+
+
+@pytest.mark.parametrize("case", dispatch_shapes(), ids=lambda c: f"{c[0]}-{c[1]}x{c[2]}x{c[3]}")
+def test_float_random_shapes_default_dispatch(lib, case):
+    dtype, M, N, K = case
+    ops = inputs.make_operands(dtype, M, N, K, seed=190 + M % 97)
+    A, B, sa, sb = _dev(ops.a), _dev(ops.b), _dev(ops.scale_a), _dev(ops.scale_b)
+    Bp = gp.preshuffle_b(B, dtype)
+    C = torch.full((M, N), float("nan"), dtype=torch.float16 if dtype == "fp16" else torch.bfloat16, device="cuda")
+    gp.matmul(A, Bp, dtype, N, K, scale_a=sa, scale_b=sb, out=C)
+    torch.cuda.synchronize()
+    assert gp.gemm_last_device_status() == 0
+    c = _float_result(C, dtype)
+    assert not np.isnan(c).any(), "outputs left unwritten"
+    err = oracle.max_rel_err(c, oracle.gemm_dequantized(ops))
+    assert err <= oracle.FLOAT_TOL, f"max rel err {err:.3e}"
+
+
+def mxfp4_shapes(n=10):
+    rng = np.random.default_rng(7311)
+    out = []
+    for i in range(n):
+        M = int(rng.integers(1, 129)) if i % 3 == 0 else int(rng.integers(129, 701))
+        N = 256 * int(rng.integers(1, 7))
+        K = 256 * int(rng.integers(1, 25))
+        out.append(("e2m1", M, N, K))
+    return out
+
+
+@pytest.mark.parametrize("case", mxfp4_shapes(), ids=lambda c: f"{c[0]}-{c[1]}x{c[2]}x{c[3]}")
+def test_mxfp4_random_shapes(lib, case):
+    dtype, M, N, K = case
+    ops = inputs.make_operands(dtype, M, N, K, seed=230 + M % 89)
+    A, B, ea, eb = _dev(ops.a), _dev(ops.b), _dev(ops.scale_a), _dev(ops.scale_b)
+    Bp = gp.preshuffle_b(B, dtype, B_scales=eb)
+    C = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    gp.matmul(A, Bp, dtype, N, K, scale_a=ea, out=C)
+    torch.cuda.synchronize()
+    assert gp.gemm_last_device_status() == 0
+    c = _float_result(C, dtype)
+    assert not np.isnan(c).any(), "outputs left unwritten"
+    err = oracle.max_rel_err(c, oracle.gemm_dequantized(ops))
+    assert err <= oracle.FLOAT_TOL, f"max rel err {err:.3e}"
